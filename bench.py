@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of one step of the path on the 4M-token workload (default).
+
+A step is one pass of the whole hot path over one chunk with every input
+resident in HBM: page representatives of all pages -> Top-K selection ->
+sparse attention forward -> sparse attention backward with in-place paged
+dK/dV.  The metric is the method's: sparse-attention fwd+bwd TFLOP/s, counting
+14 * D * Hq flops per unmasked (query, key) pair, with tokens/s per chunk and
+the fraction of the bf16 tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...    # the CPU float64 oracle, bounded sample
+
+For N > 1 (torchrun), every rank runs an independent replica on its own GPU
+(the path has no exchange step); value = all ranks' work / the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_sparse_attention_oomb_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "sparse attn fwd+bwd TFLOP/s and tokens/s per chunk at 256K–4M ctx; % of bf16 peak"
+DEFAULT_WORKLOAD = "qwen7b_ctx4m_k128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def pairs_per_head(wl, rows=None):
+    """Unmasked (query, key) pairs of one query head for the chunk (or its
+    first `rows` rows): every selected key, plus the causal own keys."""
+    c = wl.chunk_len if rows is None else rows
+    return wl.n_sel * wl.page_size * c + c * (c + 1) // 2
+
+
+def attn_flops(wl, rows=None):
+    return 14.0 * wl.head_dim * wl.num_q_heads * pairs_per_head(wl, rows)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+REASON_COLS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", "-i", str(self.gpu),
+               "--query-gpu=clocks.sm,clocks.max.sm,power.draw,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(REASON_COLS, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, dev):
+    from paged_sparse_attention_oomb_gb300 import oomb
+
+    wl = WORKLOADS[args.workload]
+    torch.cuda.set_device(dev)
+    x = make_inputs(wl, seed=0, device=dev)
+    kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, torch.zeros_like(x.k_pool),
+                      torch.zeros_like(x.v_pool))
+    hkv, d, c, hq = wl.num_kv_heads, wl.head_dim, wl.chunk_len, wl.num_q_heads
+    n_sel = wl.n_sel
+    reps = torch.empty((wl.num_pages, hkv, d), dtype=torch.float32, device=dev)
+    sel = torch.empty((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
+    o = torch.empty_like(x.q)
+    lse = torch.empty((hq, c), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(x.q)
+    ws_r = oomb.workspace(oomb.OOMB_OP_PAGE_REPS, kv)
+    ws_s = oomb.workspace(oomb.OOMB_OP_SELECT_TOPK, kv, hq, c, wl.top_k)
+    ws_f = oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv, hq, c)
+    ws_b = oomb.workspace(oomb.OOMB_OP_ATTN_BWD, kv, hq, c)
+    stream = torch.cuda.current_stream()
+    names = ["page_reps", "select_topk", "attn_fwd", "attn_bwd"]
+
+    def step(q, dout, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        oomb.oomb_page_reps(kv, 0, wl.num_pages, reps, ws_r, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        oomb.oomb_select_topk(q, wl.start, reps, kv, wl.top_k, sel, ws_s, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        oomb.oomb_sparse_attn_fwd(q, kv, sel, n_sel, wl.start, o, lse, ws_f, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        oomb.oomb_sparse_attn_bwd(q, o, dout, lse, kv, sel, n_sel, wl.start, dq, ws_b,
+                                  stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step(x.q, x.do)
+    torch.cuda.synchronize()
+    for w in (ws_r, ws_s, ws_f, ws_b):
+        code, where, blk = oomb.oomb_device_status(w)
+        if code != 0:
+            raise RuntimeError(f"device status {oomb.oomb_status_string(code)} at {where}/{blk}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    phys = vis.split(",")[dev.index] if vis and vis.split(",")[0].isdigit() else dev.index
+    with ClockSampler(phys) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(x.q, x.do, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    per = {n: statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps))
+           for k, n in enumerate(names)}
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the same C ABI calls with host buffers: per step the
+    # chunk's queries and output grads come from pinned host memory and the
+    # outputs (O, LSE, dQ) go back to pinned host memory, inside the timed region
+    q_h = x.q.cpu().pin_memory()
+    do_h = x.do.cpu().pin_memory()
+    o_h = torch.empty_like(q_h).pin_memory()
+    dq_h = torch.empty_like(q_h).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d, do_d = torch.empty_like(x.q), torch.empty_like(x.do)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 2)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        q_d.copy_(q_h, non_blocking=True)
+        do_d.copy_(do_h, non_blocking=True)
+        step(q_d, do_d)
+        o_h.copy_(o, non_blocking=True)
+        dq_h.copy_(dq, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = q_h.numel() * q_h.element_size() + do_h.numel() * do_h.element_size()
+    d2h = (o_h.numel() * o_h.element_size() + dq_h.numel() * dq_h.element_size()
+           + lse_h.numel() * lse_h.element_size())
+    for w in (ws_r, ws_s, ws_f, ws_b):
+        code, where, blk = oomb.oomb_device_status(w)
+        if code != 0:
+            raise RuntimeError(f"device status {oomb.oomb_status_string(code)} at {where}/{blk}")
+
+    flops = attn_flops(wl)
+    pk, pk_src = peaks()
+    pairs_total = pairs_per_head(wl) * hq
+    bwd_flops = 10.0 * d * pairs_total
+    fwd_flops = 4.0 * d * pairs_total
+    bytes_reps = wl.num_pages * hkv * wl.page_size * d * 2 + wl.num_pages * hkv * d * 4
+    bytes_sel = c * hq * d * 2 + wl.num_candidates * hkv * d * 4 + hkv * n_sel * 4
+    peak_t = pk["bf16_tflops_sustained"]
+    peak_b = pk["hbm_gbs"]
+    kern = {
+        "page_reps": {"ms": per["page_reps"], "GB/s": bytes_reps / per["page_reps"] / 1e6,
+                      "frac_hbm": bytes_reps / per["page_reps"] / 1e6 / peak_b},
+        "select_topk": {"ms": per["select_topk"], "GB/s": bytes_sel / per["select_topk"] / 1e6,
+                        "frac_hbm": bytes_sel / per["select_topk"] / 1e6 / peak_b},
+        "attn_fwd": {"ms": per["attn_fwd"], "TFLOP/s": fwd_flops / per["attn_fwd"] / 1e9,
+                     "frac_bf16": fwd_flops / per["attn_fwd"] / 1e9 / peak_t},
+        "attn_bwd": {"ms": per["attn_bwd"], "TFLOP/s": bwd_flops / per["attn_bwd"] / 1e9,
+                     "frac_bf16": bwd_flops / per["attn_bwd"] / 1e9 / peak_t},
+    }
+    achieved = bwd_flops / per["attn_bwd"] / 1e9
+    res = {
+        "metric": METRIC,
+        "value": world * flops / ms / 1e9,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; clustered page keys, N(0,1) values/queries/grads)",
+        "config": {"workload": wl.name, "context": wl.context, "page_size": wl.page_size,
+                   "chunk_len": c, "chunk_start": wl.start, "top_k": wl.top_k,
+                   "num_q_heads": hq, "num_kv_heads": hkv, "head_dim": d,
+                   "page_table": "shuffled" if wl.shuffled else "identity",
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: each step streams the whole K pool"},
+        "tokens_per_s_per_chunk": world * c / (ms / 1e3),
+        "frac_of_bf16_peak": flops / ms / 1e9 / peak_t,
+        "kernels": kern,
+        "roofline": {"kernel": "oomb_sparse_attn_bwd (delta prep + sparse_attn_bwd_kernel + dq convert)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak_t,
+                     "peak_source": f"{pk_src} bf16_tflops_sustained", "unit": "TFLOP/s",
+                     "frac": achieved / peak_t, "traffic": None},
+        "e2e": {"value": world * flops / e2e_ms / 1e9, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (1 + 3 + 1 + 3),
+        "clocks": clk.summary(),
+    }
+    return res, x, wl
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def oracle_setup(wl, x=None):
+    """Host copies of what the oracle needs and the oracle's own selection."""
+    import oracle
+    from paged_sparse_attention_oomb_gb300.workloads import to_numpy64
+    if x is None:
+        dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+        x = make_inputs(wl, seed=0, device=dev)
+    pt = x.page_table.cpu().long()
+    k_host = x.k_pool.cpu()
+    reps = np.concatenate([oracle.page_reps(k_host[pt[b:b + 512]].float().numpy(),
+                                            np.arange(min(512, wl.num_pages - b)))
+                           for b in range(0, wl.num_pages, 512)])
+    q = to_numpy64(x.q)
+    do = to_numpy64(x.do)
+    sel = oracle.select_topk(oracle.page_scores(oracle.query_summary(q, wl.num_kv_heads), reps,
+                                                wl.num_candidates), wl.top_k)
+    own = np.arange(wl.start // wl.page_size, (wl.start + wl.chunk_len) // wl.page_size)
+    need = np.unique(np.concatenate([sel.reshape(-1), own]))
+    slots = pt.numpy()[need]
+    kc = k_host[torch.as_tensor(slots)].float().numpy()
+    vc = x.v_pool.cpu()[torch.as_tensor(slots)].float().numpy()
+    ptc = np.full(wl.num_pages, -1, np.int64)
+    ptc[need] = np.arange(need.size)
+    return dict(q=q, do=do, sel=sel, kc=kc, vc=vc, ptc=ptc)
+
+
+def oracle_step(wl, st, rows):
+    """fwd + bwd of the oracle for the first `rows` rows of the chunk (all heads)."""
+    import oracle
+    q, do = st["q"][:rows], st["do"][:rows]
+    o, lse = oracle.attn_fwd(q, st["kc"], st["vc"], st["ptc"], st["sel"], wl.start, wl.page_size)
+    shp = (st["kc"].shape[0],) + st["kc"].shape[1:]
+    oracle.attn_bwd(q, st["kc"], st["vc"], st["ptc"], st["sel"], wl.start, wl.page_size, o, lse,
+                    do, dk_acc=np.zeros(shp), dv_acc=np.zeros(shp), acc_rows=st["ptc"])
+
+
+def cpu_baseline(wl, st, rows, reps=1):
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(wl, st, rows)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": attn_flops(wl, rows) / dt / 1e12, "unit": "TFLOP/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {rows} chunk rows, all {wl.num_q_heads} heads, fwd+bwd "
+                      f"(float64 NumPy); oracle's own selection made outside the timed part",
+            "seconds": dt}
+
+
+def run_reference(args, rank, world):
+    wl = WORKLOADS[args.workload]
+    if rank != 0:
+        return None
+    st = oracle_setup(wl)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_step(wl, st, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(wl, st, rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    val = attn_flops(wl, rows) / dt / 1e12
+    cb = {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+          "sample": f"first {rows} chunk rows, all heads, fwd+bwd per step (float64 NumPy)"}
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": wl.name, "rows_per_step": rows},
+            "cpu_baseline": cb,
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+    else:
+        dev = torch.device("cuda", local)
+        res, x, wl = run_ours(args, rank, world, dev)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            st = oracle_setup(wl, x)
+            del x
+            torch.cuda.empty_cache()
+            res["cpu_baseline"] = cpu_baseline(wl, st, args.cpu_rows)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * oomb.h -- C ABI of liboomb: page-level sparse causal attention of one query
+ * chunk against a paged KV cache, forward and backward, on one GB300 (sm_103a).
+ *
+ * Method: "Out of the Memory Barrier: A Highly Memory Efficient Training
+ * System for LLMs with Million-Token Contexts" (gist.science summary of arXiv
+ * 2602.02108), technical summary section 2 "Methodology":
+ *   - "Paged Memory Management": the KV cache AND its gradients are allocated
+ *     per page; gradients are accumulated in place, outside autograd.
+ *   - "Page-level Sparse Attention": Top-K page retrieval; for dense-attention
+ *     models the forward picks the most relevant key pages from
+ *     representative vectors and the backward reuses that choice.
+ *   - "Specialized Kernels": KV-cache operations are kept out of the autograd
+ *     graph (this ABI has no autograd at all).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory; scratch comes from the caller's workspace
+ *     `ws` (size from oomb_workspace_bytes, 256-byte aligned, zero-filled
+ *     before its first use; the library leaves its counters at zero after
+ *     every call that completes).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on it, except oomb_validate_page_table and
+ *     oomb_device_status, which synchronise the stream.
+ *   - Argument errors are detected on the host and returned before anything
+ *     is launched (OOMB_ERR_INVALID_ARG / OOMB_ERR_UNSUPPORTED, with a message
+ *     from oomb_last_error()).  Errors found on the device (a bounded wait that
+ *     timed out, an index out of range) are recorded in the status word at the
+ *     start of `ws` and read with oomb_device_status.  No call traps or
+ *     asserts on the device.
+ *   - Tensor layouts (row-major, innermost last):
+ *       K/V pools and dK/dV pools  [num_slots][Hkv][P][D]   (one page of one
+ *                                   KV head is a contiguous P x D tile)
+ *       page_table                 int32 [num_pages], logical page -> slot,
+ *                                   injective, every entry < num_slots
+ *       q, o, dout, dq             [chunk_len][Hq][D]
+ *       lse                        float [Hq][chunk_len], natural log
+ *       reps                       float [num_pages][Hkv][D], logical order
+ *       sel                        int32 [Hkv][n_sel], ascending, unique
+ *   - GQA: query head h uses KV head h / (Hq / Hkv).
+ *   - Own pages of a chunk: logical pages [chunk_start/P, (chunk_start +
+ *     chunk_len)/P).  Candidates: logical pages [0, chunk_start/P).
+ *   - Supported: bf16 with D = 128 and P in {16, 32, 64, 128}; fp32 with
+ *     D = 64 and P in {16, 32, 64, 128}.  chunk_start and chunk_len are
+ *     multiples of P, chunk_len >= P.
+ */
+#ifndef OOMB_H
+#define OOMB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OOMB_OK = 0,
+  OOMB_ERR_INVALID_ARG = 1,   /* bad pointer, shape, alignment or index  */
+  OOMB_ERR_UNSUPPORTED = 2,   /* valid request this build does not serve */
+  OOMB_ERR_CUDA = 3,          /* a CUDA runtime call failed              */
+  OOMB_ERR_TIMEOUT = 4,       /* a device-side bounded wait gave up      */
+  OOMB_ERR_DEVICE_BOUNDS = 5  /* a device-side index check failed        */
+} oomb_status;
+
+typedef enum { OOMB_BF16 = 0, OOMB_FP32 = 1 } oomb_dtype;
+
+/* The paged KV cache and its paged gradient buffers (Paged Memory Management
+ * item).  dk/dv may be NULL for forward-only use. */
+typedef struct {
+  void *k, *v;
+  void *dk, *dv;
+  const int32_t *page_table;
+  int32_t num_pages;
+  int32_t num_slots;
+  int32_t page_size;     /* P */
+  int32_t num_kv_heads;  /* Hkv */
+  int32_t head_dim;      /* D */
+  int32_t dtype;         /* oomb_dtype of k, v, dk, dv, q, o, dout, dq */
+} oomb_paged_kv;
+
+typedef enum {
+  OOMB_OP_VALIDATE = 0,
+  OOMB_OP_PAGE_REPS = 1,
+  OOMB_OP_SELECT_TOPK = 2,
+  OOMB_OP_ATTN_FWD = 3,
+  OOMB_OP_ATTN_BWD = 4
+} oomb_op;
+
+/* Bytes of workspace `op` needs for these shapes (>= 256: the status block).
+ * top_k is used by OOMB_OP_SELECT_TOPK only.  Returns 0 for an unknown op. */
+size_t oomb_workspace_bytes(int op, const oomb_paged_kv *kv, int32_t num_q_heads,
+                            int32_t chunk_len, int32_t top_k);
+
+/* Host-only check of a host copy of a page table: every entry in
+ * [0, num_slots) and no slot used twice (a shared slot would make two
+ * backward tiles update the same gradient page).  Paged Memory Management. */
+oomb_status oomb_validate_page_table_host(const int32_t *page_table, int32_t num_pages,
+                                          int32_t num_slots);
+
+/* The same check on the device copy kv->page_table, using ws as a slot
+ * bitmap.  Synchronises `stream`.  Returns OOMB_ERR_INVALID_ARG if the table
+ * is out of range or not injective. */
+oomb_status oomb_validate_page_table(const oomb_paged_kv *kv, void *ws, size_t ws_bytes,
+                                     void *stream);
+
+/* Step 1 -- representative vector of each page (Page-level Sparse Attention
+ * item: "representative vectors"; reading: the fp32 mean of the page's P
+ * keys, per KV head).  For logical pages [first_page, first_page + n_pages):
+ *   reps[l][g][d] = (1/P) sum_t K[page_table[l]][g][t][d]     (fp32 accumulate)
+ * reps points at the row of logical page 0 ([num_pages][Hkv][D]); only the
+ * requested rows are written.  ws: oomb_workspace_bytes(PAGE_REPS) (status
+ * word only). */
+oomb_status oomb_page_reps(const oomb_paged_kv *kv, int32_t first_page, int32_t n_pages,
+                           float *reps, void *ws, size_t ws_bytes, void *stream);
+
+/* Step 2 -- Top-K page selection per (chunk, KV head) (Page-level Sparse
+ * Attention item: "Top-K page retrieval").  With qbar[g] the fp32 mean of q
+ * over the chunk's tokens and the heads of group g:
+ *   score[g][l] = qbar[g] . reps[l][g]      for candidates l < chunk_start/P
+ * keeps the n_sel = min(top_k, chunk_start/P) highest scores per KV head;
+ * equal scores go to the lower page index; sel[g][0..n_sel) is written in
+ * ascending page order.  scores_opt, if not NULL, receives float
+ * [Hkv][num_pages] (non-candidates = -inf).  Deterministic: the fp32
+ * reductions run in a fixed order.  ws: oomb_workspace_bytes(SELECT_TOPK). */
+oomb_status oomb_select_topk(const void *q, int32_t num_q_heads, int32_t chunk_len,
+                             int32_t chunk_start, const float *reps, const oomb_paged_kv *kv,
+                             int32_t top_k, int32_t *sel, float *scores_opt, void *ws,
+                             size_t ws_bytes, void *stream);
+
+/* Step 3 -- sparse attention forward (Page-level Sparse Attention item).
+ * For query head h (KV head g) and chunk row t (position p = chunk_start+t)
+ * the keys are all tokens of the n_sel pages sel[g][*] plus the chunk's own
+ * tokens at positions <= p:
+ *   o[t][h] = softmax_k(scale * q[t][h] . k) v,  lse[h][t] = log sum_k exp(...)
+ * scale <= 0 selects 1/sqrt(D).  bf16: tcgen05 tensor cores, fp32
+ * accumulation, o rounded once to bf16.  fp32: CUDA-core FMA.
+ * sel must be the same array later passed to the backward (the backward
+ * reuses the forward's choice). */
+oomb_status oomb_sparse_attn_fwd(const void *q, const oomb_paged_kv *kv, const int32_t *sel,
+                                 int32_t n_sel, int32_t num_q_heads, int32_t chunk_len,
+                                 int32_t chunk_start, float scale, void *o, float *lse, void *ws,
+                                 size_t ws_bytes, void *stream);
+
+/* Step 4 -- sparse attention backward with in-place paged gradient
+ * accumulation (Paged Memory Management: gradients of the KV cache are
+ * paged and accumulated in place; Page-level Sparse Attention: the selection
+ * of the forward is reused).  Recomputes P = exp(scale q.k - lse); with
+ * Delta[t][h] = dout[t][h] . o[t][h]:
+ *   dq[t][h]  = scale sum_k P (dP - Delta) k              (written)
+ *   dK[slot]  += scale sum_{t,h in group} P (dP - Delta) q   (read-add-write)
+ *   dV[slot]  += sum_{t,h in group} P dout                    (read-add-write)
+ * for the slots of the selected and own pages only; each of those slots is
+ * rounded once per call.  kv->dk and kv->dv must be set.
+ * ws: oomb_workspace_bytes(ATTN_BWD) (holds Delta and an fp32 dq accumulator). */
+oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *dout, const float *lse,
+                                 const oomb_paged_kv *kv, const int32_t *sel, int32_t n_sel,
+                                 int32_t num_q_heads, int32_t chunk_len, int32_t chunk_start,
+                                 float scale, void *dq, void *ws, size_t ws_bytes, void *stream);
+
+/* Reads and clears the device status word at the start of ws (synchronises
+ * `stream`).  Returns OOMB_OK, OOMB_ERR_TIMEOUT or OOMB_ERR_DEVICE_BOUNDS;
+ * info (optional, 2 ints) receives {where, block} of the first error. */
+oomb_status oomb_device_status(void *ws, void *stream, int32_t *info);
+
+/* Upper bound, in nanoseconds, of every device-side wait (default 2e9).
+ * Process-wide; for tests of the timeout path.  0 restores the default. */
+void oomb_set_wait_limit_ns(uint64_t ns);
+
+/* Debug: a one-thread kernel that waits on a flag in ws nothing ever sets,
+ * bounded by the wait limit; records OOMB_ERR_TIMEOUT in the status word. */
+oomb_status oomb_debug_wait_unset_flag(void *ws, size_t ws_bytes, void *stream);
+
+const char *oomb_status_string(int status);
+
+/* Message of the last host-side error of the calling thread ("" if none). */
+const char *oomb_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OOMB_H */

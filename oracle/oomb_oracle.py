@@ -48,6 +48,7 @@ __all__ = [
     "attn_fwd",
     "attn_bwd",
     "attn_bwd_pages",
+    "attn_dq_rows",
     "dense_causal_reference",
     "chunk_recurrent_grads",
 ]
@@ -201,7 +202,7 @@ def attn_fwd(q, k_pool, v_pool, page_table, sel, chunk_start, page_size, scale=N
 
 
 def attn_bwd(q, k_pool, v_pool, page_table, sel, chunk_start, page_size, o, lse, do,
-             scale=None, dk_acc=None, dv_acc=None, row_block=1024):
+             scale=None, dk_acc=None, dv_acc=None, row_block=1024, acc_rows=None):
     """Backward of the sparse attention with the same selection as the forward.
 
     Recomputes P = exp(s - lse) from the saved LSE, then with
@@ -213,7 +214,9 @@ def attn_bwd(q, k_pool, v_pool, page_table, sel, chunk_start, page_size, o, lse,
 
     dK/dV are added in place into ``dk_acc``/``dv_acc`` (float64, indexed by
     LOGICAL page ``[num_pages, Hkv, P, D]``; created if None), which is how
-    gradients reach the paged buffers across chunks.  Returns
+    gradients reach the paged buffers across chunks.  ``acc_rows`` (optional)
+    maps a logical page to its row of the accumulators, for callers that keep
+    accumulators for the touched pages only.  Returns
     ``(dq [C, Hq, D], dk_acc, dv_acc)``.
     """
     c, hq, d = q.shape
@@ -249,6 +252,8 @@ def attn_bwd(q, k_pool, v_pool, page_table, sel, chunk_start, page_size, o, lse,
                 dq[rr, h] = scale * (ds @ kset)
                 dks += scale * (ds.T @ qh)
         pages = kpos // page_size
+        if acc_rows is not None:
+            pages = np.asarray(acc_rows)[pages]
         offs = kpos % page_size
         np.add.at(dk_acc, (pages, g, offs), dks)
         np.add.at(dv_acc, (pages, g, offs), dvs)
@@ -291,6 +296,36 @@ def attn_bwd_pages(q, k_pool, v_pool, page_table, sel, chunk_start, page_size, o
             dks += scale * (ds.T @ qh)
     n = pages.shape[0]
     return dks.reshape(n, page_size, d), dvs.reshape(n, page_size, d)
+
+
+def attn_dq_rows(q, k_pool, v_pool, page_table, sel, chunk_start, page_size, o_rows, lse_rows,
+                 do, rows, scale=None):
+    """dQ of a few chunk rows only (every head), same arithmetic as :func:`attn_bwd`.
+
+    ``o_rows [len(rows), Hq, D]`` and ``lse_rows [Hq, len(rows)]`` are the
+    forward outputs of those rows.  Returns float64 ``[len(rows), Hq, D]``.
+    """
+    c, hq, d = q.shape
+    hkv = k_pool.shape[1]
+    grp = hq // hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows = np.asarray(rows)
+    qpos = chunk_start + rows
+    dq = np.zeros((rows.shape[0], hq, d))
+    for g in range(hkv):
+        kpos = key_positions(sel[g], chunk_start, c, page_size)
+        kset = _gather(k_pool, page_table, kpos, g, page_size)
+        vset = _gather(v_pool, page_table, kpos, g, page_size)
+        for h in range(g * grp, (g + 1) * grp):
+            qh = q[rows, h].astype(np.float64)
+            doh = do[rows, h].astype(np.float64)
+            s, allowed = _scores(qh, kset, kpos, qpos, scale)
+            p = np.where(allowed, np.exp(s - lse_rows[h][:, None]), 0.0)
+            dp = doh @ vset.T
+            delta = (doh * o_rows[:, h]).sum(axis=1)
+            dq[:, h] = scale * ((p * (dp - delta[:, None])) @ kset)
+    return dq
 
 
 # ---------------------------------------------------------------------------

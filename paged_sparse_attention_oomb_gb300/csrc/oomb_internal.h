@@ -1,0 +1,79 @@
+// Internal interface between the C-ABI host layer (oomb_abi.cu) and the
+// kernel translation units.  Host-callable launchers only; plain pointers.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace oomb {
+
+// Workspace: a 256-byte status block first.
+//   int[0] status code (0 = ok), int[1] where, int[2] block
+//   int[16] qbar "last block" ticket counter (self-resetting)
+//   int[17] debug flag that nothing sets
+constexpr size_t kStatusBytes = 256;
+constexpr int kTicketIdx = 16;
+constexpr int kDebugFlagIdx = 17;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Where-codes recorded with a device error (status int[1]).
+enum Where : int {
+  kWhereReps = 10,
+  kWhereTopk = 20,
+  kWhereFwdProducer = 30,
+  kWhereFwdMma = 31,
+  kWhereFwdSoftmax = 32,
+  kWhereBwdProducer = 40,
+  kWhereBwdMma = 41,
+  kWhereBwdCompute = 42,
+  kWhereBwdEpilogue = 43,
+  kWhereFp32 = 50,
+  kWhereDebug = 90,
+};
+
+struct KvDesc {
+  const void* k;
+  const void* v;
+  void* dk;
+  void* dv;
+  const int32_t* page_table;
+  int num_pages, num_slots, page_size, hkv, head_dim;
+};
+
+// --- k_reps_select.cu
+cudaError_t launch_page_reps(const KvDesc& kv, bool bf16, int first_page, int n_pages,
+                             float* reps, int* status, cudaStream_t st);
+constexpr int kQbarBlocks = 152;
+size_t select_ws_bytes(int num_pages, int hkv, int head_dim);
+cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, int n_cand,
+                               const float* reps, int num_pages, int hkv, int head_dim, int top_k,
+                               int32_t* sel, float* scores_opt, void* ws, cudaStream_t st);
+cudaError_t launch_validate_page_table(const int32_t* pt, int num_pages, int num_slots,
+                                       uint32_t* bitmap, int* status, cudaStream_t st);
+cudaError_t launch_debug_wait(int* status, uint64_t limit_ns, cudaStream_t st);
+
+// --- k_attn_fp32.cu
+size_t fp32_bwd_ws_bytes(int hq, int chunk_len);
+cudaError_t launch_attn_fwd_fp32(const float* q, const KvDesc& kv, const int32_t* sel, int n_sel,
+                                 int hq, int chunk_len, int chunk_start, float scale, float* o,
+                                 float* lse, int* status, cudaStream_t st);
+cudaError_t launch_attn_bwd_fp32(const float* q, const float* o, const float* dout,
+                                 const float* lse, const KvDesc& kv, const int32_t* sel,
+                                 int n_sel, int hq, int chunk_len, int chunk_start, float scale,
+                                 float* dq, void* ws, cudaStream_t st);
+
+// --- k_attn_fwd_bf16.cu
+cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t* sel, int n_sel,
+                                 int hq, int chunk_len, int chunk_start, float scale, void* o,
+                                 float* lse, int* status, uint64_t wait_ns, cudaStream_t st);
+
+// --- k_attn_bwd_bf16.cu
+size_t bf16_bwd_ws_bytes(int hq, int chunk_len, int head_dim);
+cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* dout,
+                                 const float* lse, const KvDesc& kv, const int32_t* sel,
+                                 int n_sel, int hq, int chunk_len, int chunk_start, float scale,
+                                 void* dq, void* ws, uint64_t wait_ns, cudaStream_t st);
+
+}  // namespace oomb

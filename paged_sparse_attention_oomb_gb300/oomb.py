@@ -1,0 +1,237 @@
+"""Thin Python binding of liboomb (C ABI in include/oomb.h), same call names.
+
+Argument marshalling only: torch tensors are passed as device pointers with
+their sizes; every step of the path runs in liboomb's CUDA kernels.  The
+library is loaded from this package directory and an ``OombError`` is raised
+if it is missing -- there is no other implementation behind these calls.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liboomb.so")
+
+OOMB_OK, OOMB_ERR_INVALID_ARG, OOMB_ERR_UNSUPPORTED = 0, 1, 2
+OOMB_ERR_CUDA, OOMB_ERR_TIMEOUT, OOMB_ERR_DEVICE_BOUNDS = 3, 4, 5
+OOMB_BF16, OOMB_FP32 = 0, 1
+OOMB_OP_VALIDATE, OOMB_OP_PAGE_REPS, OOMB_OP_SELECT_TOPK = 0, 1, 2
+OOMB_OP_ATTN_FWD, OOMB_OP_ATTN_BWD = 3, 4
+
+EXPORTED = [
+    "oomb_workspace_bytes", "oomb_validate_page_table_host", "oomb_validate_page_table",
+    "oomb_page_reps", "oomb_select_topk", "oomb_sparse_attn_fwd", "oomb_sparse_attn_bwd",
+    "oomb_device_status", "oomb_set_wait_limit_ns", "oomb_debug_wait_unset_flag",
+    "oomb_status_string", "oomb_last_error",
+]
+
+
+class OombError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{_STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_STATUS_NAMES = {0: "OOMB_OK", 1: "OOMB_ERR_INVALID_ARG", 2: "OOMB_ERR_UNSUPPORTED",
+                 3: "OOMB_ERR_CUDA", 4: "OOMB_ERR_TIMEOUT", 5: "OOMB_ERR_DEVICE_BOUNDS"}
+
+
+class OombPagedKV(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+                ("dv", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load():
+    """Load liboomb.so (built in-tree by ``build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise OombError(-1, f"{LIB_PATH} is missing: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    kvp = ctypes.POINTER(OombPagedKV)
+    sig = {
+        "oomb_workspace_bytes": (sz, [ctypes.c_int, kvp, i32, i32, i32]),
+        "oomb_validate_page_table_host": (ctypes.c_int, [vp, i32, i32]),
+        "oomb_validate_page_table": (ctypes.c_int, [kvp, vp, sz, vp]),
+        "oomb_page_reps": (ctypes.c_int, [kvp, i32, i32, vp, vp, sz, vp]),
+        "oomb_select_topk": (ctypes.c_int, [vp, i32, i32, i32, vp, kvp, i32, vp, vp, vp, sz, vp]),
+        "oomb_sparse_attn_fwd": (ctypes.c_int, [vp, kvp, vp, i32, i32, i32, i32, ctypes.c_float,
+                                                vp, vp, vp, sz, vp]),
+        "oomb_sparse_attn_bwd": (ctypes.c_int, [vp, vp, vp, vp, kvp, vp, i32, i32, i32, i32,
+                                                ctypes.c_float, vp, vp, sz, vp]),
+        "oomb_device_status": (ctypes.c_int, [vp, vp, vp]),
+        "oomb_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+        "oomb_debug_wait_unset_flag": (ctypes.c_int, [vp, sz, vp]),
+        "oomb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "oomb_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(code):
+    if code != OOMB_OK:
+        raise OombError(code, load().oomb_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+
+
+@dataclass
+class PagedKV:
+    """The paged KV cache (and its paged gradient buffers) as torch tensors.
+
+    k, v, dk, dv: ``[num_slots, Hkv, P, D]``; page_table: int32 ``[num_pages]``
+    on the device (logical page -> slot).
+    """
+    k: torch.Tensor
+    v: torch.Tensor
+    page_table: torch.Tensor
+    dk: Optional[torch.Tensor] = None
+    dv: Optional[torch.Tensor] = None
+
+    def struct(self) -> OombPagedKV:
+        ns, hkv, p, d = self.k.shape
+        dt = OOMB_BF16 if self.k.dtype == torch.bfloat16 else OOMB_FP32
+        return OombPagedKV(self.k.data_ptr(), self.v.data_ptr(),
+                           self.dk.data_ptr() if self.dk is not None else None,
+                           self.dv.data_ptr() if self.dv is not None else None,
+                           self.page_table.data_ptr(), self.page_table.numel(), ns, p, hkv, d, dt)
+
+
+def oomb_workspace_bytes(op, kv: PagedKV, num_q_heads=0, chunk_len=0, top_k=0) -> int:
+    s = kv.struct()
+    return load().oomb_workspace_bytes(op, ctypes.byref(s), num_q_heads, chunk_len, top_k)
+
+
+def workspace(op, kv: PagedKV, num_q_heads=0, chunk_len=0, top_k=0) -> torch.Tensor:
+    """A zero-filled device workspace of the size ``op`` needs (caller-owned)."""
+    n = oomb_workspace_bytes(op, kv, num_q_heads, chunk_len, top_k)
+    return torch.zeros(n, dtype=torch.uint8, device=kv.k.device)
+
+
+def oomb_validate_page_table_host(page_table, num_slots):
+    pt = torch.as_tensor(page_table, dtype=torch.int32).contiguous().cpu()
+    _check(load().oomb_validate_page_table_host(ctypes.c_void_p(pt.data_ptr()), pt.numel(),
+                                                num_slots))
+
+
+def oomb_validate_page_table(kv: PagedKV, ws: torch.Tensor, stream=None):
+    s = kv.struct()
+    _check(load().oomb_validate_page_table(ctypes.byref(s), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def oomb_page_reps(kv: PagedKV, first_page, n_pages, reps: torch.Tensor, ws: torch.Tensor,
+                   stream=None):
+    s = kv.struct()
+    _check(load().oomb_page_reps(ctypes.byref(s), first_page, n_pages, _ptr(reps), _ptr(ws),
+                                 ws.numel(), _stream(stream)))
+
+
+def oomb_select_topk(q, chunk_start, reps, kv: PagedKV, top_k, sel, ws, scores=None,
+                     stream=None):
+    s = kv.struct()
+    c, hq, _ = q.shape
+    _check(load().oomb_select_topk(_ptr(q), hq, c, chunk_start, _ptr(reps), ctypes.byref(s), top_k,
+                                   _ptr(sel), _ptr(scores), _ptr(ws), ws.numel(),
+                                   _stream(stream)))
+
+
+def oomb_sparse_attn_fwd(q, kv: PagedKV, sel, n_sel, chunk_start, o, lse, ws, scale=0.0,
+                         stream=None):
+    s = kv.struct()
+    c, hq, _ = q.shape
+    _check(load().oomb_sparse_attn_fwd(_ptr(q), ctypes.byref(s), _ptr(sel), n_sel, hq, c,
+                                       chunk_start, float(scale), _ptr(o), _ptr(lse), _ptr(ws),
+                                       ws.numel(), _stream(stream)))
+
+
+def oomb_sparse_attn_bwd(q, o, dout, lse, kv: PagedKV, sel, n_sel, chunk_start, dq, ws,
+                         scale=0.0, stream=None):
+    s = kv.struct()
+    c, hq, _ = q.shape
+    _check(load().oomb_sparse_attn_bwd(_ptr(q), _ptr(o), _ptr(dout), _ptr(lse), ctypes.byref(s),
+                                       _ptr(sel), n_sel, hq, c, chunk_start, float(scale),
+                                       _ptr(dq), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def oomb_device_status(ws: torch.Tensor, stream=None):
+    """Read and clear the device status word; returns (code, where, block)."""
+    info = (ctypes.c_int32 * 2)()
+    code = load().oomb_device_status(_ptr(ws), _stream(stream), info)
+    return code, info[0], info[1]
+
+
+def oomb_set_wait_limit_ns(ns: int):
+    load().oomb_set_wait_limit_ns(ctypes.c_uint64(int(ns)))
+
+
+def oomb_debug_wait_unset_flag(ws: torch.Tensor, stream=None):
+    _check(load().oomb_debug_wait_unset_flag(_ptr(ws), ws.numel(), _stream(stream)))
+
+
+def oomb_status_string(code: int) -> str:
+    return load().oomb_status_string(code).decode()
+
+
+def oomb_last_error() -> str:
+    return load().oomb_last_error().decode()
+
+
+# ---------------------------------------------------------------------------
+# Convenience: one full pass of the path on one chunk (allocations by torch).
+# ---------------------------------------------------------------------------
+def sparse_attention_step(q, dout, kv: PagedKV, chunk_start, top_k, reps=None, stream=None):
+    """reps (all pages) -> Top-K selection -> forward -> backward (dK/dV in place).
+
+    Returns dict(reps, sel, o, lse, dq).  Every call here is one of the C ABI
+    entry points above; outputs and workspaces are caller (torch) allocations.
+    """
+    ns, hkv, p, d = kv.k.shape
+    c, hq, _ = q.shape
+    n_pages = kv.page_table.numel()
+    dev = q.device
+    ws_r = workspace(OOMB_OP_PAGE_REPS, kv)
+    if reps is None:
+        reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
+        oomb_page_reps(kv, 0, n_pages, reps, ws_r, stream)
+    n_sel = min(top_k, chunk_start // p)
+    sel = torch.empty((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
+    ws_s = workspace(OOMB_OP_SELECT_TOPK, kv, hq, c, top_k)
+    oomb_select_topk(q, chunk_start, reps, kv, n_sel, sel, ws_s, stream=stream)
+    o = torch.empty_like(q)
+    lse = torch.empty((hq, c), dtype=torch.float32, device=dev)
+    ws_f = workspace(OOMB_OP_ATTN_FWD, kv, hq, c)
+    oomb_sparse_attn_fwd(q, kv, sel, n_sel, chunk_start, o, lse, ws_f, stream=stream)
+    dq = torch.empty_like(q)
+    ws_b = workspace(OOMB_OP_ATTN_BWD, kv, hq, c)
+    oomb_sparse_attn_bwd(q, o, dout, lse, kv, sel, n_sel, chunk_start, dq, ws_b, stream=stream)
+    for w in (ws_r, ws_s, ws_f, ws_b):
+        code, where, blk = oomb_device_status(w, stream)
+        if code != OOMB_OK:
+            raise OombError(code, f"device status (where {where}, block {blk})")
+    return dict(reps=reps, sel=sel[:, :n_sel], o=o, lse=lse, dq=dq)

@@ -1,0 +1,130 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+declared in include/oomb.h, and rejects bad arguments on the host before any
+launch (the pointers below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_sparse_attention_oomb_gb300 import oomb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(oomb.LIB_PATH):
+        from paged_sparse_attention_oomb_gb300.build import build
+        build()
+    return oomb.load()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "oomb.h")) as f:
+        txt = f.read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(oomb_[a-z_]+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(oomb.EXPORTED) == names
+
+
+def test_status_strings(lib):
+    assert oomb.oomb_status_string(0) == "OOMB_OK"
+    assert oomb.oomb_status_string(4) == "OOMB_ERR_TIMEOUT"
+    assert oomb.oomb_status_string(99) == "OOMB_ERR_UNKNOWN"
+
+
+def test_validate_page_table_host(lib):
+    oomb.oomb_validate_page_table_host([3, 0, 2, 1], 4)
+    oomb.oomb_validate_page_table_host([5, 0], 8)
+    with pytest.raises(oomb.OombError, match="outside"):
+        oomb.oomb_validate_page_table_host([0, 4], 4)
+    with pytest.raises(oomb.OombError, match="outside"):
+        oomb.oomb_validate_page_table_host([-1, 0], 4)
+    with pytest.raises(oomb.OombError, match="more than one page"):
+        oomb.oomb_validate_page_table_host([1, 2, 1], 4)
+
+
+FAKE = 1 << 20   # aligned, never dereferenced: every case below fails host checks first
+
+
+def _kv(**kw):
+    d = dict(k=FAKE, v=FAKE, dk=FAKE, dv=FAKE, page_table=FAKE, num_pages=64, num_slots=64,
+             page_size=64, num_kv_heads=4, head_dim=128, dtype=oomb.OOMB_BF16)
+    d.update(kw)
+    return oomb.OombPagedKV(**d)
+
+
+def _fwd(lib, kv, q=FAKE, n_sel=0, hq=28, clen=256, cstart=3840, ws=FAKE, ws_bytes=1 << 20):
+    return lib.oomb_sparse_attn_fwd(ctypes.c_void_p(q), ctypes.byref(kv), ctypes.c_void_p(FAKE),
+                                    n_sel, hq, clen, cstart, 0.0, ctypes.c_void_p(FAKE),
+                                    ctypes.c_void_p(FAKE), ctypes.c_void_p(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(page_size=48), 2, "page_size"),
+    (dict(head_dim=64), 2, "head_dim"),
+    (dict(dtype=7), 1, "dtype"),
+    (dict(num_slots=10), 1, "num_slots"),
+    (dict(num_kv_heads=0), 2, "num_kv_heads"),
+    (dict(k=FAKE + 8), 1, "aligned"),
+    (dict(page_table=0), 1, "page_table"),
+])
+def test_bad_cache_rejected(lib, kw, code, msg):
+    rc = _fwd(lib, _kv(**kw))
+    assert rc == code
+    assert msg in oomb.oomb_last_error()
+
+
+@pytest.mark.parametrize("args,msg", [
+    (dict(hq=30), "multiple of Hkv"),
+    (dict(clen=100), "chunk_len"),
+    (dict(cstart=100), "chunk_start"),
+    (dict(cstart=4032), "runs past"),
+    (dict(n_sel=61), "n_sel"),
+    (dict(n_sel=-1), "n_sel"),
+    (dict(ws_bytes=16), "ws has"),
+    (dict(ws=FAKE + 64), "256-byte"),
+    (dict(q=FAKE + 4), "aligned"),
+])
+def test_bad_call_rejected(lib, args, msg):
+    rc = _fwd(lib, _kv(), **args)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG
+    assert msg in oomb.oomb_last_error()
+
+
+def test_bwd_requires_grad_buffers(lib):
+    kv = _kv(dk=0)
+    rc = lib.oomb_sparse_attn_bwd(*(ctypes.c_void_p(FAKE),) * 4, ctypes.byref(kv),
+                                  ctypes.c_void_p(FAKE), 0, 28, 256, 3840, 0.0,
+                                  ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1 << 30, None)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "dk" in oomb.oomb_last_error()
+
+
+def test_select_rejects_bad_pages(lib):
+    kv = _kv()
+    rc = lib.oomb_page_reps(ctypes.byref(kv), 60, 8, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                            256, None)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "outside" in oomb.oomb_last_error()
+    rc = lib.oomb_select_topk(ctypes.c_void_p(FAKE), 28, 256, 3840, ctypes.c_void_p(FAKE),
+                              ctypes.byref(kv), -3, ctypes.c_void_p(FAKE), None,
+                              ctypes.c_void_p(FAKE), 1 << 20, None)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "top_k" in oomb.oomb_last_error()
+
+
+def test_workspace_sizes(lib):
+    kv = _kv(num_pages=32768, num_slots=32768, page_size=128)
+    bwd = lib.oomb_workspace_bytes(oomb.OOMB_OP_ATTN_BWD, ctypes.byref(kv), 28, 8192, 0)
+    # status block + Delta [28][8192] + fp32 dq accumulator [8192][28][128]
+    assert bwd == 256 + 28 * 8192 * 4 + 8192 * 28 * 128 * 4
+    assert lib.oomb_workspace_bytes(oomb.OOMB_OP_ATTN_FWD, ctypes.byref(kv), 28, 8192, 0) == 256
+    sel = lib.oomb_workspace_bytes(oomb.OOMB_OP_SELECT_TOPK, ctypes.byref(kv), 28, 8192, 128)
+    assert sel >= 256 + 4 * 32768 * 4
+    assert lib.oomb_workspace_bytes(99, ctypes.byref(kv), 0, 0, 0) == 0

@@ -86,6 +86,16 @@ def test_sparse_all_pages_equals_dense(shuffle):
     np.testing.assert_allclose(dq, dqd[t0:], atol=1e-12)
     np.testing.assert_allclose(_flat(dk_acc), dkd, atol=1e-12)
     np.testing.assert_allclose(_flat(dv_acc), dvd, atol=1e-12)
+    rows = np.array([0, 7, 31, 47])
+    dqr = oracle.attn_dq_rows(qc, c["k_pool"], c["v_pool"], c["pt"], sel, t0, c["p"], o[rows],
+                              lse[:, rows], doc, rows)
+    np.testing.assert_allclose(dqr, dqd[t0 + rows], atol=1e-12)
+    kvh = [1]
+    o1, lse1 = oracle.attn_fwd(qc, c["k_pool"], c["v_pool"], c["pt"], sel, t0, c["p"], kv_heads=kvh)
+    dkp, dvp = oracle.attn_bwd_pages(qc, c["k_pool"], c["v_pool"], c["pt"], sel, t0, c["p"], o1,
+                                     lse1, doc, 1, [2, 7, 9])
+    np.testing.assert_allclose(dkp, dkd.reshape(-1, 8, 2, 8)[[2, 7, 9], :, 1], atol=1e-12)
+    np.testing.assert_allclose(dvp, dvd.reshape(-1, 8, 2, 8)[[2, 7, 9], :, 1], atol=1e-12)
 
 
 def test_sparse_all_pages_equals_dense_tiny_fp32_workload():

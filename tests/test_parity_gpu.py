@@ -1,0 +1,261 @@
+"""CUDA path vs the CPU oracle, through the C ABI (GB300 only).
+
+Small cases are compared element by element (several tiles, ragged tails,
+every page size, K = 0 / some / all, first chunk, shuffled page tables).  The
+five named workloads run at full size: selection in full, outputs on sampled
+rows and gradients on sampled pages, each computed exactly by the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_sparse_attention_oomb_gb300 import oomb
+from paged_sparse_attention_oomb_gb300.workloads import WORKLOADS, Workload, make_inputs, to_numpy64
+
+from parity_util import (check_selection, compare, gpu_bwd, gpu_fwd, gpu_kv, gpu_reps,
+                         gpu_select, oracle_reps_blocked, oracle_selection, sel_tensor)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    oomb.load()
+    oomb.oomb_set_wait_limit_ns(0)
+
+
+def W(name, dtype, hq, hkv, ctx, p, c, k, shuffled=True, start=-1):
+    return Workload(name, dtype, hq, hkv, 128 if dtype == "bf16" else 64, ctx, p, c, k, shuffled,
+                    start)
+
+
+SMALL = [
+    W("bf16_p64_ragged_c576_k13", "bf16", 4, 2, 4096, 64, 576, 13),
+    W("bf16_p128_g8_c384_k5", "bf16", 8, 1, 2048, 128, 384, 5, shuffled=False),
+    W("bf16_p16_g1_c208_k37", "bf16", 2, 2, 1024, 16, 208, 37),
+    W("bf16_p32_k0", "bf16", 4, 4, 1536, 32, 256, 0),
+    W("bf16_first_chunk", "bf16", 4, 2, 2048, 64, 1024, 8, start=0),
+    W("bf16_dense_all", "bf16", 4, 2, 2048, 64, 512, 1 << 20),
+    W("bf16_mid_chunk_k20", "bf16", 14, 2, 4096, 64, 640, 20, start=1920),
+    W("fp32_ragged_c176_k7", "fp32", 4, 2, 512, 16, 176, 7),
+    W("fp32_p32_k3", "fp32", 2, 1, 1024, 32, 320, 3),
+]
+
+
+def _run_small(wl, seed=0):
+    x = make_inputs(wl, seed=seed, device=DEV)
+    kv = gpu_kv(x)
+    q, kp, vp, do, pt = (to_numpy64(x.q), to_numpy64(x.k_pool), to_numpy64(x.v_pool),
+                         to_numpy64(x.do), to_numpy64(x.page_table))
+    # step 1: representative vectors
+    reps = gpu_reps(kv)
+    reps64 = oracle.page_reps(kp, pt)
+    compare(reps.cpu().numpy(), reps64, "fp32", f"{wl.name} reps")
+    # step 2: selection (bit-exact up to flagged near-ties)
+    sel_g, scores_g = gpu_select(x, kv, reps, wl.top_k)
+    sel_o, scores_o = oracle_selection(x, reps64, wl.top_k)
+    check_selection(sel_g.cpu().numpy(), sel_o, scores_o)
+    nc = wl.num_candidates
+    if nc:
+        np.testing.assert_allclose(scores_g[:, :nc].cpu().numpy(), scores_o, rtol=1e-5, atol=1e-6)
+    assert torch.all(torch.isinf(scores_g[:, nc:]))
+    # steps 3-4 on the oracle's selection (its output may feed the GPU, never the reverse)
+    n_sel = sel_o.shape[1]
+    st = sel_tensor(sel_o, DEV)
+    o_g, lse_g = gpu_fwd(x, kv, st, n_sel)
+    dq_g = gpu_bwd(x, kv, st, n_sel, o_g, lse_g)
+    o_o, lse_o = oracle.attn_fwd(q, kp, vp, pt, sel_o, wl.start, wl.page_size)
+    dq_o, dk_o, dv_o = oracle.attn_bwd(q, kp, vp, pt, sel_o, wl.start, wl.page_size, o_o, lse_o, do)
+    dt = wl.dtype
+    compare(o_g.float().cpu().numpy(), o_o, dt, f"{wl.name} O")
+    compare(lse_g.cpu().numpy(), lse_o, "fp32" if dt == "fp32" else "bf16", f"{wl.name} LSE")
+    np.testing.assert_allclose(lse_g.cpu().numpy(), lse_o, atol=2e-3 if dt == "bf16" else 1e-4)
+    compare(dq_g.float().cpu().numpy(), dq_o, dt, f"{wl.name} dQ")
+    ptl = x.page_table.long().cpu()
+    dk_g = to_numpy64(kv.dk)[ptl.numpy()]           # logical page order
+    dv_g = to_numpy64(kv.dv)[ptl.numpy()]
+    compare(dk_g, dk_o, dt, f"{wl.name} dK")
+    compare(dv_g, dv_o, dt, f"{wl.name} dV")
+    # untouched pages stay exactly zero
+    untouched = np.all(dk_o == 0, axis=(2, 3))
+    assert np.all(dk_g[untouched] == 0) and np.all(dv_g[untouched] == 0)
+    return x, kv
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_small_parity(wl):
+    _run_small(wl)
+
+
+def test_tiny_fp32_workload_k8_and_all():
+    base = WORKLOADS["tiny_fp32_ctx1k"]
+    _run_small(base)
+    _run_small(base.with_(name="tiny_fp32_all", top_k=1 << 20))
+
+
+def test_bwd_accumulates_in_place():
+    wl = W("acc", "bf16", 4, 2, 2048, 64, 256, 6)
+    x = make_inputs(wl, seed=3, device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(11)
+    init_k = torch.randn(x.k_pool.shape, generator=g, device=DEV).to(torch.bfloat16)
+    init_v = torch.randn(x.v_pool.shape, generator=g, device=DEV).to(torch.bfloat16)
+    kv = gpu_kv(x, grad_init=(init_k, init_v))
+    q, kp, vp, do, pt = (to_numpy64(x.q), to_numpy64(x.k_pool), to_numpy64(x.v_pool),
+                         to_numpy64(x.do), to_numpy64(x.page_table))
+    sel_o, _ = oracle_selection(x, oracle.page_reps(kp, pt), wl.top_k)
+    st = sel_tensor(sel_o, DEV)
+    o_g, lse_g = gpu_fwd(x, kv, st, sel_o.shape[1])
+    gpu_bwd(x, kv, st, sel_o.shape[1], o_g, lse_g)
+    o_o, lse_o = oracle.attn_fwd(q, kp, vp, pt, sel_o, wl.start, wl.page_size)
+    dk_acc = to_numpy64(init_k)[pt]
+    dv_acc = to_numpy64(init_v)[pt]
+    _, dk_o, dv_o = oracle.attn_bwd(q, kp, vp, pt, sel_o, wl.start, wl.page_size, o_o, lse_o, do,
+                                    dk_acc=dk_acc, dv_acc=dv_acc)
+    compare(to_numpy64(kv.dk)[pt], dk_o, "bf16", "dK += ")
+    compare(to_numpy64(kv.dv)[pt], dv_o, "bf16", "dV += ")
+
+
+def test_cross_chunk_accumulation():
+    """Chunks processed forward in order, backward in reverse, dK/dV accumulated
+    across chunks in the same paged buffers (chunk-recurrent pass)."""
+    base = W("xchunk", "bf16", 4, 2, 2048, 64, 512, 1 << 20)
+    x = make_inputs(base, seed=5, device=DEV)
+    kv = gpu_kv(x)
+    q_full = torch.randn((2048, 4, 128), device=DEV, generator=torch.Generator(device=DEV).manual_seed(1)).to(torch.bfloat16)
+    do_full = torch.randn((2048, 4, 128), device=DEV, generator=torch.Generator(device=DEV).manual_seed(2)).to(torch.bfloat16)
+    reps = gpu_reps(kv)
+    outs = []
+    for c in range(4):
+        wl = base.with_(chunk_start=c * 512)
+        xc = type(x)(wl, q_full[c * 512:(c + 1) * 512].contiguous(), x.k_pool, x.v_pool,
+                     do_full[c * 512:(c + 1) * 512].contiguous(), x.page_table)
+        sel, _ = gpu_select(xc, kv, reps, wl.top_k)
+        o, lse = gpu_fwd(xc, kv, sel.contiguous(), sel.shape[1])
+        outs.append((xc, sel.contiguous(), o, lse))
+    for xc, sel, o, lse in reversed(outs):
+        gpu_bwd(xc, kv, sel if sel.numel() else sel_tensor(np.zeros((2, 0), np.int32), DEV),
+                sel.shape[1], o, lse)
+    kp, vp, pt = to_numpy64(x.k_pool), to_numpy64(x.v_pool), to_numpy64(x.page_table)
+    o_o, dq_o, dk_o, dv_o, _ = oracle.chunk_recurrent_grads(
+        to_numpy64(q_full), kp, vp, pt, to_numpy64(do_full), 512, 64, 1 << 20)
+    compare(to_numpy64(kv.dk)[pt], dk_o, "bf16", "cross-chunk dK")
+    compare(to_numpy64(kv.dv)[pt], dv_o, "bf16", "cross-chunk dV")
+
+
+def test_deterministic_selection_and_forward():
+    wl = W("det", "bf16", 8, 2, 8192, 64, 512, 31)
+    x = make_inputs(wl, seed=9, device=DEV)
+    kv = gpu_kv(x, with_grads=False)
+    reps = gpu_reps(kv)
+    s1, sc1 = gpu_select(x, kv, reps, wl.top_k)
+    s2, sc2 = gpu_select(x, kv, gpu_reps(kv), wl.top_k)
+    assert torch.equal(s1, s2) and torch.equal(sc1, sc2)
+    o1, l1 = gpu_fwd(x, kv, s1.contiguous(), s1.shape[1])
+    o2, l2 = gpu_fwd(x, kv, s1.contiguous(), s1.shape[1])
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    kv = gpu_kv(make_inputs(W("t", "bf16", 4, 2, 1024, 64, 128, 2), device=DEV), with_grads=False)
+    ws = oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv)
+    oomb.oomb_set_wait_limit_ns(1_000_000)   # 1 ms
+    try:
+        oomb.oomb_debug_wait_unset_flag(ws)
+        code, where, _ = oomb.oomb_device_status(ws)
+    finally:
+        oomb.oomb_set_wait_limit_ns(0)
+    assert code == oomb.OOMB_ERR_TIMEOUT and where == 90
+    # the context is still usable: a normal call completes with OK status
+    reps = gpu_reps(kv)
+    assert torch.isfinite(reps).all()
+
+
+def test_out_of_range_selection_is_flagged_not_read():
+    wl = W("oob", "bf16", 4, 2, 2048, 64, 256, 4)
+    x = make_inputs(wl, device=DEV)
+    kv = gpu_kv(x)
+    bad = torch.tensor([[0, 1, 2, 10_000], [0, 1, 2, 3]], dtype=torch.int32, device=DEV)
+    o = torch.empty_like(x.q)
+    lse = torch.empty((4, 256), dtype=torch.float32, device=DEV)
+    ws = oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv)
+    oomb.oomb_sparse_attn_fwd(x.q, kv, bad, 4, wl.start, o, lse, ws)
+    code, _, _ = oomb.oomb_device_status(ws)
+    assert code == oomb.OOMB_ERR_DEVICE_BOUNDS
+
+
+def test_device_page_table_validation():
+    wl = W("pt", "bf16", 4, 2, 1024, 64, 128, 2)
+    x = make_inputs(wl, device=DEV)
+    kv = gpu_kv(x, with_grads=False)
+    ws = oomb.workspace(oomb.OOMB_OP_VALIDATE, kv)
+    oomb.oomb_validate_page_table(kv, ws)
+    bad = x.page_table.clone()
+    bad[3] = bad[5]
+    with pytest.raises(oomb.OombError, match="two pages"):
+        oomb.oomb_validate_page_table(oomb.PagedKV(x.k_pool, x.v_pool, bad), ws)
+    bad[3] = 99
+    with pytest.raises(oomb.OombError, match="outside"):
+        oomb.oomb_validate_page_table(oomb.PagedKV(x.k_pool, x.v_pool, bad), ws)
+
+
+# ---------------------------------------------------------------------------
+# the named workloads at full size
+# ---------------------------------------------------------------------------
+FULL = ["qwen7b_dense_ctx32k", "qwen7b_ctx256k_k64", "qwen7b_ctx1m_k128", "qwen7b_ctx4m_k128"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    wl = WORKLOADS[name]
+    x = make_inputs(wl, seed=0, device=DEV)
+    kv = gpu_kv(x)
+    reps = gpu_reps(kv)
+    reps64 = oracle_reps_blocked(x.k_pool, x.page_table)
+    rs = np.random.default_rng(1).choice(wl.num_pages, 256, replace=False)
+    compare(reps[rs].cpu().numpy(), reps64[rs], "fp32", f"{name} reps (256 sampled pages)")
+    sel_g, _ = gpu_select(x, kv, reps, wl.top_k)
+    sel_o, scores_o = oracle_selection(x, reps64, wl.top_k)
+    flagged = check_selection(sel_g.cpu().numpy(), sel_o, scores_o)
+    print(f"{name}: near-tie swaps flagged: {flagged}")
+    n_sel = sel_o.shape[1]
+    st = sel_tensor(sel_o, DEV)
+    o_g, lse_g = gpu_fwd(x, kv, st, n_sel)
+    dq_g = gpu_bwd(x, kv, st, n_sel, o_g, lse_g)
+    # oracle on sampled rows (all heads) and on sampled pages of one KV head
+    q, do = to_numpy64(x.q), to_numpy64(x.do)
+    pt = x.page_table.cpu().numpy().astype(np.int64)
+    rng = np.random.default_rng(2)
+    rows = np.sort(np.concatenate([rng.choice(wl.chunk_len, 126, replace=False),
+                                   [0, wl.chunk_len - 1]]))
+    rows = np.unique(rows)
+    g = FULL.index(name) % wl.num_kv_heads
+    # gather just the pages the oracle needs into a compact host pool
+    own = np.arange(wl.start // wl.page_size, (wl.start + wl.chunk_len) // wl.page_size)
+    need = np.unique(np.concatenate([sel_o.reshape(-1), own]))
+    slots = torch.as_tensor(pt[need])
+    kc = x.k_pool[slots.to(DEV)].float().cpu().numpy()
+    vc = x.v_pool[slots.to(DEV)].float().cpu().numpy()
+    ptc = np.full(wl.num_pages, -1, np.int64)
+    ptc[need] = np.arange(need.size)
+    o_o, lse_o = oracle.attn_fwd(q, kc, vc, ptc, sel_o, wl.start, wl.page_size, rows=rows)
+    compare(o_g.float().cpu().numpy()[rows], o_o, "bf16", f"{name} O (sampled rows)")
+    np.testing.assert_allclose(lse_g.cpu().numpy()[:, rows], lse_o, atol=2e-3)
+    dq_o = oracle.attn_dq_rows(q, kc, vc, ptc, sel_o, wl.start, wl.page_size, o_o, lse_o, do, rows)
+    compare(dq_g.float().cpu().numpy()[rows], dq_o, "bf16", f"{name} dQ (sampled rows)")
+    o_all, lse_all = oracle.attn_fwd(q, kc, vc, ptc, sel_o, wl.start, wl.page_size, kv_heads=[g])
+    pages = np.concatenate([rng.choice(sel_o[g], min(6, n_sel), replace=False),
+                            rng.choice(own, 3, replace=False)])
+    dk_o, dv_o = oracle.attn_bwd_pages(q, kc, vc, ptc, sel_o, wl.start, wl.page_size, o_all,
+                                       lse_all, do, g, pages)
+    dk_g = kv.dk[torch.as_tensor(pt[pages], device=DEV), g].float().cpu().numpy()
+    dv_g = kv.dv[torch.as_tensor(pt[pages], device=DEV), g].float().cpu().numpy()
+    compare(dk_g, dk_o, "bf16", f"{name} dK (sampled pages, KV head {g})")
+    compare(dv_g, dv_o, "bf16", f"{name} dV (sampled pages, KV head {g})")
+    del x, kv
+    torch.cuda.empty_cache()
