@@ -3,23 +3,33 @@
 // buffers fused into the tile loop.
 // Method: "Out of the Memory Barrier" technical summary, section 2: "Paged
 // Memory Management" (KV gradients live in pages and are accumulated in place
-// outside autograd) and "Page-level Sparse Attention" (the backward reuses the
-// forward's page choice).
+// outside autograd), "Page-level Sparse Attention" (the backward reuses the
+// forward's page choice), "Chunk-Recurrent Training Framework" (the backward
+// recomputes what the forward discarded).
 //
 // One CTA owns one 128-key tile of one KV head: a tile of selected pages
 // (attended by every query tile of the chunk) or of the chunk's own pages
 // (attended by the query tiles at or after it).  It loops over the G query
-// heads of the group x the query tiles that see it; per iteration:
-//   dP^T = V dO^T, S^T = K Q^T          (TMEM, keys on lanes, queries on columns)
-//   P^T = exp(scale S^T - lse),  dS^T = P^T (dP^T - Delta)    (compute warps)
-//   dV += P^T dO,  dK += dS^T Q          (TMEM accumulators, whole CTA life)
-//   dQ_tile = dS K                       (TMEM, drained with fp32 reductions)
-// At the end dK (x scale) and dV are added to the bf16 gradient pages of the
-// tile's slots: one read-add-write and one rounding per slot per call.  Each
-// (slot, KV head) has exactly one owner CTA, so no atomics touch dK/dV.
-// Roles (192 threads): warp 0 TMA producer + TMEM allocator, warp 1 MMA
-// issuer, warps 2..5 compute (TMEM lane quarter = warp % 4).
-// TMEM: [0,128) S^T then dQ, [128,256) dP^T, [256,384) dV, [384,512) dK.
+// heads of the group x the query tiles that see it.  Iteration n:
+//   MMA1  S^T  = K Q^T                 TMEM R0 (keys on lanes, queries on columns)
+//   MMA2  dP^T = V dO^T                TMEM R1
+//   P^T = exp2(S^T * scale*log2e - lse2)   -> bf16 pairs, back into R0 (TMEM)
+//   MMA3  dV  += P^T dO                A from TMEM (R0), B = dO (shared)
+//   dS^T = scale * P^T (dP^T - Delta)   -> bf16 into a swizzled shared tile
+//   MMA4  dK  += dS^T Q                TMEM R3
+//   MMA5  dQ^T = K^T dS^T              TMEM R1 (head dim on lanes), drained with
+//                                      coalesced fp32 reductions
+// Q/dO tiles (+ their lse2/Delta rows) stream through a 2-stage TMA ring, and
+// MMA1 of iteration n+1 is issued as soon as MMA3 of n has consumed P^T, so the
+// tensor pipe overlaps the exponentials, the dS pass and the dQ drain.
+// At the end the CTA adds dK and dV to the bf16 gradient pages of its slots:
+// one read-add-write and one rounding per slot per call, no atomics, because
+// each (slot, KV head) has exactly one owner CTA.
+// Roles (320 threads): warp 0 TMA producer + TMEM allocator, warp 1 MMA
+// issuer, warps 2..9 compute: TMEM lane quarter = warp % 4, and the two warps
+// of a quarter split the 128 columns into halves.
+// TMEM: R0 [0,128) S^T / P^T, R1 [128,256) dP^T / dQ, R2 [256,384) dV,
+// R3 [384,512) dK.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,35 +42,36 @@
 namespace oomb {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kComputeThreads = 256;
 constexpr uint32_t kKOff = 0;
 constexpr uint32_t kVOff = kTileBytes;
-constexpr uint32_t kQOff = 2 * kTileBytes;
-constexpr uint32_t kDOOff = 3 * kTileBytes;
-constexpr uint32_t kPTOff = 4 * kTileBytes;
-constexpr uint32_t kDSOff = 5 * kTileBytes;
-constexpr uint32_t kVecOff = 6 * kTileBytes;      // lse[2][128], delta[2][128] floats
-constexpr uint32_t kBarOff = kVecOff + 2048;
-constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
+constexpr uint32_t kQOff = 2 * kTileBytes;        // 2 stages
+constexpr uint32_t kDOOff = 4 * kTileBytes;       // 2 stages
+constexpr uint32_t kDSOff = 6 * kTileBytes;
+constexpr uint32_t kVecOff = 7 * kTileBytes;      // per stage: lse2[128], delta[128]
+constexpr uint32_t kBarOff = kVecOff + 2 * 1024;
+constexpr uint32_t kSmemBytes = kBarOff + 256;    // base is 1024-aligned by declaration
 
 struct Bars {
   uint64_t kv_full;
-  uint64_t q_full, q_empty;
-  uint64_t do_full, do_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t do_full[2], do_empty[2];
   uint64_t s_full, dp_full, dq_full;
-  uint64_t r0_free, r1_free;
-  uint64_t pt_ready, ds_ready, pds_free;
+  uint64_t p_ready, ds_ready, r1_free;
+  uint64_t pt_consumed, ds_free;
   uint64_t acc_done;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct BwdParams {
   const int32_t* sel;
   const int32_t* pt;
-  const float* lse;        // [hq][chunk_len]
-  const float* delta;      // [hq][n_qtiles*128]
+  const float* lse2;       // [hq][n_qtiles*128]  lse * log2(e); +inf on padding rows
+  const float* delta;      // [hq][n_qtiles*128]  0 on padding rows
   float* dq_acc;           // [chunk_len][hq][128]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -88,16 +99,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tm_do,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   const uint32_t bbase = sbase + kBarOff;
-  float* vec = reinterpret_cast<float*>(smem + kVecOff);   // lse: [0,256), delta: [256,512)
+  const float* vec = reinterpret_cast<const float*>(smem + kVecOff);
 #define BAR(f) bar_addr(bbase, &bars->f, bars)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (sbase & 1023u) {          // the swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) raise_status(p.status, kStatusBounds, kWhereBwdProducer);
+    return;
+  }
   const int g = static_cast<int>(blockIdx.x) % p.hkv;
   const int kt = static_cast<int>(blockIdx.x) / p.hkv;     // selected tiles first
   const bool is_sel = kt < p.t_sel;
@@ -109,22 +122,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ppt = 128 / p.page_size;
   const int own_page0 = p.chunk_start / p.page_size;
   const int n_own_pages = p.chunk_len / p.page_size;
+  const int padded = p.n_qtiles * 128;
   const int32_t* sel_g = p.sel + static_cast<long>(g) * p.n_sel;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(kv_full), 1);
-    mbar_init(BAR(q_full), 1);
-    mbar_init(BAR(q_empty), 1);
-    mbar_init(BAR(do_full), 1);
-    mbar_init(BAR(do_empty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(q_full[i]), 1);
+      mbar_init(BAR(q_empty[i]), 1);
+      mbar_init(BAR(do_full[i]), 1);
+      mbar_init(BAR(do_empty[i]), 1);
+    }
     mbar_init(BAR(s_full), 1);
     mbar_init(BAR(dp_full), 1);
     mbar_init(BAR(dq_full), 1);
-    mbar_init(BAR(r0_free), 128);
-    mbar_init(BAR(r1_free), 128);
-    mbar_init(BAR(pt_ready), 128);
-    mbar_init(BAR(ds_ready), 128);
-    mbar_init(BAR(pds_free), 1);
+    mbar_init(BAR(p_ready), kComputeThreads);
+    mbar_init(BAR(ds_ready), kComputeThreads);
+    mbar_init(BAR(r1_free), kComputeThreads);
+    mbar_init(BAR(pt_consumed), 1);
+    mbar_init(BAR(ds_free), 1);
     mbar_init(BAR(acc_done), 1);
     mbar_init(BAR(drain), 1);
     bars->abort_flag = 0;
@@ -140,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{p.status, &bars->abort_flag, p.wait_ns};
 
-  // Logical page of slot-row u of this key tile, and whether its keys are real.
+  // Logical page of page-slot u of this key tile, and whether its keys are real.
   auto tile_page = [&](int u, bool* valid) -> int {
     if (is_sel) {
       const int pi = kt * ppt + u;
@@ -183,28 +199,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; n < n_iter; ++n) {
         const int h = g * grp + n / nq;
         const int qi = i0 + n % nq;
-        const uint32_t ph1 = (n & 1) ^ 1;
-        if (!mbar_wait(BAR(q_empty), ph1, wc, kWhereBwdProducer)) break;
-        mbar_arrive_expect_tx(BAR(q_full), kTileBytes);
-        tma_load_3d(sbase + kQOff, &tm_q, BAR(q_full), 0, h, qi * 128);
-        tma_load_3d(sbase + kQOff + kHalfBytes, &tm_q, BAR(q_full), 64, h, qi * 128);
+        const int s = n & 1;
+        const uint32_t phe = ((n >> 1) & 1) ^ 1;
+        if (!mbar_wait(BAR(q_empty[s]), phe, wc, kWhereBwdProducer)) break;
+        mbar_arrive_expect_tx(BAR(q_full[s]), kTileBytes);
+        tma_load_3d(sbase + kQOff + s * kTileBytes, &tm_q, BAR(q_full[s]), 0, h, qi * 128);
+        tma_load_3d(sbase + kQOff + s * kTileBytes + kHalfBytes, &tm_q, BAR(q_full[s]), 64, h,
+                    qi * 128);
         ++nq_issued;
-        if (!mbar_wait(BAR(do_empty), ph1, wc, kWhereBwdProducer)) break;
-        const int rows = min(128, p.chunk_len - qi * 128);
-        const uint32_t vb = sbase + kVecOff + (n & 1) * 512;
-        mbar_arrive_expect_tx(BAR(do_full), kTileBytes + rows * 4 + 512);
-        tma_load_3d(sbase + kDOOff, &tm_do, BAR(do_full), 0, h, qi * 128);
-        tma_load_3d(sbase + kDOOff + kHalfBytes, &tm_do, BAR(do_full), 64, h, qi * 128);
-        bulk_load(vb, p.lse + static_cast<long>(h) * p.chunk_len + qi * 128, rows * 4,
-                  BAR(do_full));
-        bulk_load(vb + 1024, p.delta + static_cast<long>(h) * p.n_qtiles * 128 + qi * 128, 512,
-                  BAR(do_full));
+        if (!mbar_wait(BAR(do_empty[s]), phe, wc, kWhereBwdProducer)) break;
+        const uint32_t vb = sbase + kVecOff + s * 1024;
+        const long voff = static_cast<long>(h) * padded + qi * 128;
+        mbar_arrive_expect_tx(BAR(do_full[s]), kTileBytes + 1024);
+        tma_load_3d(sbase + kDOOff + s * kTileBytes, &tm_do, BAR(do_full[s]), 0, h, qi * 128);
+        tma_load_3d(sbase + kDOOff + s * kTileBytes + kHalfBytes, &tm_do, BAR(do_full[s]), 64, h,
+                    qi * 128);
+        bulk_load(vb, p.lse2 + voff, 512, BAR(do_full[s]));
+        bulk_load(vb + 512, p.delta + voff, 512, BAR(do_full[s]));
         ++ndo_issued;
       }
       if (bars->abort_flag) {
+        // unwinding: let every copy this thread issued land before the CTA exits
         mbar_drain_wait(BAR(kv_full), 0);
-        if (nq_issued > 0) mbar_drain_wait(BAR(q_full), (nq_issued - 1) & 1);
-        if (ndo_issued > 0) mbar_drain_wait(BAR(do_full), (ndo_issued - 1) & 1);
+        for (int s = 0; s < 2; ++s) {
+          const int lq = (nq_issued - 1 - s) >= 0 ? ((nq_issued - 1 - s) / 2) * 2 + s : -1;
+          if (lq >= 0) mbar_drain_wait(BAR(q_full[s]), (lq >> 1) & 1);
+          const int ld = (ndo_issued - 1 - s) >= 0 ? ((ndo_issued - 1 - s) / 2) * 2 + s : -1;
+          if (ld >= 0) mbar_drain_wait(BAR(do_full[s]), (ld >> 1) & 1);
+        }
       }
     }
   } else if (warp == 1) {
@@ -212,51 +234,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdKQ = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, 128, false, true);  // dV, dK
-      constexpr uint32_t kIdDQ = idesc_bf16_f32(128, 128, true, true);    // dQ
+      constexpr uint32_t kIdDQ = idesc_bf16_f32(128, 128, true, true);    // dQ^T
       const uint32_t t_r0 = tmem, t_r1 = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 384;
       bool ok = mbar_wait(BAR(kv_full), 0, wc, kWhereBwdMma);
       for (int n = 0; ok && n < n_iter; ++n) {
-        const uint32_t ph = n & 1, ph1 = ph ^ 1;
-        // dP^T = V dO^T
-        if (!(ok = mbar_wait(BAR(do_full), ph, wc, kWhereBwdMma))) break;
+        const int s = n & 1;
+        const uint32_t phs = (n >> 1) & 1;       // stage phase
+        const uint32_t ph = n & 1, ph1 = ph ^ 1; // per-iteration phase
+        const uint32_t qa = sbase + kQOff + s * kTileBytes;
+        const uint32_t da = sbase + kDOOff + s * kTileBytes;
+        // MMA1: S^T = K Q^T  (R0 must be free: MMA3 of n-1 consumed P^T, and the
+        // dS pass of n-1 -- which reads P^T -- ended before MMA4 of n-1 was issued)
+        if (!(ok = mbar_wait(BAR(q_full[s]), phs, wc, kWhereBwdMma))) break;
+        if (!(ok = mbar_wait(BAR(pt_consumed), ph1, wc, kWhereBwdMma))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(t_r0, desc_kmajor(sbase + kKOff, kk), desc_kmajor(qa, kk), kIdKQ, kk > 0);
+        umma_commit(BAR(s_full));
+        // MMA2: dP^T = V dO^T  (R1 must be free: dQ of n-1 drained)
+        if (!(ok = mbar_wait(BAR(do_full[s]), phs, wc, kWhereBwdMma))) break;
         if (!(ok = mbar_wait(BAR(r1_free), ph1, wc, kWhereBwdMma))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_r1, desc_kmajor(sbase + kVOff, kk), desc_kmajor(sbase + kDOOff, kk), kIdKQ,
-                  kk > 0);
+          umma_ss(t_r1, desc_kmajor(sbase + kVOff, kk), desc_kmajor(da, kk), kIdKQ, kk > 0);
         umma_commit(BAR(dp_full));
-        // S^T = K Q^T
-        if (!(ok = mbar_wait(BAR(q_full), ph, wc, kWhereBwdMma))) break;
-        if (!(ok = mbar_wait(BAR(r0_free), ph1, wc, kWhereBwdMma))) break;
+        // MMA3: dV += P^T dO  (P^T in TMEM R0 as bf16 pairs, 8 columns per k-step;
+        // query columns [64 h, 64 h + 64) sit at R0 columns [64 h, 64 h + 32))
+        if (!(ok = mbar_wait(BAR(p_ready), ph, wc, kWhereBwdMma))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_r0, desc_kmajor(sbase + kKOff, kk), desc_kmajor(sbase + kQOff, kk), kIdKQ,
-                  kk > 0);
-        umma_commit(BAR(s_full));
-        // dV += P^T dO
-        if (!(ok = mbar_wait(BAR(pt_ready), ph, wc, kWhereBwdMma))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_dv, desc_kmajor(sbase + kPTOff, kk), desc_mnmajor(sbase + kDOOff, kk), kIdAcc,
+          umma_ts(t_dv, t_r0 + 64 * (kk >> 2) + 8 * (kk & 3), desc_mnmajor(da, kk), kIdAcc,
                   (n > 0 || kk > 0));
-        umma_commit(BAR(do_empty));
-        // dK += dS^T Q ; dQ = dS K
+        umma_commit(BAR(pt_consumed));
+        umma_commit(BAR(do_empty[s]));
+        // MMA4: dK += dS^T Q ; MMA5: dQ = dS K
         if (!(ok = mbar_wait(BAR(ds_ready), ph, wc, kWhereBwdMma))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_dk, desc_kmajor(sbase + kDSOff, kk), desc_mnmajor(sbase + kQOff, kk), kIdAcc,
+          umma_ss(t_dk, desc_kmajor(sbase + kDSOff, kk), desc_mnmajor(qa, kk), kIdAcc,
                   (n > 0 || kk > 0));
-        umma_commit(BAR(q_empty));
+        umma_commit(BAR(q_empty[s]));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_r0, desc_mnmajor(sbase + kDSOff, kk), desc_mnmajor(sbase + kKOff, kk), kIdDQ,
+          umma_ss(t_r1, desc_mnmajor(sbase + kKOff, kk), desc_mnmajor(sbase + kDSOff, kk), kIdDQ,
                   kk > 0);
         umma_commit(BAR(dq_full));
-        umma_commit(BAR(pds_free));
+        umma_commit(BAR(ds_free));
       }
       if (ok) {
         umma_commit(BAR(acc_done));
@@ -268,102 +295,107 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ compute
     const int q4 = warp & 3;
+    const int ch = (warp - 2) >> 2;                // column half: [64 ch, 64 ch + 64)
     const int r = q4 * 32 + lane;                  // key row (S/dP/dK/dV) or query row (dQ)
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    const float LOG2E = 1.4426950408889634f;
-    // key row validity and, for own tiles, its position within the chunk
+    const uint32_t t_r0 = tmem + lane_base, t_r1 = tmem + lane_base + 128;
+    // key row validity: invalid rows (padding of a ragged tile) get P = 0
     bool key_valid;
     tile_page(r / p.page_size, &key_valid);
-    const int key_u = is_sel ? -1 : own_t * 128 + r;
-    if (!is_sel) key_valid = key_valid && key_u < p.chunk_len;
+    if (!is_sel) key_valid = key_valid && (own_t * 128 + r) < p.chunk_len;
+    const float row_bias = key_valid ? 0.f : -INFINITY;
     bool ok = true;
     for (int n = 0; n < n_iter; ++n) {
-      const int h = g * grp + n / nq;
       const int qi = i0 + n % nq;
-      const uint32_t ph = n & 1, ph1 = ph ^ 1;
-      const float* lse_s = vec + (n & 1) * 128;
-      const float* dl_s = vec + 256 + (n & 1) * 128;
-      // columns c valid iff c < lim (query rows of the chunk, causal)
-      int lo = 0;
-      if (!is_sel && qi == own_t) lo = r;          // key r sees query columns c >= r
-      const int lim = min(128, p.chunk_len - qi * 128);
-      // ---- P^T from S^T
+      const int h = g * grp + n / nq;
+      const int s = n & 1;
+      const uint32_t phs = (n >> 1) & 1, ph = n & 1, ph1 = ph ^ 1;
+      const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 256 + 64 * ch);
+      const float4* dl4 = reinterpret_cast<const float4*>(vec + s * 256 + 128 + 64 * ch);
+      const bool diag = !is_sel && qi == own_t;   // key r sees query columns c >= r only
+      // ---- P^T = exp2(S^T scale log2e - lse2) -> bf16 pairs into R0
       ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full), ph, wc, kWhereBwdCompute));
-      if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(do_full), ph, wc, kWhereBwdCompute));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(do_full[s]), phs, wc, kWhereBwdCompute));
       if (!ok) break;
       tc_fence_after();
-      float pr[128];
+      {
+        uint32_t rr[64];
+        tmem_ld64(t_r0 + 64 * ch, rr);
+        uint32_t pk[32];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + c4 * 32, rr);
+        for (int i = 0; i < 64; i += 4) {
+          const float4 l = lse4[i >> 2];
+          const float lv[4] = {l.x, l.y, l.z, l.w};
+          float e[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = c4 * 32 + i;
-          const float x = fmaf(__uint_as_float(rr[i]), p.scale_log2, -lse_s[c] * LOG2E);
-          pr[c] = (key_valid && c >= lo && c < lim) ? ex2(x) : 0.f;
+          for (int j = 0; j < 4; ++j) {
+            float x = fmaf(__uint_as_float(rr[i + j]), p.scale_log2, row_bias - lv[j]);
+            if (diag && 64 * ch + i + j < r) x = -INFINITY;
+            e[j] = ex2(x);
+          }
+          pk[i >> 1] = pack_bf16(e[0], e[1]);
+          pk[(i >> 1) + 1] = pack_bf16(e[2], e[3]);
         }
+        // P^T of query columns [64 ch, 64 ch + 64) goes to R0 columns
+        // [64 ch, 64 ch + 32): inside the S^T columns this warp has just read, so
+        // the other warp of the lane quarter is never overtaken
+        tmem_st32(t_r0 + 64 * ch, pk);
+        tmem_st_wait();
       }
-      if (n > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(BAR(pds_free), ph1, wc, kWhereBwdCompute));
-        if (!ok) break;
-      }
-      const uint32_t pt_row = sbase + kPTOff;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_shared_v4(pt_row + tile128_chunk_off(r, c), pack_bf16(pr[8 * c], pr[8 * c + 1]),
-                     pack_bf16(pr[8 * c + 2], pr[8 * c + 3]), pack_bf16(pr[8 * c + 4], pr[8 * c + 5]),
-                     pack_bf16(pr[8 * c + 6], pr[8 * c + 7]));
-      fence_async_smem();
       tc_fence_before();
-      mbar_arrive(BAR(pt_ready));
-      // ---- dS^T = P^T (dP^T - Delta)
+      mbar_arrive(BAR(p_ready));
+      // ---- dS^T = scale P^T (dP^T - Delta) -> shared (bf16, swizzled)
       ok = __all_sync(0xffffffffu, mbar_wait(BAR(dp_full), ph, wc, kWhereBwdCompute));
+      if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(BAR(ds_free), ph1, wc, kWhereBwdCompute));
       if (!ok) break;
       tc_fence_after();
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + 128 + c4 * 32, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = c4 * 32 + i;
-          pr[c] = pr[c] * (__uint_as_float(rr[i]) - dl_s[c]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(BAR(r1_free));
       const uint32_t ds_row = sbase + kDSOff;
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c32 = 2 * ch + cc;               // 32-column chunk
+        uint32_t dp[32], pp[16];
+        tmem_ld32_16(t_r1 + 32 * c32, dp, t_r0 + 64 * ch + 16 * cc, pp);
+        uint32_t w[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_shared_v4(ds_row + tile128_chunk_off(r, c), pack_bf16(pr[8 * c], pr[8 * c + 1]),
-                     pack_bf16(pr[8 * c + 2], pr[8 * c + 3]), pack_bf16(pr[8 * c + 4], pr[8 * c + 5]),
-                     pack_bf16(pr[8 * c + 6], pr[8 * c + 7]));
+        for (int i = 0; i < 32; i += 4) {
+          const float4 dl = dl4[(32 * cc + i) >> 2];
+          const float dv[4] = {dl.x, dl.y, dl.z, dl.w};
+          float d[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t pw = pp[(i + j) >> 1];
+            const float pv = __uint_as_float(((i + j) & 1) ? (pw & 0xFFFF0000u) : (pw << 16));
+            d[j] = p.scale * pv * (__uint_as_float(dp[i + j]) - dv[j]);
+          }
+          w[i >> 1] = pack_bf16(d[0], d[1]);
+          w[(i >> 1) + 1] = pack_bf16(d[2], d[3]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_shared_v4(ds_row + tile128_chunk_off(r, 4 * c32 + k), w[4 * k], w[4 * k + 1],
+                       w[4 * k + 2], w[4 * k + 3]);
+      }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(BAR(ds_ready));
-      // ---- drain dQ (TMEM lane = query row)
+      // ---- drain dQ^T (TMEM lane = head-dim index r, columns = query rows): each
+      // warp instruction adds one 128-byte line (32 consecutive d of one row)
       ok = __all_sync(0xffffffffu, mbar_wait(BAR(dq_full), ph, wc, kWhereBwdCompute));
       if (!ok) break;
       tc_fence_after();
-      const int t = qi * 128 + r;
-      float* dst = p.dq_acc + (static_cast<long>(t) * p.hq + h) * 128;
+      {
+        const int t0 = qi * 128 + 64 * ch;
+        float* dst = p.dq_acc + (static_cast<long>(t0) * p.hq + h) * 128 + r;
+        const long row_stride = static_cast<long>(p.hq) * 128;
+        const int rows = min(64, p.chunk_len - t0);
+        uint32_t rr[64];
+        tmem_ld64(t_r1 + 64 * ch, rr);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + c4 * 32, rr);
-        if (t < p.chunk_len) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            red_add_v4(dst + c4 * 32 + 4 * i, __uint_as_float(rr[4 * i]) * p.scale,
-                       __uint_as_float(rr[4 * i + 1]) * p.scale,
-                       __uint_as_float(rr[4 * i + 2]) * p.scale,
-                       __uint_as_float(rr[4 * i + 3]) * p.scale);
-        }
+        for (int c = 0; c < 64; ++c)
+          if (c < rows) red_add_f32(dst + c * row_stride, __uint_as_float(rr[c]));
       }
       tc_fence_before();
-      mbar_arrive(BAR(r0_free));
+      mbar_arrive(BAR(r1_free));
     }
     // ---- epilogue: dK, dV rows of this key tile into the paged bf16 gradients
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(acc_done), 0, wc, kWhereBwdEpilogue));
@@ -386,28 +418,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         raise_status(p.status, kStatusBounds, kWhereBwdEpilogue);
         write = false;
       }
-      const long row = ((static_cast<long>(slot) * p.hkv + g) * p.page_size + r % p.page_size) * 128;
-#pragma unroll
+      const long row = ((static_cast<long>(slot) * p.hkv + g) * p.page_size + r % p.page_size) * 128
+                       + 64 * ch;
+#pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* pool = which == 0 ? p.dk : p.dv;
-        const float mul = which == 0 ? p.scale : 1.f;
-        const uint32_t tcol = which == 0 ? 384 : 256;
+        const uint32_t tcol = (which == 0 ? 384 : 256) + 64 * ch;
         uint4* dst = reinterpret_cast<uint4*>(pool + row);
+        uint32_t rr[64];
+        tmem_ld64(tmem + lane_base + tcol, rr);
+        if (write) {
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + tcol + c4 * 32, rr);
-          if (write) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 o = dst[c4 * 4 + i];
-              const float* a = reinterpret_cast<const float*>(rr) + 8 * i;
-              o.x = bf16x2_add(o.x, a[0] * mul, a[1] * mul);
-              o.y = bf16x2_add(o.y, a[2] * mul, a[3] * mul);
-              o.z = bf16x2_add(o.z, a[4] * mul, a[5] * mul);
-              o.w = bf16x2_add(o.w, a[6] * mul, a[7] * mul);
-              dst[c4 * 4 + i] = o;
-            }
+          for (int i = 0; i < 8; ++i) {
+            uint4 o = dst[i];
+            const float* a = reinterpret_cast<const float*>(rr) + 8 * i;
+            o.x = bf16x2_add(o.x, a[0], a[1]);
+            o.y = bf16x2_add(o.y, a[2], a[3]);
+            o.z = bf16x2_add(o.z, a[4], a[5]);
+            o.w = bf16x2_add(o.w, a[6], a[7]);
+            dst[i] = o;
           }
         }
       }
@@ -422,12 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef BAR
 }
 
-// Delta[h][t] = dout[t][h] . o[t][h] (0 for the padding rows of the last
-// query tile) and a zeroed fp32 dq accumulator.  Half a warp per (t, h) row.
+// Delta[h][t] = dout[t][h] . o[t][h], lse2[h][t] = lse[h][t] * log2(e); on the
+// padding rows of the last query tile Delta = 0 and lse2 = +inf (so P = 0
+// there).  Also zeroes the fp32 dq accumulator.  Half a warp per (t, h) row.
 __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
-                                const __nv_bfloat16* __restrict__ dout, int hq, int chunk_len,
+                                const __nv_bfloat16* __restrict__ dout,
+                                const float* __restrict__ lse, int hq, int chunk_len,
                                 int padded_len, float* __restrict__ delta,
-                                float* __restrict__ dq_acc) {
+                                float* __restrict__ lse2, float* __restrict__ dq_acc) {
   const long row = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
   const int l16 = threadIdx.x & 15;
   const long n_rows = static_cast<long>(padded_len) * hq;
@@ -449,7 +480,12 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (l16 == 0) delta[static_cast<long>(h) * padded_len + t] = s;
+  if (l16 == 0) {
+    const long o2 = static_cast<long>(h) * padded_len + t;
+    delta[o2] = s;
+    lse2[o2] = t < chunk_len ? lse[static_cast<long>(h) * chunk_len + t] * 1.4426950408889634f
+                             : INFINITY;
+  }
 }
 
 __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
@@ -470,7 +506,7 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* 
 
 size_t bf16_bwd_ws_bytes(int hq, int chunk_len, int head_dim) {
   const size_t padded = static_cast<size_t>((chunk_len + 127) / 128) * 128;
-  return kStatusBytes + align_up(static_cast<size_t>(hq) * padded * 4, 256) +
+  return kStatusBytes + 2 * align_up(static_cast<size_t>(hq) * padded * 4, 256) +
          align_up(static_cast<size_t>(chunk_len) * hq * head_dim * 4, 256);
 }
 
@@ -482,9 +518,10 @@ cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* dout,
   const int padded = n_qtiles * 128;
   char* w = static_cast<char*>(ws);
   int* status = reinterpret_cast<int*>(w);
+  const size_t vec_bytes = align_up(static_cast<size_t>(hq) * padded * 4, 256);
   float* delta = reinterpret_cast<float*>(w + kStatusBytes);
-  float* dq_acc = reinterpret_cast<float*>(w + kStatusBytes +
-                                           align_up(static_cast<size_t>(hq) * padded * 4, 256));
+  float* lse2 = reinterpret_cast<float*>(w + kStatusBytes + vec_bytes);
+  float* dq_acc = reinterpret_cast<float*>(w + kStatusBytes + 2 * vec_bytes);
   CUtensorMap tq, tdo, tk, tv;
   {
     const uint64_t dims[3] = {128, static_cast<uint64_t>(hq), static_cast<uint64_t>(chunk_len)};
@@ -504,15 +541,15 @@ cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* dout,
   {
     const long rows16 = static_cast<long>(padded) * hq * 16;
     bwd_prep_kernel<<<static_cast<unsigned>((rows16 + 255) / 256), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), hq,
-        chunk_len, padded, delta, dq_acc);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, hq,
+        chunk_len, padded, delta, lse2, dq_acc);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   BwdParams p;
   p.sel = sel;
   p.pt = kv.page_table;
-  p.lse = lse;
+  p.lse2 = lse2;
   p.delta = delta;
   p.dq_acc = dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(kv.dk);

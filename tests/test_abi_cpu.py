@@ -122,8 +122,8 @@ def test_select_rejects_bad_pages(lib):
 def test_workspace_sizes(lib):
     kv = _kv(num_pages=32768, num_slots=32768, page_size=128)
     bwd = lib.oomb_workspace_bytes(oomb.OOMB_OP_ATTN_BWD, ctypes.byref(kv), 28, 8192, 0)
-    # status block + Delta [28][8192] + fp32 dq accumulator [8192][28][128]
-    assert bwd == 256 + 28 * 8192 * 4 + 8192 * 28 * 128 * 4
+    # status block + Delta and lse*log2(e) [28][8192] each + fp32 dq accumulator [8192][28][128]
+    assert bwd == 256 + 2 * 28 * 8192 * 4 + 8192 * 28 * 128 * 4
     assert lib.oomb_workspace_bytes(oomb.OOMB_OP_ATTN_FWD, ctypes.byref(kv), 28, 8192, 0) == 256
     sel = lib.oomb_workspace_bytes(oomb.OOMB_OP_SELECT_TOPK, ctypes.byref(kv), 28, 8192, 128)
     assert sel >= 256 + 4 * 32768 * 4
