@@ -57,6 +57,20 @@ def attn_flops(wl, rows=None):
     return 14.0 * wl.head_dim * wl.num_q_heads * pairs_per_head(wl, rows)
 
 
+def max_over_ranks(x, world, device="cpu"):
+    """The slowest rank's value (replicas: the job ends when the last one does)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_replica, ms_slowest, world):
+    """Whole-job throughput in TFLOP/s: every replica's work over the slowest time."""
+    return world * flops_per_replica / ms_slowest / 1e9
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
@@ -179,11 +193,7 @@ def run_ours(args, rank, world, dev):
     total_ms = t_start.elapsed_time(t_end)
     per = {n: statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps))
            for k, n in enumerate(names)}
-    ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(total_ms / args.steps, world, dev)
 
     # end to end through the same C ABI calls with host buffers: per step the
     # chunk's queries and output grads come from pinned host memory and the
@@ -238,7 +248,7 @@ def run_ours(args, rank, world, dev):
     achieved = bwd_flops / per["attn_bwd"] / 1e9
     res = {
         "metric": METRIC,
-        "value": world * flops / ms / 1e9,
+        "value": job_value(flops, ms, world),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,

@@ -4,21 +4,25 @@
 // "Page-level Sparse Attention": the chunk attends the pages chosen by their
 // representative vectors plus its own pages.
 //
-// One CTA computes one 128-row query tile of one query head against its key
-// tiles: first the selected pages (ceil(n_sel * P / 128) tiles, no mask except
-// a ragged last tile), then the chunk's own pages up to the diagonal tile.
-// Roles (192 threads):
-//   warp 0      TMA producer: Q once, then K/V tiles gathered page by page
-//               through the page table (one 2-D box per page and 64-column half)
-//               into a 2-stage ring; also allocates TMEM.
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S
-//               buffers, then O += P_{j-1} V_{j-1}; completion via tcgen05.commit.
-//   warps 2..5  softmax, one thread per query row: reads S_j from TMEM, masks,
-//               online softmax in base 2, writes P_j (bf16) to a 2-deep shared
-//               ring in the 128-byte swizzled K-major layout.  O is rescaled in
-//               TMEM only when a row maximum grows by more than 2^8 (the final
+// One CTA computes two consecutive 128-row query tiles (A, B) of one query
+// head.  Both read the same key tiles -- first the selected pages (ceil(n_sel
+// * P / 128) tiles, masked only in a ragged last tile), then the chunk's own
+// pages up to each tile's diagonal -- so every K/V tile is fetched once for 256
+// query rows.  Roles (320 threads):
+//   warp 0      TMA producer: Q_A, Q_B once; then K_j, V_j page by page through
+//               the page table (one 2-D box per page and 64-column half) into a
+//               5-slot shared ring; also allocates TMEM.
+//   warp 1      MMA issuer (one thread): per key tile j
+//                 S_A = Q_A K_j^T, S_B = Q_B K_j^T        (SS, into TMEM)
+//                 O_A += P_A V_j, O_B += P_B V_j          (P from TMEM)
+//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B, one thread per
+//               query row: row maximum over S in TMEM, exponentials in base 2,
+//               P written back over S as bf16 pairs.  O is rescaled in TMEM only
+//               when a row maximum grows by more than 2^8 (the final
 //               normalisation uses the same running maximum, so this is exact).
-// TMEM: S0 [0,128), S1 [128,256), O [256,384) of a 512-column allocation.
+// While one tile's softmax runs the tensor pipe works on the other tile.
+// TMEM (512 columns): S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384),
+// O_B [384,512).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,26 +35,23 @@
 namespace oomb {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKOff = kTileBytes;            // 2 stages
-constexpr uint32_t kVOff = 3 * kTileBytes;        // 2 stages
-constexpr uint32_t kPOff = 5 * kTileBytes;        // 2 buffers
-constexpr uint32_t kBarOff = 7 * kTileBytes;
-constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;   // + alignment slack
+constexpr int kThreads = 320;
+constexpr int kSlots = 5;                         // K/V ring
+constexpr uint32_t kQOff = 0;                     // Q_A, Q_B
+constexpr uint32_t kRingOff = 2 * kTileBytes;
+constexpr uint32_t kBarOff = kRingOff + kSlots * kTileBytes;
+constexpr uint32_t kSmemBytes = kBarOff + 256;    // base is 1024-aligned by declaration
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2];
-  uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full[2];
-  uint64_t o_done[2];
+  uint64_t slot_full[kSlots], slot_empty[kSlots];
+  uint64_t s_full[2], p_ready[2], pv_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct FwdParams {
   const int32_t* sel;
@@ -59,7 +60,7 @@ struct FwdParams {
   float* lse;
   int* status;
   int n_sel, hq, hkv, page_size, chunk_len, chunk_start, num_slots;
-  int n_qtiles, t_sel;                 // query tiles, selected key tiles
+  int n_qtiles, n_pairs, t_sel;        // query tiles, tile pairs, selected key tiles
   float scale_log2;
   uint64_t wait_ns;
 };
@@ -74,35 +75,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   const uint32_t bbase = sbase + kBarOff;
 #define BAR(f) bar_addr(bbase, &bars->f, bars)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest query tiles (most own key tiles) first
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / p.hq;
+  if (sbase & 1023u) {          // the swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) raise_status(p.status, kStatusBounds, kWhereFwdProducer);
+    return;
+  }
+  // heaviest pairs (most own key tiles) first
+  const int pr = p.n_pairs - 1 - static_cast<int>(blockIdx.x) / p.hq;
   const int h = static_cast<int>(blockIdx.x) % p.hq;
   const int g = h / (p.hq / p.hkv);
-  const int n_tiles = p.t_sel + qt + 1;
+  const int qt_a = 2 * pr, qt_b = 2 * pr + 1;
+  const bool has_b = qt_b < p.n_qtiles;
+  const int n_a = p.t_sel + qt_a + 1;              // key tiles of tile A
+  const int n_b = has_b ? p.t_sel + qt_b + 1 : 0;  // key tiles of tile B
+  const int n_tiles = has_b ? n_b : n_a;
   const int ppt = 128 / p.page_size;               // pages per key tile
   const int own_page0 = p.chunk_start / p.page_size;
   const int n_own_pages = p.chunk_len / p.page_size;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(q_full), 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(BAR(slot_full[i]), 1);
+      mbar_init(BAR(slot_empty[i]), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(BAR(k_full[i]), 1);
-      mbar_init(BAR(k_empty[i]), 1);
-      mbar_init(BAR(v_full[i]), 1);
-      mbar_init(BAR(v_empty[i]), 1);
       mbar_init(BAR(s_full[i]), 1);
-      mbar_init(BAR(s_empty[i]), 128);
-      mbar_init(BAR(p_full[i]), 128);
-      mbar_init(BAR(o_done[i]), 1);
+      mbar_init(BAR(p_ready[i]), 128);
+      mbar_init(BAR(pv_done[i]), 1);
     }
     mbar_init(BAR(drain), 1);
     bars->abort_flag = 0;
@@ -124,14 +130,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int issued = 0;                              // K/V tiles issued
-      mbar_arrive_expect_tx(BAR(q_full), kTileBytes);
-      tma_load_3d(sbase + kQOff, &tm_q, BAR(q_full), 0, h, qt * 128);
-      tma_load_3d(sbase + kQOff + kHalfBytes, &tm_q, BAR(q_full), 64, h, qt * 128);
+      mbar_arrive_expect_tx(BAR(q_full), (has_b ? 2u : 1u) * kTileBytes);
+      for (int t = 0; t < (has_b ? 2 : 1); ++t)
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(sbase + kQOff + t * kTileBytes + hf * kHalfBytes, &tm_q, BAR(q_full),
+                      hf * 64, h, (qt_a + t) * 128);
       const int32_t* sel_g = p.sel + static_cast<long>(g) * p.n_sel;
+      int issued = 0;                              // ring loads issued (K_0, V_0, K_1, ...)
       for (int j = 0; j < n_tiles; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
         int rows[8];
         for (int u = 0; u < ppt; ++u) {
           int lp;
@@ -153,32 +159,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           rows[u] = (slot * p.hkv + g) * p.page_size;
         }
-        if (!mbar_wait(BAR(k_empty[s]), ph ^ 1, wc, kWhereFwdProducer)) break;
-        mbar_arrive_expect_tx(BAR(k_full[s]), kTileBytes);
-        for (int u = 0; u < ppt; ++u)
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_2d(sbase + kKOff + s * kTileBytes + hf * kHalfBytes + u * p.page_size * 128,
-                        &tm_k, BAR(k_full[s]), hf * 64, rows[u]);
-        if (!mbar_wait(BAR(v_empty[s]), ph ^ 1, wc, kWhereFwdProducer)) {
-          issued = 2 * j + 1;
-          break;
+        bool ok = true;
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const int q = 2 * j + kv;
+          const int sl = q % kSlots;
+          const uint32_t phe = ((q / kSlots) & 1) ^ 1;
+          if (!(ok = mbar_wait(BAR(slot_empty[sl]), phe, wc, kWhereFwdProducer))) break;
+          const uint32_t dst = sbase + kRingOff + sl * kTileBytes;
+          mbar_arrive_expect_tx(BAR(slot_full[sl]), kTileBytes);
+          for (int u = 0; u < ppt; ++u)
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_2d(dst + hf * kHalfBytes + u * p.page_size * 128, kv ? &tm_v : &tm_k,
+                          BAR(slot_full[sl]), hf * 64, rows[u]);
+          ++issued;
         }
-        mbar_arrive_expect_tx(BAR(v_full[s]), kTileBytes);
-        for (int u = 0; u < ppt; ++u)
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_2d(sbase + kVOff + s * kTileBytes + hf * kHalfBytes + u * p.page_size * 128,
-                        &tm_v, BAR(v_full[s]), hf * 64, rows[u]);
-        issued = 2 * j + 2;
+        if (!ok) break;
       }
       if (bars->abort_flag) {
         // unwinding: let every copy this thread issued land before the CTA exits
         mbar_drain_wait(BAR(q_full), 0);
-        const int nk = (issued + 1) / 2, nv = issued / 2;   // K/V tiles issued
-        for (int s = 0; s < 2; ++s) {
-          const int lastk = (nk - 1 - s) >= 0 ? ((nk - 1 - s) / 2) * 2 + s : -1;
-          if (lastk >= 0) mbar_drain_wait(BAR(k_full[s]), (lastk >> 1) & 1);
-          const int lastv = (nv - 1 - s) >= 0 ? ((nv - 1 - s) / 2) * 2 + s : -1;
-          if (lastv >= 0) mbar_drain_wait(BAR(v_full[s]), (lastv >> 1) & 1);
+        for (int sl = 0; sl < kSlots; ++sl) {
+          int last = -1;
+          for (int q = sl; q < issued; q += kSlots) last = q;
+          if (last >= 0) mbar_drain_wait(BAR(slot_full[sl]), (last / kSlots) & 1);
         }
       }
     }
@@ -187,39 +190,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
-      const uint32_t t_o = tmem + 256;
       bool ok = mbar_wait(BAR(q_full), 0, wc, kWhereFwdMma);
-      auto issue_pv = [&](int jj) -> bool {
-        const int s = jj & 1;
-        const uint32_t ph = (jj >> 1) & 1;
-        if (!mbar_wait(BAR(p_full[s]), ph, wc, kWhereFwdMma)) return false;
-        if (!mbar_wait(BAR(v_full[s]), ph, wc, kWhereFwdMma)) return false;
-        tc_fence_after();
-        const uint32_t pa = sbase + kPOff + s * kTileBytes;
-        const uint32_t va = sbase + kVOff + s * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_o, desc_kmajor(pa, kk), desc_mnmajor(va, kk), kIdPV, (jj > 0 || kk > 0));
-        umma_commit(BAR(o_done[s]));
-        umma_commit(BAR(v_empty[s]));
-        return true;
-      };
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(BAR(k_full[s]), ph, wc, kWhereFwdMma)) { ok = false; break; }
-        if (!mbar_wait(BAR(s_empty[s]), ph ^ 1, wc, kWhereFwdMma)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t ka = sbase + kKOff + s * kTileBytes;
+        const int qk = 2 * j, qv = 2 * j + 1;
+        const int sk = qk % kSlots, sv = qv % kSlots;
+        // S_X = Q_X K_j^T (S_X may be overwritten once PV_X of tile j-1 is done)
+        if (!(ok = mbar_wait(BAR(slot_full[sk]), (qk / kSlots) & 1, wc, kWhereFwdMma))) break;
+        const uint32_t ka = sbase + kRingOff + sk * kTileBytes;
+        for (int t = 0; t < 2; ++t) {
+          if (j >= (t == 0 ? n_a : n_b)) continue;
+          if (j > 0 && !(ok = mbar_wait(BAR(pv_done[t]), (j - 1) & 1, wc, kWhereFwdMma))) break;
+          tc_fence_after();
+          const uint32_t qa = sbase + kQOff + t * kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + s * 128, desc_kmajor(sbase + kQOff, kk), desc_kmajor(ka, kk), kIdQK,
-                  kk > 0);
-        umma_commit(BAR(s_full[s]));
-        umma_commit(BAR(k_empty[s]));
-        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(tmem + t * 128, desc_kmajor(qa, kk), desc_kmajor(ka, kk), kIdQK, kk > 0);
+          umma_commit(BAR(s_full[t]));
+        }
+        if (!ok) break;
+        umma_commit(BAR(slot_empty[sk]));
+        // O_X += P_X V_j (P_X in TMEM as bf16 pairs over S_X, 8 columns per k-step)
+        if (!(ok = mbar_wait(BAR(slot_full[sv]), (qv / kSlots) & 1, wc, kWhereFwdMma))) break;
+        const uint32_t va = sbase + kRingOff + sv * kTileBytes;
+        for (int t = 0; t < 2; ++t) {
+          if (j >= (t == 0 ? n_a : n_b)) continue;
+          if (!(ok = mbar_wait(BAR(p_ready[t]), j & 1, wc, kWhereFwdMma))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_mnmajor(va, kk), kIdPV,
+                    (j > 0 || kk > 0));
+          umma_commit(BAR(pv_done[t]));
+        }
+        if (!ok) break;
+        umma_commit(BAR(slot_empty[sv]));
       }
-      if (ok) ok = issue_pv(n_tiles - 1);
       if (!ok) {
         umma_commit(BAR(drain));
         mbar_drain_wait(BAR(drain), 0);
@@ -227,56 +232,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
+    const int tsel = (warp - 2) >> 2;              // 0: tile A, 1: tile B
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;                  // row of the query tile
+    const int qt = qt_a + tsel;
     const int t = qt * 128 + r;                    // chunk row
+    const int n_mine = tsel == 0 ? n_a : n_b;
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t t_o = tmem + lane_base + 256;
+    const uint32_t t_s = tmem + lane_base + tsel * 128;
+    const uint32_t t_o = tmem + lane_base + 256 + tsel * 128;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full[b]), ph, wc, kWhereFwdSoftmax));
+    for (int j = 0; j < n_mine; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full[tsel]), j & 1, wc, kWhereFwdSoftmax));
       if (!ok) break;
       tc_fence_after();
-      float x[128];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + b * 128 + c4 * 32, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c4 * 32 + i] = __uint_as_float(rr[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(BAR(s_empty[b]));
-      // valid columns are [0, lim)
+      // valid columns are [0, lim); `masked` is uniform over the warp group
       int lim = 128;
+      bool masked = false;
       if (j < p.t_sel) {
         const int rem = (p.n_sel - j * ppt) * p.page_size;
-        lim = rem < 128 ? rem : 128;
+        if (rem < 128) {
+          lim = rem;
+          masked = true;
+        }
       } else if (j - p.t_sel == qt) {
         lim = r + 1;
+        masked = true;
       }
-      float mt = -INFINITY;
+      // pass 1: row maximum of the raw scores (scale > 0 commutes with max)
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(t_s + c4 * 32, rr);
+        if (masked) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        x[c] = (c < lim) ? x[c] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[c]);
+          for (int i = 0; i < 32; i += 4) {
+            const int c = c4 * 32 + i;
+            mx0 = fmaxf(mx0, c < lim ? __uint_as_float(rr[i]) : -INFINITY);
+            mx1 = fmaxf(mx1, c + 1 < lim ? __uint_as_float(rr[i + 1]) : -INFINITY);
+            mx2 = fmaxf(mx2, c + 2 < lim ? __uint_as_float(rr[i + 2]) : -INFINITY);
+            mx3 = fmaxf(mx3, c + 3 < lim ? __uint_as_float(rr[i + 3]) : -INFINITY);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            mx0 = fmaxf(mx0, __uint_as_float(rr[i]));
+            mx1 = fmaxf(mx1, __uint_as_float(rr[i + 1]));
+            mx2 = fmaxf(mx2, __uint_as_float(rr[i + 2]));
+            mx3 = fmaxf(mx3, __uint_as_float(rr[i + 3]));
+          }
+        }
       }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
       if (j == 0) {
         m = mt;
       } else {
+        // O_X is stable here: S_X of tile j was issued after PV_X of tile j-1 completed
         const float m_new = fmaxf(m, mt);
         const bool need = m_new > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          const int pb = (j - 1) & 1;
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(BAR(o_done[pb]), ((j - 1) >> 1) & 1, wc, kWhereFwdSoftmax));
-          if (!ok) break;
-          tc_fence_after();
           const float alpha = need ? ex2(m - m_new) : 1.f;
-#pragma unroll
+#pragma unroll 1
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t rr[32];
             tmem_ld32(t_o + c4 * 32, rr);
@@ -284,48 +302,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
             tmem_st32(t_o + c4 * 32, rr);
           }
-          tmem_st_wait();
           if (need) {
             l *= alpha;
             m = m_new;
           }
         }
       }
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(BAR(o_done[b]), ((j - 2) >> 1) & 1, wc, kWhereFwdSoftmax));
-        if (!ok) break;
-      }
-      // P_j row r -> shared, bf16, swizzled K-major (keys are the K dimension)
-      const uint32_t prow = sbase + kPOff + b * kTileBytes;
-      float rs = 0.f;
+      // pass 2: P = exp2(s * scale_log2 - m) -> bf16 pairs over S (chunk c4 is
+      // written to columns [16 c4, 16 c4 + 16), all of which were already read)
+      const float neg_m = -m;
+      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(t_s + c4 * 32, rr);
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float e[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          e[i] = ex2(x[c * 8 + i] - m);
-          rs += e[i];
+        for (int i = 0; i < 32; i += 2) {
+          float x0 = fmaf(__uint_as_float(rr[i]), p.scale_log2, neg_m);
+          float x1 = fmaf(__uint_as_float(rr[i + 1]), p.scale_log2, neg_m);
+          if (masked && c4 * 32 + i >= lim) x0 = -INFINITY;
+          if (masked && c4 * 32 + i + 1 >= lim) x1 = -INFINITY;
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          if (i & 2) {
+            rs2 += e0;
+            rs3 += e1;
+          } else {
+            rs0 += e0;
+            rs1 += e1;
+          }
+          pk[i >> 1] = pack_bf16(e0, e1);
         }
-        st_shared_v4(prow + tile128_chunk_off(r, c), pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]),
-                     pack_bf16(e[4], e[5]), pack_bf16(e[6], e[7]));
+        tmem_st16(t_s + c4 * 16, pk);
       }
-      l += rs;
-      fence_async_smem();
+      tmem_st_wait();
+      l += (rs0 + rs1) + (rs2 + rs3);
       tc_fence_before();
-      mbar_arrive(BAR(p_full[b]));
+      mbar_arrive(BAR(p_ready[tsel]));
     }
-    if (ok) {
-      const int jl = n_tiles - 1;
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(BAR(o_done[jl & 1]), (jl >> 1) & 1, wc, kWhereFwdSoftmax));
+    if (ok && n_mine > 0) {
+      const int jl = n_mine - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(pv_done[tsel]), jl & 1, wc, kWhereFwdSoftmax));
     }
-    if (ok) {
+    if (ok && n_mine > 0) {
       tc_fence_after();
       const float inv = 1.f / l;
       const bool row_ok = t < p.chunk_len;
       uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<long>(t) * p.hq + h) * 128);
-#pragma unroll
+#pragma unroll 1
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t rr[32];
         tmem_ld32(t_o + c4 * 32, rr);
@@ -388,6 +412,7 @@ cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t*
   p.chunk_start = chunk_start;
   p.num_slots = kv.num_slots;
   p.n_qtiles = (chunk_len + 127) / 128;
+  p.n_pairs = (p.n_qtiles + 1) / 2;
   p.t_sel = (n_sel * kv.page_size + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = wait_ns;
@@ -398,7 +423,7 @@ cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t*
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  sparse_attn_fwd_kernel<<<p.n_qtiles * hq, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  sparse_attn_fwd_kernel<<<p.n_pairs * hq, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -136,6 +136,7 @@ cudaError_t reps_dispatch(const KvDesc& kv, int first_page, int n_pages, float* 
 // float4 column, then the 7 sub-sums in order.
 // ---------------------------------------------------------------------------
 constexpr int kQbarThreads = 896;
+constexpr int kTailMax = 12;                      // partials per sub-slice of the tree
 
 template <typename T>
 __global__ void __launch_bounds__(kQbarThreads) qbar_kernel(const T* __restrict__ q, int chunk_len,
@@ -161,12 +162,13 @@ __global__ void __launch_bounds__(kQbarThreads) qbar_kernel(const T* __restrict_
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     const T* base = q + static_cast<size_t>(col) * E;
-    int t = t0 + sub;
-    for (; t + (U - 1) * R < t1; t += U * R) {
+    // rounds of U predicated loads, all in flight together (no serial remainder)
+    for (int t = t0 + sub; t < t1; t += U * R) {
       uint4 v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        v[u] = ldg_stream(base + static_cast<size_t>(t + u * R) * row_elems);
+        v[u] = (t + u * R < t1) ? ldg_stream(base + static_cast<size_t>(t + u * R) * row_elems)
+                                : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         float f[E];
@@ -174,12 +176,6 @@ __global__ void __launch_bounds__(kQbarThreads) qbar_kernel(const T* __restrict_
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] += f[e];
       }
-    }
-    for (; t < t1; t += R) {
-      float f[E];
-      Vec<T>::to_float(ldg_stream(base + static_cast<size_t>(t) * row_elems), f);
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += f[e];
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) sm[sub * row_elems + col * E + e] = acc[e];
@@ -212,11 +208,18 @@ __global__ void __launch_bounds__(kQbarThreads) qbar_kernel(const T* __restrict_
     const int c4 = threadIdx.x % n_out4, s = threadIdx.x / n_out4;
     const int per = (nb + n_sub - 1) / n_sub;
     const int b0 = s * per, b1 = min(nb, b0 + per);
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4* p4 = reinterpret_cast<const float4*>(partials);
-    for (int b = b0; b < b1; ++b) {
-      const float4 x = __ldcg(p4 + static_cast<size_t>(b) * n_out4 + c4);
-      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = b0; base < b1; base += kTailMax) {   // kTailMax loads in flight
+      float4 x[kTailMax];
+#pragma unroll
+      for (int u = 0; u < kTailMax; ++u)
+        x[u] = (base + u < b1) ? __ldcg(p4 + static_cast<size_t>(base + u) * n_out4 + c4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kTailMax; ++u) {
+        a.x += x[u].x; a.y += x[u].y; a.z += x[u].z; a.w += x[u].w;
+      }
     }
     red[s * n_out4 + c4] = a;
   }
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(256) page_scores_kernel(const float* __restric
                                                           float* __restrict__ scores) {
   constexpr int L = D / 4;                        // lanes per row
   constexpr int RPW = 32 / L;                     // rows per warp-step
-  constexpr int U = 4;
+  constexpr int U = 8;
   __shared__ float4 qs[16 * L];                   // hkv <= 16
   for (int i = threadIdx.x; i < hkv * L; i += blockDim.x)
     qs[i] = reinterpret_cast<const float4*>(qbar)[i];
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   __shared__ int hist[2048];
   __shared__ int warp_tot[32];
   __shared__ int total;
-  __shared__ uint32_t sh_prefix;
+  __shared__ uint32_t sh_prefix, sh_min, sh_max;
   __shared__ int sh_need;
   const int g = blockIdx.x;
   const float* sc = scores + static_cast<long>(g) * num_pages;
@@ -347,18 +350,56 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     return;
   }
   const bool cached = n_cand <= kTopkSmemKeys;
-  if (cached)
-    for (int i = threadIdx.x; i < n_cand; i += blockDim.x) keys_sm[i] = order_key(__ldcg(sc + i));
+  if (threadIdx.x == 0) {
+    sh_min = 0xFFFFFFFFu;
+    sh_max = 0u;
+  }
+  __syncthreads();
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  constexpr int kU = 8;                           // loads in flight per thread
+  for (int base = threadIdx.x; base < n_cand; base += kU * blockDim.x) {
+    float v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * blockDim.x;
+      v[u] = i < n_cand ? __ldcg(sc + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * blockDim.x;
+      if (i < n_cand) {
+        const uint32_t key = order_key(v[u]);
+        if (cached) keys_sm[i] = key;
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMin(&sh_min, kmin);
+    atomicMax(&sh_max, kmax);
+  }
   __syncthreads();
   auto key_at = [&](int i) -> uint32_t { return cached ? keys_sm[i] : order_key(__ldcg(sc + i)); };
 
-  uint32_t prefix = 0, mask = 0;
+  // Every key shares the bits above the highest bit where min and max differ:
+  // the radix digits start just below that common prefix, so the first
+  // histogram spreads even when all scores have similar magnitude.
+  const uint32_t diff = sh_min ^ sh_max;
+  int lo_bit = diff ? 32 - __clz(diff) : 0;       // bits [0, lo_bit) still vary
+  const uint32_t low = (lo_bit >= 32) ? 0xFFFFFFFFu : ((1u << lo_bit) - 1u);
+  uint32_t prefix = sh_max & ~low;                // the common high bits
+  uint32_t mask = ~low;
   int need = k;                                   // still to take at or below `prefix`
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass], nbins = 1 << widths[pass];
-    for (int i = threadIdx.x; i < 2048; i += blockDim.x) hist[i] = 0;
+  while (lo_bit > 0) {
+    const int width = lo_bit < 11 ? lo_bit : 11;
+    const int sh = lo_bit - width, nbins = 1 << width;
+    for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n_cand; i += blockDim.x) {
       const uint32_t key = key_at(i);
@@ -367,15 +408,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     __syncthreads();
     // Bin counts from the top: thread t owns bins [2t, 2t+1] of the reversed order.
     const int b_hi = nbins - 1 - 2 * static_cast<int>(threadIdx.x);
-    const int c0 = (2 * threadIdx.x < static_cast<unsigned>(nbins)) ? hist[b_hi] : 0;
-    const int c1 = (2 * threadIdx.x + 1 < static_cast<unsigned>(nbins)) ? hist[b_hi - 1] : 0;
+    const int c0 = (2 * static_cast<int>(threadIdx.x) < nbins) ? hist[b_hi] : 0;
+    const int c1 = (2 * static_cast<int>(threadIdx.x) + 1 < nbins) ? hist[b_hi - 1] : 0;
     const int before = block_excl_scan(c0 + c1, warp_tot, &total);
     // the bin where the running count from the top first reaches `need`
-    if (2 * threadIdx.x < static_cast<unsigned>(nbins)) {
+    if (2 * static_cast<int>(threadIdx.x) < nbins) {
       if (before < need && before + c0 >= need) {
         sh_prefix = prefix | (static_cast<uint32_t>(b_hi) << sh);
         sh_need = need - before;
-      } else if (2 * threadIdx.x + 1 < static_cast<unsigned>(nbins) && before + c0 < need &&
+      } else if (2 * static_cast<int>(threadIdx.x) + 1 < nbins && before + c0 < need &&
                  before + c0 + c1 >= need) {
         sh_prefix = prefix | (static_cast<uint32_t>(b_hi - 1) << sh);
         sh_need = need - before - c0;
@@ -385,6 +426,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     prefix = sh_prefix;
     need = sh_need;
     mask |= static_cast<uint32_t>(nbins - 1) << sh;
+    lo_bit = sh;
     __syncthreads();
   }
   // prefix == T (the k-th key), need == how many keys equal to T are kept.

@@ -45,6 +45,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread is suspended (issues nothing) until the
+// phase completes or `hint_ns` nanoseconds pass, so waiting warps leave the
+// issue slots to the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -71,20 +87,19 @@ __device__ __forceinline__ void raise_status(int* status, int code, int where) {
   }
 }
 
+constexpr uint32_t kSleepHintNs = 200000;   // re-check abort flag and limit every 0.2 ms
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                           int where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  uint32_t n = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++n & 15u) == 0) {
-      if (*c.abort_flag) return false;
-      if (global_timer_ns() - t0 > c.limit_ns) {
-        raise_status(c.status, kStatusTimeout, where);
-        *c.abort_flag = 1;
-        return false;
-      }
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*c.abort_flag) return false;
+    if (global_timer_ns() - t0 > c.limit_ns) {
+      raise_status(c.status, kStatusTimeout, where);
+      *c.abort_flag = 1;
+      return false;
     }
   }
 }
@@ -93,7 +108,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 // independent of the (possibly tiny, test-set) limit of the normal waits.
 __device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
     if (global_timer_ns() - t0 > 2000000000ull) return false;
   }
   return true;
