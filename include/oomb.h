@@ -128,6 +128,30 @@ oomb_status oomb_select_topk(const void *q, int32_t num_q_heads, int32_t chunk_l
                              int32_t top_k, int32_t *sel, float *scores_opt, void *ws,
                              size_t ws_bytes, void *stream);
 
+/* Top-K page selection exactly as oomb_select_topk, for callers that cannot
+ * allocate device memory -- for example code running inside a CUDA graph
+ * whose memory is fixed up front, or a host framework that owns every device
+ * allocation and hands this library only its input and output buffers.  The
+ * paper has no counterpart; it is a property of this library's interface.
+ * Instead of a workspace argument the call uses a scratch array inside the
+ * library: a file-scope device array of OOMB_NOALLOC_SCRATCH_BYTES (4 MiB),
+ * which every GPU that loads the library holds until the process exits.  It
+ * must hold oomb_workspace_bytes(OOMB_OP_SELECT_TOPK, ...) for these shapes
+ * (about 256 B + 2.4 KiB * Hkv * D / 16 + 4 B * Hkv * num_pages); larger
+ * requests return OOMB_ERR_INVALID_ARG before anything is launched.  The
+ * first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  The call
+ * never calls cudaMalloc, cudaFree or any allocating routine.  All calls
+ * share the one array, which keeps the last call's contents: the call clears
+ * the part that must start at zero, and calls that overlap on the GPU (other
+ * streams, other host threads) race on it -- serialise them.  The selection
+ * kernels record no device-side status, so there is no status word to read. */
+#define OOMB_NOALLOC_SCRATCH_BYTES (4u << 20)
+oomb_status oomb_select_topk_noalloc(const void *q, int32_t num_q_heads, int32_t chunk_len,
+                                     int32_t chunk_start, const float *reps,
+                                     const oomb_paged_kv *kv, int32_t top_k, int32_t *sel,
+                                     float *scores_opt, void *stream);
+
 /* Step 3 -- sparse attention forward (Page-level Sparse Attention item).
  * For query head h (KV head g) and chunk row t (position p = chunk_start+t)
  * the keys are all tokens of the n_sel pages sel[g][*] plus the chunk's own

@@ -6,7 +6,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
+#include "oomb.h"
 #include "oomb_internal.h"
 #include "sm100.cuh"
 
@@ -540,6 +542,51 @@ cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, 
   }
   topk_kernel<<<hkv, kTopkThreads, ksm, st>>>(scores, num_pages, n_cand, top_k, sel);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Selection without a caller workspace: the scratch is this file-scope device
+// array.  Host code may not pass the symbol itself to a kernel (on the host it
+// names a host-side stand-in), so its device address is looked up once per
+// device, with that device current, and cached.
+// ---------------------------------------------------------------------------
+namespace {
+__device__ __align__(256) unsigned char g_select_scratch[OOMB_NOALLOC_SCRATCH_BYTES];
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+cudaError_t select_scratch_addr(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_select_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = addr;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_select_topk_noalloc(const void* q, bool bf16, int hq, int chunk_len,
+                                       int n_cand, const float* reps, int num_pages, int hkv,
+                                       int head_dim, int top_k, int32_t* sel, float* scores_opt,
+                                       bool* too_big, cudaStream_t st) {
+  *too_big = select_ws_bytes(num_pages, hkv, head_dim) > OOMB_NOALLOC_SCRATCH_BYTES;
+  if (*too_big) return cudaSuccess;
+  void* scratch = nullptr;
+  cudaError_t e = select_scratch_addr(&scratch);
+  if (e != cudaSuccess) return e;
+  // the status block (with the query-summary ticket counter) must start at zero
+  e = cudaMemsetAsync(scratch, 0, kStatusBytes, st);
+  if (e != cudaSuccess) return e;
+  return launch_select_topk(q, bf16, hq, chunk_len, n_cand, reps, num_pages, hkv, head_dim,
+                            top_k, sel, scores_opt, scratch, st);
 }
 
 cudaError_t launch_validate_page_table(const int32_t* pt, int num_pages, int num_slots,

@@ -248,6 +248,38 @@ oomb_status oomb_select_topk(const void* q, int32_t num_q_heads, int32_t chunk_l
   return e == cudaSuccess ? OOMB_OK : cuda_fail(e, "oomb_select_topk launch");
 }
 
+oomb_status oomb_select_topk_noalloc(const void* q, int32_t num_q_heads, int32_t chunk_len,
+                                     int32_t chunk_start, const float* reps,
+                                     const oomb_paged_kv* kv, int32_t top_k, int32_t* sel,
+                                     float* scores_opt, void* stream) {
+  oomb_status s = check_kv(kv);
+  if (s != OOMB_OK) return s;
+  s = check_chunk(kv, num_q_heads, chunk_len, chunk_start);
+  if (s != OOMB_OK) return s;
+  if (!q || !reps) return fail(OOMB_ERR_INVALID_ARG, "q and reps must be set");
+  if (!aligned(q, 16) || !aligned(reps, 16) || (scores_opt && !aligned(scores_opt, 16)))
+    return fail(OOMB_ERR_INVALID_ARG, "q, reps and scores must be 16-byte aligned");
+  if (top_k < 0) return fail(OOMB_ERR_INVALID_ARG, "top_k %d < 0", top_k);
+  const int n_cand = chunk_start / kv->page_size;
+  const int n_sel = top_k < n_cand ? top_k : n_cand;
+  if (n_sel > 0 && !sel) return fail(OOMB_ERR_INVALID_ARG, "sel is NULL");
+  const int vec_elems = kv->dtype == OOMB_BF16 ? 8 : 4;
+  if (static_cast<long long>(num_q_heads) * kv->head_dim / vec_elems > 896)
+    return fail(OOMB_ERR_UNSUPPORTED, "num_q_heads * head_dim too large for the query summary");
+  bool too_big = false;
+  cudaError_t e = oomb::launch_select_topk_noalloc(
+      q, kv->dtype == OOMB_BF16, num_q_heads, chunk_len, n_cand, reps, kv->num_pages,
+      kv->num_kv_heads, kv->head_dim, n_sel, sel, scores_opt, &too_big,
+      static_cast<cudaStream_t>(stream));
+  if (too_big)
+    return fail(OOMB_ERR_INVALID_ARG,
+                "selection needs %zu bytes of scratch; the fixed scratch holds %u bytes "
+                "(use oomb_select_topk with a workspace)",
+                oomb::select_ws_bytes(kv->num_pages, kv->num_kv_heads, kv->head_dim),
+                OOMB_NOALLOC_SCRATCH_BYTES);
+  return e == cudaSuccess ? OOMB_OK : cuda_fail(e, "oomb_select_topk_noalloc");
+}
+
 oomb_status oomb_sparse_attn_fwd(const void* q, const oomb_paged_kv* kv, const int32_t* sel,
                                  int32_t n_sel, int32_t num_q_heads, int32_t chunk_len,
                                  int32_t chunk_start, float scale, void* o, float* lse, void* ws,

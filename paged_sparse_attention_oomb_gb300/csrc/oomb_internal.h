@@ -50,6 +50,12 @@ size_t select_ws_bytes(int num_pages, int hkv, int head_dim);
 cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, int n_cand,
                                const float* reps, int num_pages, int hkv, int head_dim, int top_k,
                                int32_t* sel, float* scores_opt, void* ws, cudaStream_t st);
+// The selection with its scratch in a fixed device array of the library
+// (oomb_select_topk_noalloc); sets *too_big when the shapes need more.
+cudaError_t launch_select_topk_noalloc(const void* q, bool bf16, int hq, int chunk_len,
+                                       int n_cand, const float* reps, int num_pages, int hkv,
+                                       int head_dim, int top_k, int32_t* sel, float* scores_opt,
+                                       bool* too_big, cudaStream_t st);
 cudaError_t launch_validate_page_table(const int32_t* pt, int num_pages, int num_slots,
                                        uint32_t* bitmap, int* status, cudaStream_t st);
 cudaError_t launch_debug_wait(int* status, uint64_t limit_ns, cudaStream_t st);

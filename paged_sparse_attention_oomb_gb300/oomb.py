@@ -25,7 +25,8 @@ OOMB_OP_ATTN_FWD, OOMB_OP_ATTN_BWD = 3, 4
 
 EXPORTED = [
     "oomb_workspace_bytes", "oomb_validate_page_table_host", "oomb_validate_page_table",
-    "oomb_page_reps", "oomb_select_topk", "oomb_sparse_attn_fwd", "oomb_sparse_attn_bwd",
+    "oomb_page_reps", "oomb_select_topk", "oomb_select_topk_noalloc", "oomb_sparse_attn_fwd",
+    "oomb_sparse_attn_bwd",
     "oomb_device_status", "oomb_set_wait_limit_ns", "oomb_debug_wait_unset_flag",
     "oomb_status_string", "oomb_last_error",
 ]
@@ -68,6 +69,7 @@ def load():
         "oomb_validate_page_table": (ctypes.c_int, [kvp, vp, sz, vp]),
         "oomb_page_reps": (ctypes.c_int, [kvp, i32, i32, vp, vp, sz, vp]),
         "oomb_select_topk": (ctypes.c_int, [vp, i32, i32, i32, vp, kvp, i32, vp, vp, vp, sz, vp]),
+        "oomb_select_topk_noalloc": (ctypes.c_int, [vp, i32, i32, i32, vp, kvp, i32, vp, vp, vp]),
         "oomb_sparse_attn_fwd": (ctypes.c_int, [vp, kvp, vp, i32, i32, i32, i32, ctypes.c_float,
                                                 vp, vp, vp, sz, vp]),
         "oomb_sparse_attn_bwd": (ctypes.c_int, [vp, vp, vp, vp, kvp, vp, i32, i32, i32, i32,
@@ -161,6 +163,16 @@ def oomb_select_topk(q, chunk_start, reps, kv: PagedKV, top_k, sel, ws, scores=N
                                    _stream(stream)))
 
 
+def oomb_select_topk_noalloc(q, chunk_start, reps, kv: PagedKV, top_k, sel, scores=None,
+                             stream=None):
+    """oomb_select_topk without a workspace (scratch inside the library; see oomb.h)."""
+    s = kv.struct()
+    c, hq, _ = q.shape
+    _check(load().oomb_select_topk_noalloc(_ptr(q), hq, c, chunk_start, _ptr(reps),
+                                           ctypes.byref(s), top_k, _ptr(sel), _ptr(scores),
+                                           _stream(stream)))
+
+
 def oomb_sparse_attn_fwd(q, kv: PagedKV, sel, n_sel, chunk_start, o, lse, ws, scale=0.0,
                          stream=None):
     s = kv.struct()
@@ -235,3 +247,4 @@ def sparse_attention_step(q, dout, kv: PagedKV, chunk_start, top_k, reps=None, s
         if code != OOMB_OK:
             raise OombError(code, f"device status (where {where}, block {blk})")
     return dict(reps=reps, sel=sel[:, :n_sel], o=o, lse=lse, dq=dq)
+

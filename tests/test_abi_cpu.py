@@ -128,3 +128,10 @@ def test_workspace_sizes(lib):
     sel = lib.oomb_workspace_bytes(oomb.OOMB_OP_SELECT_TOPK, ctypes.byref(kv), 28, 8192, 128)
     assert sel >= 256 + 4 * 32768 * 4
     assert lib.oomb_workspace_bytes(99, ctypes.byref(kv), 0, 0, 0) == 0
+
+
+def test_noalloc_selection_refuses_oversized_shapes_on_the_host(lib):
+    kv = _kv(num_pages=1 << 20, num_slots=1 << 20, page_size=16)   # scores alone: 16 MiB
+    rc = lib.oomb_select_topk_noalloc(ctypes.c_void_p(FAKE), 28, 256, 4096, ctypes.c_void_p(FAKE),
+                                      ctypes.byref(kv), 64, ctypes.c_void_p(FAKE), None, None)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "fixed scratch" in oomb.oomb_last_error()
