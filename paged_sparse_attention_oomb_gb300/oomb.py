@@ -248,3 +248,59 @@ def sparse_attention_step(q, dout, kv: PagedKV, chunk_start, top_k, reps=None, s
             raise OombError(code, f"device status (where {where}, block {blk})")
     return dict(reps=reps, sel=sel[:, :n_sel], o=o, lse=lse, dq=dq)
 
+
+def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale=0.0,
+                         stream=None):
+    """One chunk-recurrent pass over a whole sequence, through the C ABI only.
+
+    Chunk-Recurrent Training Framework item: the sequence is processed chunk by
+    chunk.  Forward, chunks in order: chunk c selects its Top-K past pages from
+    the representatives of the pages written so far, attends them plus its own
+    pages, and then the representatives of its own pages are computed (they
+    become candidates for the later chunks).  Backward, chunks in reverse: the
+    same selections are reused and every chunk adds its dK/dV into the paged
+    gradient buffers of ``kv`` in place.  O and LSE of each chunk are kept for
+    its backward (the attention itself is recomputed inside the backward).
+
+    q_full, dout_full: ``[T, Hq, D]`` with T = num_pages * P.  Returns
+    ``(o_full, dq_full, sels)``; sels[c] is ``[Hkv, n_sel_c]``.
+    """
+    t, hq, d = q_full.shape
+    ns, hkv, p, _ = kv.k.shape
+    n_pages = kv.page_table.numel()
+    if t != n_pages * p or t % chunk_len or chunk_len % p:
+        raise OombError(OOMB_ERR_INVALID_ARG, "sequence must be whole chunks of whole pages")
+    dev = q_full.device
+    reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
+    ws_r = workspace(OOMB_OP_PAGE_REPS, kv)
+    ws_s = workspace(OOMB_OP_SELECT_TOPK, kv, hq, chunk_len, top_k)
+    ws_f = workspace(OOMB_OP_ATTN_FWD, kv, hq, chunk_len)
+    ws_b = workspace(OOMB_OP_ATTN_BWD, kv, hq, chunk_len)
+    o_full = torch.empty_like(q_full)
+    dq_full = torch.empty_like(q_full)
+    lses, sels = [], []
+    n_chunks = t // chunk_len
+    for c in range(n_chunks):
+        t0 = c * chunk_len
+        q = q_full[t0:t0 + chunk_len]
+        n_sel = min(top_k, t0 // p)
+        sel = torch.zeros((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
+        if n_sel:
+            oomb_select_topk(q, t0, reps, kv, n_sel, sel, ws_s, stream=stream)
+        lse = torch.empty((hq, chunk_len), dtype=torch.float32, device=dev)
+        oomb_sparse_attn_fwd(q, kv, sel, n_sel, t0, o_full[t0:t0 + chunk_len], lse, ws_f, scale,
+                             stream)
+        oomb_page_reps(kv, t0 // p, chunk_len // p, reps, ws_r, stream)
+        lses.append(lse)
+        sels.append((sel, n_sel))
+    for c in reversed(range(n_chunks)):
+        t0 = c * chunk_len
+        sel, n_sel = sels[c]
+        oomb_sparse_attn_bwd(q_full[t0:t0 + chunk_len], o_full[t0:t0 + chunk_len],
+                             dout_full[t0:t0 + chunk_len], lses[c], kv, sel, n_sel, t0,
+                             dq_full[t0:t0 + chunk_len], ws_b, scale, stream)
+    for w in (ws_r, ws_s, ws_f, ws_b):
+        code, where, blk = oomb_device_status(w, stream)
+        if code != OOMB_OK:
+            raise OombError(code, f"device status (where {where}, block {blk})")
+    return o_full, dq_full, [s[:, :n] for s, n in sels]

@@ -148,6 +148,28 @@ def test_cross_chunk_accumulation():
     compare(to_numpy64(kv.dv)[pt], dv_o, "bf16", "cross-chunk dV")
 
 
+@pytest.mark.parametrize("top_k", [3, 1 << 20])
+def test_chunk_recurrent_pass(top_k):
+    """Forward over chunks in order, backward in reverse, through the driver."""
+    wl = W("crp", "bf16", 4, 2, 2048, 64, 512, top_k)
+    x = make_inputs(wl, seed=8, device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(3)
+    q_full = torch.randn((2048, 4, 128), generator=g, device=DEV).to(torch.bfloat16)
+    do_full = torch.randn((2048, 4, 128), generator=g, device=DEV).to(torch.bfloat16)
+    kv = gpu_kv(x)
+    o_g, dq_g, sels = oomb.chunk_recurrent_pass(q_full, do_full, kv, 512, top_k)
+    kp, vp, pt = to_numpy64(x.k_pool), to_numpy64(x.v_pool), to_numpy64(x.page_table)
+    o_o, dq_o, dk_o, dv_o, sels_o = oracle.chunk_recurrent_grads(
+        to_numpy64(q_full), kp, vp, pt, to_numpy64(do_full), 512, 64, top_k)
+    for sg, so in zip(sels, sels_o):
+        assert sg.cpu().numpy().tolist() == so.tolist()
+    compare(o_g.float().cpu().numpy(), o_o, "bf16", "chunk-recurrent O")
+    compare(dq_g.float().cpu().numpy(), dq_o, "bf16", "chunk-recurrent dQ")
+    compare(to_numpy64(kv.dk)[pt], dk_o, "bf16", "chunk-recurrent dK")
+    compare(to_numpy64(kv.dv)[pt], dv_o, "bf16", "chunk-recurrent dV")
+
+
 def test_deterministic_selection_and_forward():
     wl = W("det", "bf16", 8, 2, 8192, 64, 512, 31)
     x = make_inputs(wl, seed=9, device=DEV)
