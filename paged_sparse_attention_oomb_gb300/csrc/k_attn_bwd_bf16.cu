@@ -15,7 +15,9 @@
 //   MMA2  dP^T = V dO^T                TMEM R1
 //   P^T = exp2(S^T * scale*log2e - lse2)   -> bf16 pairs, back into R0 (TMEM)
 //   MMA3  dV  += P^T dO                A from TMEM (R0), B = dO (shared)
-//   dS^T = scale * P^T (dP^T - Delta)   -> bf16 into a swizzled shared tile
+//   dS^T = P^T (dP^T - Delta)           -> bf16 into a swizzled shared tile
+//                                      (the softmax scale is applied to dK in the
+//                                      epilogue and to dQ when it is converted)
 //   MMA4  dK  += dS^T Q                TMEM R3
 //   MMA5  dQ^T = K^T dS^T              TMEM R1 (head dim on lanes), drained with
 //                                      coalesced fp32 reductions
@@ -25,9 +27,13 @@
 // At the end the CTA adds dK and dV to the bf16 gradient pages of its slots:
 // one read-add-write and one rounding per slot per call, no atomics, because
 // each (slot, KV head) has exactly one owner CTA.
-// Roles (320 threads): warp 0 TMA producer + TMEM allocator, warp 1 MMA
-// issuer, warps 2..9 compute: TMEM lane quarter = warp % 4, and the two warps
-// of a quarter split the 128 columns into halves.
+// Roles (448 threads): warp 0 TMA producer + TMEM allocator, warp 1 MMA
+// issuer (polls its barriers: its wake-up latency is on the critical path),
+// warps 2..9 compute P^T and dS^T (TMEM lane quarter = warp % 4; the two warps
+// of a quarter split the 128 columns), warps 10..13 drain dQ^T: they copy it
+// out of TMEM, release R1 for the next dP^T at once, and only then issue the
+// fp32 reductions, so neither the tensor pipe nor the compute warps wait on
+// the reductions.
 // TMEM: R0 [0,128) S^T / P^T, R1 [128,256) dP^T / dQ, R2 [256,384) dV,
 // R3 [384,512) dK.
 #include <cuda_bf16.h>
@@ -42,8 +48,9 @@
 namespace oomb {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kComputeThreads = 256;
+constexpr int kThreads = 448;
+constexpr int kComputeThreads = 256;              // warps 2..9: P^T and dS^T
+constexpr int kDrainThreads = 128;                // warps 10..13: dQ^T out of TMEM
 constexpr uint32_t kKOff = 0;
 constexpr uint32_t kVOff = kTileBytes;
 constexpr uint32_t kQOff = 2 * kTileBytes;        // 2 stages
@@ -138,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(dq_full), 1);
     mbar_init(BAR(p_ready), kComputeThreads);
     mbar_init(BAR(ds_ready), kComputeThreads);
-    mbar_init(BAR(r1_free), kComputeThreads);
+    mbar_init(BAR(r1_free), kDrainThreads);
     mbar_init(BAR(pt_consumed), 1);
     mbar_init(BAR(ds_free), 1);
     mbar_init(BAR(acc_done), 1);
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, 128, false, true);  // dV, dK
       constexpr uint32_t kIdDQ = idesc_bf16_f32(128, 128, true, true);    // dQ^T
       const uint32_t t_r0 = tmem, t_r1 = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 384;
-      bool ok = mbar_wait(BAR(kv_full), 0, wc, kWhereBwdMma);
+      bool ok = mbar_wait_spin(BAR(kv_full), 0, wc, kWhereBwdMma);
       for (int n = 0; ok && n < n_iter; ++n) {
         const int s = n & 1;
         const uint32_t phs = (n >> 1) & 1;       // stage phase
@@ -245,16 +252,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t da = sbase + kDOOff + s * kTileBytes;
         // MMA1: S^T = K Q^T  (R0 must be free: MMA3 of n-1 consumed P^T, and the
         // dS pass of n-1 -- which reads P^T -- ended before MMA4 of n-1 was issued)
-        if (!(ok = mbar_wait(BAR(q_full[s]), phs, wc, kWhereBwdMma))) break;
-        if (!(ok = mbar_wait(BAR(pt_consumed), ph1, wc, kWhereBwdMma))) break;
+        if (!(ok = mbar_wait_spin(BAR(q_full[s]), phs, wc, kWhereBwdMma))) break;
+        if (!(ok = mbar_wait_spin(BAR(pt_consumed), ph1, wc, kWhereBwdMma))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(t_r0, desc_kmajor(sbase + kKOff, kk), desc_kmajor(qa, kk), kIdKQ, kk > 0);
         umma_commit(BAR(s_full));
         // MMA2: dP^T = V dO^T  (R1 must be free: dQ of n-1 drained)
-        if (!(ok = mbar_wait(BAR(do_full[s]), phs, wc, kWhereBwdMma))) break;
-        if (!(ok = mbar_wait(BAR(r1_free), ph1, wc, kWhereBwdMma))) break;
+        if (!(ok = mbar_wait_spin(BAR(do_full[s]), phs, wc, kWhereBwdMma))) break;
+        if (!(ok = mbar_wait_spin(BAR(r1_free), ph1, wc, kWhereBwdMma))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(BAR(dp_full));
         // MMA3: dV += P^T dO  (P^T in TMEM R0 as bf16 pairs, 8 columns per k-step;
         // query columns [64 h, 64 h + 64) sit at R0 columns [64 h, 64 h + 32))
-        if (!(ok = mbar_wait(BAR(p_ready), ph, wc, kWhereBwdMma))) break;
+        if (!(ok = mbar_wait_spin(BAR(p_ready), ph, wc, kWhereBwdMma))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(BAR(pt_consumed));
         umma_commit(BAR(do_empty[s]));
         // MMA4: dK += dS^T Q ; MMA5: dQ = dS K
-        if (!(ok = mbar_wait(BAR(ds_ready), ph, wc, kWhereBwdMma))) break;
+        if (!(ok = mbar_wait_spin(BAR(ds_ready), ph, wc, kWhereBwdMma))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -293,10 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ compute
+    // ------------------------------------------------------------ compute / drain
     const int q4 = warp & 3;
-    const int ch = (warp - 2) >> 2;                // column half: [64 ch, 64 ch + 64)
-    const int r = q4 * 32 + lane;                  // key row (S/dP/dK/dV) or query row (dQ)
+    const bool drain_warp = warp >= 10;
+    const int ch = (warp - 2) >> 2;                // compute: column half [64 ch, 64 ch + 64)
+    const int r = q4 * 32 + lane;                  // key row (S/dP/dK/dV) or d (dQ^T)
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t t_r0 = tmem + lane_base, t_r1 = tmem + lane_base + 128;
     // key row validity: invalid rows (padding of a ragged tile) get P = 0
@@ -304,102 +312,132 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile_page(r / p.page_size, &key_valid);
     if (!is_sel) key_valid = key_valid && (own_t * 128 + r) < p.chunk_len;
     const float row_bias = key_valid ? 0.f : -INFINITY;
+    const bool warp_valid = __all_sync(0xffffffffu, key_valid);
     bool ok = true;
-    for (int n = 0; n < n_iter; ++n) {
-      const int qi = i0 + n % nq;
-      const int h = g * grp + n / nq;
-      const int s = n & 1;
-      const uint32_t phs = (n >> 1) & 1, ph = n & 1, ph1 = ph ^ 1;
-      const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 256 + 64 * ch);
-      const float4* dl4 = reinterpret_cast<const float4*>(vec + s * 256 + 128 + 64 * ch);
-      const bool diag = !is_sel && qi == own_t;   // key r sees query columns c >= r only
-      // ---- P^T = exp2(S^T scale log2e - lse2) -> bf16 pairs into R0
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full), ph, wc, kWhereBwdCompute));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(do_full[s]), phs, wc, kWhereBwdCompute));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        uint32_t rr[64];
-        tmem_ld64(t_r0 + 64 * ch, rr);
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          const float4 l = lse4[i >> 2];
-          const float lv[4] = {l.x, l.y, l.z, l.w};
-          float e[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float x = fmaf(__uint_as_float(rr[i + j]), p.scale_log2, row_bias - lv[j]);
-            if (diag && 64 * ch + i + j < r) x = -INFINITY;
-            e[j] = ex2(x);
-          }
-          pk[i >> 1] = pack_bf16(e[0], e[1]);
-          pk[(i >> 1) + 1] = pack_bf16(e[2], e[3]);
-        }
-        // P^T of query columns [64 ch, 64 ch + 64) goes to R0 columns
-        // [64 ch, 64 ch + 32): inside the S^T columns this warp has just read, so
-        // the other warp of the lane quarter is never overtaken
-        tmem_st32(t_r0 + 64 * ch, pk);
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(BAR(p_ready));
-      // ---- dS^T = scale P^T (dP^T - Delta) -> shared (bf16, swizzled)
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(dp_full), ph, wc, kWhereBwdCompute));
-      if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(BAR(ds_free), ph1, wc, kWhereBwdCompute));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t ds_row = sbase + kDSOff;
-#pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c32 = 2 * ch + cc;               // 32-column chunk
-        uint32_t dp[32], pp[16];
-        tmem_ld32_16(t_r1 + 32 * c32, dp, t_r0 + 64 * ch + 16 * cc, pp);
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 dl = dl4[(32 * cc + i) >> 2];
-          const float dv[4] = {dl.x, dl.y, dl.z, dl.w};
-          float d[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t pw = pp[(i + j) >> 1];
-            const float pv = __uint_as_float(((i + j) & 1) ? (pw & 0xFFFF0000u) : (pw << 16));
-            d[j] = p.scale * pv * (__uint_as_float(dp[i + j]) - dv[j]);
-          }
-          w[i >> 1] = pack_bf16(d[0], d[1]);
-          w[(i >> 1) + 1] = pack_bf16(d[2], d[3]);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          st_shared_v4(ds_row + tile128_chunk_off(r, 4 * c32 + k), w[4 * k], w[4 * k + 1],
-                       w[4 * k + 2], w[4 * k + 3]);
-      }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(BAR(ds_ready));
-      // ---- drain dQ^T (TMEM lane = head-dim index r, columns = query rows): each
-      // warp instruction adds one 128-byte line (32 consecutive d of one row)
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(dq_full), ph, wc, kWhereBwdCompute));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        const int t0 = qi * 128 + 64 * ch;
+    if (drain_warp) {
+      // ---- dQ^T drain: TMEM lane = head-dim index r, columns = query rows
+      for (int n = 0; n < n_iter; ++n) {
+        const int qi = i0 + n % nq;
+        const int h = g * grp + n / nq;
+        ok = __all_sync(0xffffffffu, mbar_wait(BAR(dq_full), n & 1, wc, kWhereBwdCompute));
+        if (!ok) break;
+        tc_fence_after();
+        const int t0 = qi * 128;
+        const int rows = min(128, p.chunk_len - t0);
         float* dst = p.dq_acc + (static_cast<long>(t0) * p.hq + h) * 128 + r;
         const long row_stride = static_cast<long>(p.hq) * 128;
-        const int rows = min(64, p.chunk_len - t0);
-        uint32_t rr[64];
-        tmem_ld64(t_r1 + 64 * ch, rr);
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[64];
+          tmem_ld64(t_r1 + 64 * half, v);
+          if (half == 1) {
+            tc_fence_before();
+            mbar_arrive(BAR(r1_free));             // R1 may now take the next dP^T
+          }
+          float* d0 = dst + 64 * half * row_stride;
+          if (rows >= 128) {                       // full query tile: the common case
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < rows) red_add_f32(dst + c * row_stride, __uint_as_float(rr[c]));
+            for (int c = 0; c < 64; ++c) red_add_f32(d0 + c * row_stride, __uint_as_float(v[c]));
+          } else {
+            const int lim = rows - 64 * half;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c < lim) red_add_f32(d0 + c * row_stride, __uint_as_float(v[c]));
+          }
+        }
       }
-      tc_fence_before();
-      mbar_arrive(BAR(r1_free));
+    } else {
+      for (int n = 0; n < n_iter; ++n) {
+        const int qi = i0 + n % nq;
+        const int s = n & 1;
+        const uint32_t phs = (n >> 1) & 1, ph = n & 1, ph1 = ph ^ 1;
+        const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 256 + 64 * ch);
+        const float4* dl4 = reinterpret_cast<const float4*>(vec + s * 256 + 128 + 64 * ch);
+        const bool diag = !is_sel && qi == own_t;   // key r sees query columns c >= r only
+        // ---- P^T = exp2(S^T scale log2e - lse2) -> bf16 pairs into R0
+        ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full), ph, wc, kWhereBwdCompute));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(do_full[s]), phs, wc, kWhereBwdCompute));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint32_t rr[64];
+          tmem_ld64(t_r0 + 64 * ch, rr);
+          uint32_t pk[32];
+          if (warp_valid && !diag) {               // no mask: the common case
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+              const float4 l = lse4[i >> 2];
+              const float e0 = ex2(fmaf(__uint_as_float(rr[i]), p.scale_log2, -l.x));
+              const float e1 = ex2(fmaf(__uint_as_float(rr[i + 1]), p.scale_log2, -l.y));
+              const float e2 = ex2(fmaf(__uint_as_float(rr[i + 2]), p.scale_log2, -l.z));
+              const float e3 = ex2(fmaf(__uint_as_float(rr[i + 3]), p.scale_log2, -l.w));
+              pk[i >> 1] = pack_bf16(e0, e1);
+              pk[(i >> 1) + 1] = pack_bf16(e2, e3);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+              const float4 l = lse4[i >> 2];
+              const float lv[4] = {l.x, l.y, l.z, l.w};
+              float e[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float x = fmaf(__uint_as_float(rr[i + j]), p.scale_log2, row_bias - lv[j]);
+                if (diag && 64 * ch + i + j < r) x = -INFINITY;
+                e[j] = ex2(x);
+              }
+              pk[i >> 1] = pack_bf16(e[0], e[1]);
+              pk[(i >> 1) + 1] = pack_bf16(e[2], e[3]);
+            }
+          }
+          // P^T of query columns [64 ch, 64 ch + 64) goes to R0 columns
+          // [64 ch, 64 ch + 32): inside the S^T columns this warp has just read,
+          // so the other warp of the lane quarter is never overtaken
+          tmem_st32(t_r0 + 64 * ch, pk);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(p_ready));
+        // ---- dS^T = P^T (dP^T - Delta) -> shared (bf16, swizzled)
+        ok = __all_sync(0xffffffffu, mbar_wait(BAR(dp_full), ph, wc, kWhereBwdCompute));
+        if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(BAR(ds_free), ph1, wc, kWhereBwdCompute));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ds_row = sbase + kDSOff;
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c32 = 2 * ch + cc;             // 32-column chunk
+          uint32_t dp[32], pp[16];
+          tmem_ld32_16(t_r1 + 32 * c32, dp, t_r0 + 64 * ch + 16 * cc, pp);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 dl = dl4[(32 * cc + i) >> 2];
+            const float dv[4] = {dl.x, dl.y, dl.z, dl.w};
+            float d[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t pw = pp[(i + j) >> 1];
+              const float pv = __uint_as_float(((i + j) & 1) ? (pw & 0xFFFF0000u) : (pw << 16));
+              d[j] = pv * (__uint_as_float(dp[i + j]) - dv[j]);
+            }
+            w[i >> 1] = pack_bf16(d[0], d[1]);
+            w[(i >> 1) + 1] = pack_bf16(d[2], d[3]);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            st_shared_v4(ds_row + tile128_chunk_off(r, 4 * c32 + k), w[4 * k], w[4 * k + 1],
+                         w[4 * k + 2], w[4 * k + 3]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(BAR(ds_ready));
+      }
     }
-    // ---- epilogue: dK, dV rows of this key tile into the paged bf16 gradients
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(acc_done), 0, wc, kWhereBwdEpilogue));
-    if (ok) {
+    // ---- epilogue: dK (x scale), dV rows of this key tile into the paged bf16 gradients
+    if (ok && !drain_warp)
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(acc_done), 0, wc, kWhereBwdEpilogue));
+    if (ok && !drain_warp) {
       tc_fence_after();
       const int u = r / p.page_size;
       bool valid;
@@ -424,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* pool = which == 0 ? p.dk : p.dv;
         const uint32_t tcol = (which == 0 ? 384 : 256) + 64 * ch;
+        const float mul = which == 0 ? p.scale : 1.f;
         uint4* dst = reinterpret_cast<uint4*>(pool + row);
         uint32_t rr[64];
         tmem_ld64(tmem + lane_base + tcol, rr);
@@ -432,10 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 8; ++i) {
             uint4 o = dst[i];
             const float* a = reinterpret_cast<const float*>(rr) + 8 * i;
-            o.x = bf16x2_add(o.x, a[0], a[1]);
-            o.y = bf16x2_add(o.y, a[2], a[3]);
-            o.z = bf16x2_add(o.z, a[4], a[5]);
-            o.w = bf16x2_add(o.w, a[6], a[7]);
+            o.x = bf16x2_add(o.x, a[0] * mul, a[1] * mul);
+            o.y = bf16x2_add(o.y, a[2] * mul, a[3] * mul);
+            o.z = bf16x2_add(o.z, a[4] * mul, a[5] * mul);
+            o.w = bf16x2_add(o.w, a[6] * mul, a[7] * mul);
             dst[i] = o;
           }
         }
@@ -489,16 +528,16 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
 }
 
 __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                  long n8) {
+                                  long n8, float scale) {
   const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
   const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
   const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
   uint4 v;
-  v.x = pack_bf16(a.x, a.y);
-  v.y = pack_bf16(a.z, a.w);
-  v.z = pack_bf16(b.x, b.y);
-  v.w = pack_bf16(b.z, b.w);
+  v.x = pack_bf16(a.x * scale, a.y * scale);
+  v.y = pack_bf16(a.z * scale, a.w * scale);
+  v.z = pack_bf16(b.x * scale, b.y * scale);
+  v.w = pack_bf16(b.z * scale, b.w * scale);
   reinterpret_cast<uint4*>(dq)[i] = v;
 }
 
@@ -580,7 +619,7 @@ cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* dout,
   if (e != cudaSuccess) return e;
   const long n8 = static_cast<long>(chunk_len) * hq * 128 / 8;
   dq_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, st>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
+      dq_acc, static_cast<__nv_bfloat16*>(dq), n8, scale);
   return cudaGetLastError();
 }
 

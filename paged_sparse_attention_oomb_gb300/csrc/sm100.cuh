@@ -104,6 +104,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// Same contract as mbar_wait, polling without suspending: for the single
+// thread that issues the MMAs, whose wake-up latency is on the critical path.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                               int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 255u) == 0) {
+      if (*c.abort_flag) return false;
+      if (global_timer_ns() - t0 > c.limit_ns) {
+        raise_status(c.status, kStatusTimeout, where);
+        *c.abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Wait used only while unwinding after an abort: a fixed, generous bound,
 // independent of the (possibly tiny, test-set) limit of the normal waits.
 __device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity) {
