@@ -12,12 +12,14 @@
 //   warp 0      TMA producer: Q_A, Q_B once; then K_j, V_j page by page through
 //               the page table (one 2-D box per page and 64-column half) into a
 //               5-slot shared ring; also allocates TMEM.
-//   warp 1      MMA issuer (one thread): per key tile j
+//   warp 1      MMA issuer (one thread, polling): per key tile j
 //                 S_A = Q_A K_j^T, S_B = Q_B K_j^T        (SS, into TMEM)
 //                 O_A += P_A V_j, O_B += P_B V_j          (P from TMEM)
+//               issuing for whichever tile is ready next.
 //   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B, one thread per
-//               query row: row maximum over S in TMEM, exponentials in base 2,
-//               P written back over S as bf16 pairs.  O is rescaled in TMEM only
+//               query row: the row of S is read from TMEM into registers
+//               once, row maximum, exponentials in base 2, P written back
+//               over S as bf16 pairs.  O is rescaled in TMEM only
 //               when a row maximum grows by more than 2^8 (the final
 //               normalisation uses the same running maximum, so this is exact).
 // While one tile's softmax runs the tensor pipe works on the other tile.
@@ -187,43 +189,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per tile X the sequence is S_X(0), PV_X(0), S_X(1), PV_X(1), ...; the
+    // issuer polls both tiles and issues whichever next step is ready, so
+    // neither softmax group waits behind the other.  S_X(j) overwrites P_X(j-1),
+    // so it waits for PV_X(j-1) to complete (pv_done).  A ring slot is released
+    // once both tiles have issued the MMAs that read it.
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
-      bool ok = mbar_wait(BAR(q_full), 0, wc, kWhereFwdMma);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int qk = 2 * j, qv = 2 * j + 1;
-        const int sk = qk % kSlots, sv = qv % kSlots;
-        // S_X = Q_X K_j^T (S_X may be overwritten once PV_X of tile j-1 is done)
-        if (!(ok = mbar_wait(BAR(slot_full[sk]), (qk / kSlots) & 1, wc, kWhereFwdMma))) break;
-        const uint32_t ka = sbase + kRingOff + sk * kTileBytes;
-        for (int t = 0; t < 2; ++t) {
-          if (j >= (t == 0 ? n_a : n_b)) continue;
-          if (j > 0 && !(ok = mbar_wait(BAR(pv_done[t]), (j - 1) & 1, wc, kWhereFwdMma))) break;
-          tc_fence_after();
-          const uint32_t qa = sbase + kQOff + t * kTileBytes;
+      bool ok = mbar_wait_spin(BAR(q_full), 0, wc, kWhereFwdMma);
+      const int nt[2] = {n_a, n_b};
+      int sj[2] = {0, 0};                          // S issued for tiles [0, sj)
+      int pj[2] = {0, 0};                          // PV issued for tiles [0, pj)
+      uint64_t t_last = global_timer_ns();
+      uint32_t polls = 0;
+      while (ok && (pj[0] < nt[0] || pj[1] < nt[1])) {
+        bool progress = false;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(tmem + t * 128, desc_kmajor(qa, kk), desc_kmajor(ka, kk), kIdQK, kk > 0);
-          umma_commit(BAR(s_full[t]));
-        }
-        if (!ok) break;
-        umma_commit(BAR(slot_empty[sk]));
-        // O_X += P_X V_j (P_X in TMEM as bf16 pairs over S_X, 8 columns per k-step)
-        if (!(ok = mbar_wait(BAR(slot_full[sv]), (qv / kSlots) & 1, wc, kWhereFwdMma))) break;
-        const uint32_t va = sbase + kRingOff + sv * kTileBytes;
         for (int t = 0; t < 2; ++t) {
-          if (j >= (t == 0 ? n_a : n_b)) continue;
-          if (!(ok = mbar_wait(BAR(p_ready[t]), j & 1, wc, kWhereFwdMma))) break;
-          tc_fence_after();
+          if (sj[t] == pj[t] && sj[t] < nt[t]) {
+            const int j = sj[t];
+            const int sk = (2 * j) % kSlots;
+            if (mbar_test_wait(BAR(slot_full[sk]), ((2 * j) / kSlots) & 1) &&
+                (j == 0 || mbar_test_wait(BAR(pv_done[t]), (j - 1) & 1))) {
+              tc_fence_after();
+              const uint32_t qa = sbase + kQOff + t * kTileBytes;
+              const uint32_t ka = sbase + kRingOff + sk * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_mnmajor(va, kk), kIdPV,
-                    (j > 0 || kk > 0));
-          umma_commit(BAR(pv_done[t]));
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ss(tmem + t * 128, desc_kmajor(qa, kk), desc_kmajor(ka, kk), kIdQK, kk > 0);
+              umma_commit(BAR(s_full[t]));
+              sj[t] = j + 1;
+              if (sj[t ^ 1] > j || j >= nt[t ^ 1]) umma_commit(BAR(slot_empty[sk]));
+              progress = true;
+            }
+          } else if (pj[t] < sj[t]) {
+            const int j = pj[t];
+            const int sv = (2 * j + 1) % kSlots;
+            if (mbar_test_wait(BAR(slot_full[sv]), ((2 * j + 1) / kSlots) & 1) &&
+                mbar_test_wait(BAR(p_ready[t]), j & 1)) {
+              tc_fence_after();
+              const uint32_t va = sbase + kRingOff + sv * kTileBytes;
+              // O_X += P_X V_j (P_X in TMEM as bf16 pairs over S_X, 8 columns per k-step)
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_mnmajor(va, kk),
+                        kIdPV, (j > 0 || kk > 0));
+              umma_commit(BAR(pv_done[t]));
+              pj[t] = j + 1;
+              if (pj[t ^ 1] > j || j >= nt[t ^ 1]) umma_commit(BAR(slot_empty[sv]));
+              progress = true;
+            }
+          }
         }
-        if (!ok) break;
-        umma_commit(BAR(slot_empty[sv]));
+        if (progress) {
+          t_last = global_timer_ns();
+        } else if ((++polls & 255u) == 0) {
+          if (bars->abort_flag) {
+            ok = false;
+          } else if (global_timer_ns() - t_last > wc.limit_ns) {
+            raise_status(p.status, kStatusTimeout, kWhereFwdMma);
+            bars->abort_flag = 1;
+            ok = false;
+          }
+        }
       }
       if (!ok) {
         umma_commit(BAR(drain));
@@ -247,6 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full[tsel]), j & 1, wc, kWhereFwdSoftmax));
       if (!ok) break;
       tc_fence_after();
+      // the whole row of S in registers: one TMEM round trip per tile
+      uint32_t sr[128];
+      tmem_ld128(t_s, sr);
       // valid columns are [0, lim); `masked` is uniform over the warp group
       int lim = 128;
       bool masked = false;
@@ -260,83 +292,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         lim = r + 1;
         masked = true;
       }
-      // pass 1: row maximum of the raw scores (scale > 0 commutes with max)
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(t_s + c4 * 32, rr);
-        if (masked) {
+      if (masked) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const int c = c4 * 32 + i;
-            mx0 = fmaxf(mx0, c < lim ? __uint_as_float(rr[i]) : -INFINITY);
-            mx1 = fmaxf(mx1, c + 1 < lim ? __uint_as_float(rr[i + 1]) : -INFINITY);
-            mx2 = fmaxf(mx2, c + 2 < lim ? __uint_as_float(rr[i + 2]) : -INFINITY);
-            mx3 = fmaxf(mx3, c + 3 < lim ? __uint_as_float(rr[i + 3]) : -INFINITY);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            mx0 = fmaxf(mx0, __uint_as_float(rr[i]));
-            mx1 = fmaxf(mx1, __uint_as_float(rr[i + 1]));
-            mx2 = fmaxf(mx2, __uint_as_float(rr[i + 2]));
-            mx3 = fmaxf(mx3, __uint_as_float(rr[i + 3]));
-          }
-        }
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+      // row maximum of the raw scores (scale > 0 commutes with max), 8 chains
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(sr[c + i]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+      // lazy rescale: m moves only when the row maximum grows by more than 2^8
+      float alpha = 1.f;
+      bool any_need = false;
       if (j == 0) {
         m = mt;
       } else {
-        // O_X is stable here: S_X of tile j was issued after PV_X of tile j-1 completed
         const float m_new = fmaxf(m, mt);
         const bool need = m_new > m + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2(m - m_new) : 1.f;
-#pragma unroll 1
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t rr[32];
-            tmem_ld32(t_o + c4 * 32, rr);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            tmem_st32(t_o + c4 * 32, rr);
-          }
-          if (need) {
-            l *= alpha;
-            m = m_new;
-          }
+        any_need = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2(m - m_new);
+          m = m_new;
         }
       }
-      // pass 2: P = exp2(s * scale_log2 - m) -> bf16 pairs over S (chunk c4 is
-      // written to columns [16 c4, 16 c4 + 16), all of which were already read)
+      // P = exp2(s * scale_log2 - m) -> bf16 pairs into S's first 64 columns
+      // (S is already in registers), 8 partial row sums
       const float neg_m = -m;
-      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
-#pragma unroll 1
+      float rs[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+#pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(t_s + c4 * 32, rr);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float x0 = fmaf(__uint_as_float(rr[i]), p.scale_log2, neg_m);
-          float x1 = fmaf(__uint_as_float(rr[i + 1]), p.scale_log2, neg_m);
-          if (masked && c4 * 32 + i >= lim) x0 = -INFINITY;
-          if (masked && c4 * 32 + i + 1 >= lim) x1 = -INFINITY;
-          const float e0 = ex2(x0), e1 = ex2(x1);
-          if (i & 2) {
-            rs2 += e0;
-            rs3 += e1;
-          } else {
-            rs0 += e0;
-            rs1 += e1;
-          }
+          const float e0 = ex2(fmaf(__uint_as_float(sr[32 * c4 + i]), p.scale_log2, neg_m));
+          const float e1 = ex2(fmaf(__uint_as_float(sr[32 * c4 + i + 1]), p.scale_log2, neg_m));
+          rs[i & 7] += e0;
+          rs[(i & 7) + 1] += e1;
           pk[i >> 1] = pack_bf16(e0, e1);
         }
         tmem_st16(t_s + c4 * 16, pk);
       }
+      if (any_need) {
+        // O_X is stable here: S_X of tile j was issued after PV_X of tile j-1 completed
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t rr[32];
+          tmem_ld32(t_o + c4 * 32, rr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+          tmem_st32(t_o + c4 * 32, rr);
+        }
+      }
       tmem_st_wait();
-      l += (rs0 + rs1) + (rs2 + rs3);
+      l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
       tc_fence_before();
       mbar_arrive(BAR(p_ready[tsel]));
     }

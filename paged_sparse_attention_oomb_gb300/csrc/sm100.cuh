@@ -104,15 +104,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// Non-blocking probe of a phase: true once the phase with this parity is complete.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Same contract as mbar_wait, polling without suspending: for the single
 // thread that issues the MMAs, whose wake-up latency is on the critical path.
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                                int where) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   uint32_t n = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     if ((++n & 255u) == 0) {
       if (*c.abort_flag) return false;
       if (global_timer_ns() - t0 > c.limit_ns) {
@@ -291,6 +304,29 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : OOMB_O8(r, 0), OOMB_O8(r, 8), OOMB_O8(r, 16), OOMB_O8(r, 24), OOMB_O8(r, 32),
         OOMB_O8(r, 40), OOMB_O8(r, 48), OOMB_O8(r, 56)
       : "r"(taddr)
+      : "memory");
+}
+// 128 consecutive TMEM columns of this thread's lane (two x64 loads in flight
+// together), one wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  __syncwarp();
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+      "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%129];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : OOMB_O8(r, 0), OOMB_O8(r, 8), OOMB_O8(r, 16), OOMB_O8(r, 24), OOMB_O8(r, 32),
+        OOMB_O8(r, 40), OOMB_O8(r, 48), OOMB_O8(r, 56), OOMB_O8(r, 64), OOMB_O8(r, 72),
+        OOMB_O8(r, 80), OOMB_O8(r, 88), OOMB_O8(r, 96), OOMB_O8(r, 104), OOMB_O8(r, 112),
+        OOMB_O8(r, 120)
+      : "r"(taddr), "r"(taddr + 64)
       : "memory");
 }
 // 32 columns at `ta` and 16 columns at `tb` of this thread's lane, one wait.
