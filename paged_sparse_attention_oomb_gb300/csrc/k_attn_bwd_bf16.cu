@@ -27,13 +27,16 @@
 // At the end the CTA adds dK and dV to the bf16 gradient pages of its slots:
 // one read-add-write and one rounding per slot per call, no atomics, because
 // each (slot, KV head) has exactly one owner CTA.
-// Roles (448 threads): warp 0 TMA producer + TMEM allocator, warp 1 MMA
-// issuer (polls its barriers: its wake-up latency is on the critical path),
-// warps 2..9 compute P^T and dS^T (TMEM lane quarter = warp % 4; the two warps
-// of a quarter split the 128 columns), warps 10..13 drain dQ^T: they copy it
-// out of TMEM, release R1 for the next dP^T at once, and only then issue the
+// Roles (512 threads, four warpgroups): warp 0 TMA producer + TMEM allocator,
+// warp 1 MMA issuer (polls its barriers: its wake-up latency is on the
+// critical path), warps 2..3 idle; warps 4..11 compute P^T and dS^T (TMEM lane
+// quarter = warp % 4; the two warps of a quarter split the 128 columns); warps
+// 12..15 drain dQ^T: each thread copies its whole TMEM lane (128 columns) into
+// registers, releases R1 for the next dP^T at once, and only then issues the
 // fp32 reductions, so neither the tensor pipe nor the compute warps wait on
-// the reductions.
+// them.  The drain warpgroup takes the registers this needs from the
+// producer/MMA warpgroup (setmaxnreg: 72 + 2 x 128 + 184 per thread = the
+// 128 per thread the block is launched with).
 // TMEM: R0 [0,128) S^T / P^T, R1 [128,256) dP^T / dQ, R2 [256,384) dV,
 // R3 [384,512) dK.
 #include <cuda_bf16.h>
@@ -48,9 +51,9 @@
 namespace oomb {
 namespace {
 
-constexpr int kThreads = 448;
-constexpr int kComputeThreads = 256;              // warps 2..9: P^T and dS^T
-constexpr int kDrainThreads = 128;                // warps 10..13: dQ^T out of TMEM
+constexpr int kThreads = 512;
+constexpr int kComputeThreads = 256;              // warps 4..11: P^T and dS^T
+constexpr int kDrainThreads = 128;                // warps 12..15: dQ^T out of TMEM
 constexpr uint32_t kKOff = 0;
 constexpr uint32_t kVOff = kTileBytes;
 constexpr uint32_t kQOff = 2 * kTileBytes;        // 2 stages
@@ -175,6 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     return *valid ? lp : own_page0;
   };
 
+  if (warp < 4) {
+    regs_decrease<72>();            // producer / MMA warpgroup gives registers to the drain
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -299,11 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain_wait(BAR(drain), 0);
       }
     }
+  }
   } else {
     // ------------------------------------------------------------ compute / drain
     const int q4 = warp & 3;
-    const bool drain_warp = warp >= 10;
-    const int ch = (warp - 2) >> 2;                // compute: column half [64 ch, 64 ch + 64)
+    const bool drain_warp = warp >= 12;
+    const int ch = (warp - 4) >> 2;                // compute: column half [64 ch, 64 ch + 64)
     const int r = q4 * 32 + lane;                  // key row (S/dP/dK/dV) or d (dQ^T)
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t t_r0 = tmem + lane_base, t_r1 = tmem + lane_base + 128;
@@ -315,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool warp_valid = __all_sync(0xffffffffu, key_valid);
     bool ok = true;
     if (drain_warp) {
+      regs_increase<184>();
       // ---- dQ^T drain: TMEM lane = head-dim index r, columns = query rows
       for (int n = 0; n < n_iter; ++n) {
         const int qi = i0 + n % nq;
@@ -326,26 +333,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rows = min(128, p.chunk_len - t0);
         float* dst = p.dq_acc + (static_cast<long>(t0) * p.hq + h) * 128 + r;
         const long row_stride = static_cast<long>(p.hq) * 128;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[64];
-          tmem_ld64(t_r1 + 64 * half, v);
-          if (half == 1) {
-            tc_fence_before();
-            mbar_arrive(BAR(r1_free));             // R1 may now take the next dP^T
+        uint32_t v[128];
+        tmem_ld128(t_r1, v);
+        tc_fence_before();
+        mbar_arrive(BAR(r1_free));                 // R1 may now take the next dP^T
+        if (rows >= 128) {                         // full query tile: the common case
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            red_add_f32(dst, __uint_as_float(v[c]));
+            dst += row_stride;
           }
-          float* d0 = dst + 64 * half * row_stride;
-          if (rows >= 128) {                       // full query tile: the common case
+        } else {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) red_add_f32(d0 + c * row_stride, __uint_as_float(v[c]));
-          } else {
-            const int lim = rows - 64 * half;
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (c < lim) red_add_f32(d0 + c * row_stride, __uint_as_float(v[c]));
+          for (int c = 0; c < 128; ++c) {
+            if (c < rows) red_add_f32(dst, __uint_as_float(v[c]));
+            dst += row_stride;
           }
         }
       }
+      regs_decrease<128>();
     } else {
       for (int n = 0; n < n_iter; ++n) {
         const int qi = i0 + n % nq;

@@ -432,24 +432,51 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     __syncthreads();
   }
   // prefix == T (the k-th key), need == how many keys equal to T are kept.
+  // Index-ordered compaction: warp w owns the contiguous index range
+  // [w * span, (w + 1) * span) and walks it 32 consecutive indices at a time
+  // (lane = index within the step: conflict-free shared loads), so ballots
+  // give each key's rank in index order.
   const uint32_t T = prefix;
-  const int per = (n_cand + blockDim.x - 1) / blockDim.x;
-  const int i0 = threadIdx.x * per, i1 = min(n_cand, i0 + per);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  const int span = ((n_cand + nw - 1) / nw + 31) & ~31;
+  const int j0 = w * span, j1 = min(n_cand, j0 + span);
+  const uint32_t below = (1u << lane) - 1u;
   int n_eq = 0;
-  for (int i = i0; i < i1; ++i) n_eq += (key_at(i) == T);
-  const int eq_before = block_excl_scan(n_eq, warp_tot, &total);
-  int n_keep = 0, eq_rank = eq_before;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = key_at(i);
-    if (key > T) ++n_keep;
-    else if (key == T && eq_rank++ < need) ++n_keep;
+  for (int base = j0; base < j1; base += 32) {
+    const int i = base + lane;
+    n_eq += __popc(__ballot_sync(0xffffffffu, i < j1 && key_at(i) == T));
   }
-  int pos = block_excl_scan(n_keep, warp_tot, &total);
+  // exclusive scan over warps of the equal-key counts, then of the kept counts
+  __shared__ int wsum[32];
+  if (lane == 0) wsum[w] = n_eq;
+  __syncthreads();
+  int eq_before = 0;
+  for (int u = 0; u < w; ++u) eq_before += wsum[u];
+  __syncthreads();
+  int n_keep = 0, eq_rank = eq_before;
+  for (int base = j0; base < j1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < j1 ? key_at(i) : 0u;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, i < j1 && key == T);
+    const bool keep = i < j1 && (key > T || (key == T && eq_rank + __popc(eqm & below) < need));
+    n_keep += __popc(__ballot_sync(0xffffffffu, keep));
+    eq_rank += __popc(eqm);
+  }
+  if (lane == 0) wsum[w] = n_keep;
+  __syncthreads();
+  int pos = 0;
+  for (int u = 0; u < w; ++u) pos += wsum[u];
   eq_rank = eq_before;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = key_at(i);
-    if (key > T) out[pos++] = i;
-    else if (key == T && eq_rank++ < need) out[pos++] = i;
+  for (int base = j0; base < j1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < j1 ? key_at(i) : 0u;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, i < j1 && key == T);
+    const bool keep = i < j1 && (key > T || (key == T && eq_rank + __popc(eqm & below) < need));
+    const uint32_t km = __ballot_sync(0xffffffffu, keep);
+    if (keep) out[pos + __popc(km & below)] = i;
+    pos += __popc(km);
+    eq_rank += __popc(eqm);
   }
 }
 
