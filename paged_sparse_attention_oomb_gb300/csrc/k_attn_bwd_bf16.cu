@@ -21,9 +21,11 @@
 //   MMA4  dK  += dS^T Q                TMEM R3
 //   MMA5  dQ^T = K^T dS^T              TMEM R1 (head dim on lanes), drained with
 //                                      coalesced fp32 reductions
-// Q/dO tiles (+ their lse2/Delta rows) stream through a 2-stage TMA ring, and
-// MMA1 of iteration n+1 is issued as soon as MMA3 of n has consumed P^T, so the
-// tensor pipe overlaps the exponentials, the dS pass and the dQ drain.
+// Q (+ its lse2/Delta rows) and dO tiles stream through a 2-stage TMA ring.
+// The compute warps keep P^T in registers for the dS pass, so R0 is free as
+// soon as MMA3 has read it: the issue order is dP^T(n), dV(n), S^T(n+1),
+// dK(n), dQ^T(n), and the exponentials of n+1 follow the dS pass of n without
+// waiting for dK/dQ of n.
 // At the end the CTA adds dK and dV to the bf16 gradient pages of its slots:
 // one read-add-write and one rounding per slot per call, no atomics, because
 // each (slot, KV head) has exactly one owner CTA.
@@ -213,21 +215,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qi = i0 + n % nq;
         const int s = n & 1;
         const uint32_t phe = ((n >> 1) & 1) ^ 1;
+        // Q with its lse2 and Delta rows (read by the P and dS passes; the stage
+        // is released after dK, which follows the dS pass)
         if (!mbar_wait(BAR(q_empty[s]), phe, wc, kWhereBwdProducer)) break;
-        mbar_arrive_expect_tx(BAR(q_full[s]), kTileBytes);
+        const uint32_t vb = sbase + kVecOff + s * 1024;
+        const long voff = static_cast<long>(h) * padded + qi * 128;
+        mbar_arrive_expect_tx(BAR(q_full[s]), kTileBytes + 1024);
         tma_load_3d(sbase + kQOff + s * kTileBytes, &tm_q, BAR(q_full[s]), 0, h, qi * 128);
         tma_load_3d(sbase + kQOff + s * kTileBytes + kHalfBytes, &tm_q, BAR(q_full[s]), 64, h,
                     qi * 128);
+        bulk_load(vb, p.lse2 + voff, 512, BAR(q_full[s]));
+        bulk_load(vb + 512, p.delta + voff, 512, BAR(q_full[s]));
         ++nq_issued;
         if (!mbar_wait(BAR(do_empty[s]), phe, wc, kWhereBwdProducer)) break;
-        const uint32_t vb = sbase + kVecOff + s * 1024;
-        const long voff = static_cast<long>(h) * padded + qi * 128;
-        mbar_arrive_expect_tx(BAR(do_full[s]), kTileBytes + 1024);
+        mbar_arrive_expect_tx(BAR(do_full[s]), kTileBytes);
         tma_load_3d(sbase + kDOOff + s * kTileBytes, &tm_do, BAR(do_full[s]), 0, h, qi * 128);
         tma_load_3d(sbase + kDOOff + s * kTileBytes + kHalfBytes, &tm_do, BAR(do_full[s]), 64, h,
                     qi * 128);
-        bulk_load(vb, p.lse2 + voff, 512, BAR(do_full[s]));
-        bulk_load(vb + 512, p.delta + voff, 512, BAR(do_full[s]));
         ++ndo_issued;
       }
       if (bars->abort_flag) {
@@ -249,22 +253,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdDQ = idesc_bf16_f32(128, 128, true, true);    // dQ^T
       const uint32_t t_r0 = tmem, t_r1 = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 384;
       bool ok = mbar_wait_spin(BAR(kv_full), 0, wc, kWhereBwdMma);
+      // S^T(n) = K Q^T into R0: R0 is free once MMA3 of n-1 has read P^T (the
+      // compute warps keep their own copy of P(n-1) in registers for the dS pass)
+      auto issue_s = [&](int n) -> bool {
+        const int s = n & 1;
+        if (!mbar_wait_spin(BAR(q_full[s]), (n >> 1) & 1, wc, kWhereBwdMma)) return false;
+        if (n > 0 && !mbar_wait_spin(BAR(pt_consumed), (n - 1) & 1, wc, kWhereBwdMma)) return false;
+        tc_fence_after();
+        const uint32_t qa = sbase + kQOff + s * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(t_r0, desc_kmajor(sbase + kKOff, kk), desc_kmajor(qa, kk), kIdKQ, kk > 0);
+        umma_commit(BAR(s_full));
+        return true;
+      };
+      // Issue order: S^T(0); then per n: dP^T(n), dV(n), S^T(n+1), dK(n), dQ^T(n).
+      // S^T(n+1) goes before dK/dQ(n) so that the exponentials of n+1 can start
+      // as soon as the dS pass of n is over.
+      if (ok && n_iter > 0) ok = issue_s(0);
       for (int n = 0; ok && n < n_iter; ++n) {
         const int s = n & 1;
         const uint32_t phs = (n >> 1) & 1;       // stage phase
         const uint32_t ph = n & 1, ph1 = ph ^ 1; // per-iteration phase
         const uint32_t qa = sbase + kQOff + s * kTileBytes;
         const uint32_t da = sbase + kDOOff + s * kTileBytes;
-        // MMA1: S^T = K Q^T  (R0 must be free: MMA3 of n-1 consumed P^T, and the
-        // dS pass of n-1 -- which reads P^T -- ended before MMA4 of n-1 was issued)
-        if (!(ok = mbar_wait_spin(BAR(q_full[s]), phs, wc, kWhereBwdMma))) break;
-        if (!(ok = mbar_wait_spin(BAR(pt_consumed), ph1, wc, kWhereBwdMma))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_r0, desc_kmajor(sbase + kKOff, kk), desc_kmajor(qa, kk), kIdKQ, kk > 0);
-        umma_commit(BAR(s_full));
-        // MMA2: dP^T = V dO^T  (R1 must be free: dQ of n-1 drained)
+        // MMA2: dP^T = V dO^T  (R1 must be free: dQ^T of n-1 copied out by the drain)
         if (!(ok = mbar_wait_spin(BAR(do_full[s]), phs, wc, kWhereBwdMma))) break;
         if (!(ok = mbar_wait_spin(BAR(r1_free), ph1, wc, kWhereBwdMma))) break;
         tc_fence_after();
@@ -282,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   (n > 0 || kk > 0));
         umma_commit(BAR(pt_consumed));
         umma_commit(BAR(do_empty[s]));
-        // MMA4: dK += dS^T Q ; MMA5: dQ = dS K
+        // MMA1 of the next iteration
+        if (n + 1 < n_iter && !(ok = issue_s(n + 1))) break;
+        // MMA4: dK += dS^T Q ; MMA5: dQ^T = K^T dS^T
         if (!(ok = mbar_wait_spin(BAR(ds_ready), ph, wc, kWhereBwdMma))) break;
         tc_fence_after();
 #pragma unroll
@@ -362,13 +377,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool diag = !is_sel && qi == own_t;   // key r sees query columns c >= r only
         // ---- P^T = exp2(S^T scale log2e - lse2) -> bf16 pairs into R0
         ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full), ph, wc, kWhereBwdCompute));
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(do_full[s]), phs, wc, kWhereBwdCompute));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(q_full[s]), phs, wc, kWhereBwdCompute));
         if (!ok) break;
         tc_fence_after();
+        uint32_t pk[32];                           // P^T of this warp's 64 columns, kept for dS
         {
           uint32_t rr[64];
           tmem_ld64(t_r0 + 64 * ch, rr);
-          uint32_t pk[32];
           if (warp_valid && !diag) {               // no mask: the common case
 #pragma unroll
             for (int i = 0; i < 64; i += 4) {
@@ -410,11 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t ds_row = sbase + kDSOff;
-#pragma unroll 1
+#pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int c32 = 2 * ch + cc;             // 32-column chunk
-          uint32_t dp[32], pp[16];
-          tmem_ld32_16(t_r1 + 32 * c32, dp, t_r0 + 64 * ch + 16 * cc, pp);
+          uint32_t dp[32];
+          tmem_ld32(t_r1 + 32 * c32, dp);
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
@@ -423,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float d[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint32_t pw = pp[(i + j) >> 1];
+              const uint32_t pw = pk[16 * cc + ((i + j) >> 1)];
               const float pv = __uint_as_float(((i + j) & 1) ? (pw & 0xFFFF0000u) : (pw << 16));
               d[j] = pv * (__uint_as_float(dp[i + j]) - dv[j]);
             }
