@@ -253,6 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdDQ = idesc_bf16_f32(128, 128, true, true);    // dQ^T
       const uint32_t t_r0 = tmem, t_r1 = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 384;
       bool ok = mbar_wait_spin(BAR(kv_full), 0, wc, kWhereBwdMma);
+      // every operand descriptor = one base + compile-time constants
+      const uint64_t d0 = desc_kmajor0(sbase);
+      const uint64_t dK_k = d0 + desc_off(kKOff), dK_mn = d0 + kDescMn + desc_off(kKOff);
+      const uint64_t dV_k = d0 + desc_off(kVOff);
+      const uint64_t dDS_k = d0 + desc_off(kDSOff), dDS_mn = d0 + kDescMn + desc_off(kDSOff);
+      const uint64_t dQ_k = d0 + desc_off(kQOff), dQ_mn = d0 + kDescMn + desc_off(kQOff);
+      const uint64_t dDO_k = d0 + desc_off(kDOOff), dDO_mn = d0 + kDescMn + desc_off(kDOOff);
       // S^T(n) = K Q^T into R0: R0 is free once MMA3 of n-1 has read P^T (the
       // compute warps keep their own copy of P(n-1) in registers for the dS pass)
       auto issue_s = [&](int n) -> bool {
@@ -260,10 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_spin(BAR(q_full[s]), (n >> 1) & 1, wc, kWhereBwdMma)) return false;
         if (n > 0 && !mbar_wait_spin(BAR(pt_consumed), (n - 1) & 1, wc, kWhereBwdMma)) return false;
         tc_fence_after();
-        const uint32_t qa = sbase + kQOff + s * kTileBytes;
+        const uint64_t a = opaque(dK_k), qa = opaque(dQ_k + s * kTileDesc);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_r0, desc_kmajor(sbase + kKOff, kk), desc_kmajor(qa, kk), kIdKQ, kk > 0);
+          umma_ss(t_r0, a + kstep_kmajor(kk), qa + kstep_kmajor(kk), kIdKQ, kk > 0);
         umma_commit(BAR(s_full));
         return true;
       };
@@ -275,24 +282,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = n & 1;
         const uint32_t phs = (n >> 1) & 1;       // stage phase
         const uint32_t ph = n & 1, ph1 = ph ^ 1; // per-iteration phase
-        const uint32_t qa = sbase + kQOff + s * kTileBytes;
-        const uint32_t da = sbase + kDOOff + s * kTileBytes;
         // MMA2: dP^T = V dO^T  (R1 must be free: dQ^T of n-1 copied out by the drain)
         if (!(ok = mbar_wait_spin(BAR(do_full[s]), phs, wc, kWhereBwdMma))) break;
         if (!(ok = mbar_wait_spin(BAR(r1_free), ph1, wc, kWhereBwdMma))) break;
         tc_fence_after();
+        {
+          const uint64_t a = opaque(dV_k), da = opaque(dDO_k + s * kTileDesc);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_r1, desc_kmajor(sbase + kVOff, kk), desc_kmajor(da, kk), kIdKQ, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(t_r1, a + kstep_kmajor(kk), da + kstep_kmajor(kk), kIdKQ, kk > 0);
+        }
         umma_commit(BAR(dp_full));
         // MMA3: dV += P^T dO  (P^T in TMEM R0 as bf16 pairs, 8 columns per k-step;
         // query columns [64 h, 64 h + 64) sit at R0 columns [64 h, 64 h + 32))
         if (!(ok = mbar_wait_spin(BAR(p_ready), ph, wc, kWhereBwdMma))) break;
         tc_fence_after();
+        {
+          const uint64_t da = opaque(dDO_mn + s * kTileDesc);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(t_dv, t_r0 + 64 * (kk >> 2) + 8 * (kk & 3), desc_mnmajor(da, kk), kIdAcc,
-                  (n > 0 || kk > 0));
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(t_dv, t_r0 + 64 * (kk >> 2) + 8 * (kk & 3), da + kstep_mnmajor(kk), kIdAcc,
+                    (n > 0 || kk > 0));
+        }
         umma_commit(BAR(pt_consumed));
         umma_commit(BAR(do_empty[s]));
         // MMA1 of the next iteration
@@ -300,15 +311,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MMA4: dK += dS^T Q ; MMA5: dQ^T = K^T dS^T
         if (!(ok = mbar_wait_spin(BAR(ds_ready), ph, wc, kWhereBwdMma))) break;
         tc_fence_after();
+        {
+          const uint64_t a = opaque(dDS_k), qa = opaque(dQ_mn + s * kTileDesc);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_dk, desc_kmajor(sbase + kDSOff, kk), desc_mnmajor(qa, kk), kIdAcc,
-                  (n > 0 || kk > 0));
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(t_dk, a + kstep_kmajor(kk), qa + kstep_mnmajor(kk), kIdAcc, (n > 0 || kk > 0));
+        }
         umma_commit(BAR(q_empty[s]));
+        {
+          const uint64_t a = opaque(dK_mn), b = opaque(dDS_mn);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_r1, desc_mnmajor(sbase + kKOff, kk), desc_mnmajor(sbase + kDSOff, kk), kIdDQ,
-                  kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(t_r1, a + kstep_mnmajor(kk), b + kstep_mnmajor(kk), kIdDQ, kk > 0);
+        }
         umma_commit(BAR(dq_full));
         umma_commit(BAR(ds_free));
       }

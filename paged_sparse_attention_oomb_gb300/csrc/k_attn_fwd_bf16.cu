@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
       bool ok = mbar_wait_spin(BAR(q_full), 0, wc, kWhereFwdMma);
       const int nt[2] = {n_a, n_b};
+      const uint64_t d0 = desc_kmajor0(sbase);
+      const uint64_t dQ0 = d0 + desc_off(kQOff);
+      const uint64_t dRing_k = d0 + desc_off(kRingOff), dRing_mn = d0 + kDescMn + desc_off(kRingOff);
       int sj[2] = {0, 0};                          // S issued for tiles [0, sj)
       int pj[2] = {0, 0};                          // PV issued for tiles [0, pj)
       uint64_t t_last = global_timer_ns();
@@ -213,11 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mbar_test_wait(BAR(slot_full[sk]), ((2 * j) / kSlots) & 1) &&
                 (j == 0 || mbar_test_wait(BAR(pv_done[t]), (j - 1) & 1))) {
               tc_fence_after();
-              const uint32_t qa = sbase + kQOff + t * kTileBytes;
-              const uint32_t ka = sbase + kRingOff + sk * kTileBytes;
+              const uint64_t qa = dQ0 + t * kTileDesc;
+              const uint64_t ka = dRing_k + sk * kTileDesc;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                umma_ss(tmem + t * 128, desc_kmajor(qa, kk), desc_kmajor(ka, kk), kIdQK, kk > 0);
+                umma_ss(tmem + t * 128, qa + kstep_kmajor(kk), ka + kstep_kmajor(kk), kIdQK, kk > 0);
               umma_commit(BAR(s_full[t]));
               sj[t] = j + 1;
               if (sj[t ^ 1] > j || j >= nt[t ^ 1]) umma_commit(BAR(slot_empty[sk]));
@@ -229,11 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mbar_test_wait(BAR(slot_full[sv]), ((2 * j + 1) / kSlots) & 1) &&
                 mbar_test_wait(BAR(p_ready[t]), j & 1)) {
               tc_fence_after();
-              const uint32_t va = sbase + kRingOff + sv * kTileBytes;
+              const uint64_t va = dRing_mn + sv * kTileDesc;
               // O_X += P_X V_j (P_X in TMEM as bf16 pairs over S_X, 8 columns per k-step)
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_mnmajor(va, kk),
+                umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, va + kstep_mnmajor(kk),
                         kIdPV, (j > 0 || kk > 0));
               umma_commit(BAR(pv_done[t]));
               pj[t] = j + 1;

@@ -167,6 +167,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// L2 prefetch of one 3-D TMA box (a hint: no completion, nothing written to shared memory).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// L2 prefetch of a contiguous range (16-byte aligned address, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
 // Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -266,6 +280,38 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
   return sdesc_sw128(tile + kk * 2048, kHalfBytes, 1024);
 }
+
+// The same descriptors split into a per-tile base (computed once) and a
+// per-k-step constant added to the start-address field (shared addresses are
+// below 256 KiB, so the 14-bit field never carries).  Keeps the MMA-issuing
+// thread to a handful of instructions per MMA: it shares its SM sub-partition
+// with busy compute warps.
+__device__ __forceinline__ uint64_t desc_kmajor0(uint32_t tile) {
+  return sdesc_sw128(tile, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor0(uint32_t tile) {
+  return sdesc_sw128(tile, kHalfBytes, 1024);
+}
+__host__ __device__ constexpr uint64_t kstep_kmajor(int kk) {
+  return static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t kstep_mnmajor(int kk) {
+  return static_cast<uint64_t>((kk * 2048) >> 4);
+}
+// Descriptor offset of a whole tile128 (stage s of a ring starts s tiles on).
+constexpr uint64_t kTileDesc = kTileBytes >> 4;
+// desc_mnmajor0(t) == desc_kmajor0(t) + kDescMn: only the leading-byte-offset
+// field differs (16 bytes -> one 64-column half).
+constexpr uint64_t kDescMn = static_cast<uint64_t>((kHalfBytes >> 4) - 1) << 16;
+// Opaque copy: keeps the compiler from hoisting per-k-step descriptor sums out
+// of a loop (which would pin dozens of 64-bit registers in the issuing thread).
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  uint64_t y;
+  asm volatile("mov.b64 %0, %1;" : "=l"(y) : "l"(x));
+  return y;
+}
+// Descriptor offset of a byte offset within shared memory.
+__host__ __device__ constexpr uint64_t desc_off(uint32_t bytes) { return bytes >> 4; }
 
 // Byte offset of the 16-byte chunk `c` (0..15, 8 bf16 each) of row `r` in a tile128.
 __device__ __forceinline__ uint32_t tile128_chunk_off(int r, int c) {
