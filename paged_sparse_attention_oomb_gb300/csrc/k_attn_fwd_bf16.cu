@@ -193,8 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // issuer polls both tiles and issues whichever next step is ready, so
     // neither softmax group waits behind the other.  S_X(j) overwrites P_X(j-1),
     // so it waits for PV_X(j-1) to complete (pv_done).  A ring slot is released
-    // once both tiles have issued the MMAs that read it.
-    if (lane == 0) {
+    // once both tiles have issued the MMAs that read it.  The whole warp runs
+    // the loop in lockstep (its decisions are warp-uniform); one elected lane
+    // issues the MMAs and commits.
+    {
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
       bool ok = mbar_wait_spin(BAR(q_full), 0, wc, kWhereFwdMma);
@@ -218,12 +220,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               const uint64_t qa = dQ0 + t * kTileDesc;
               const uint64_t ka = dRing_k + sk * kTileDesc;
+              const bool rel = sj[t ^ 1] > j || j >= nt[t ^ 1];
+              if (elect_one()) {
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_ss(tmem + t * 128, qa + kstep_kmajor(kk), ka + kstep_kmajor(kk), kIdQK, kk > 0);
-              umma_commit(BAR(s_full[t]));
+                for (int kk = 0; kk < 8; ++kk)
+                  umma_ss(tmem + t * 128, qa + kstep_kmajor(kk), ka + kstep_kmajor(kk), kIdQK, kk > 0);
+                umma_commit(BAR(s_full[t]));
+                if (rel) umma_commit(BAR(slot_empty[sk]));
+              }
+              __syncwarp();
               sj[t] = j + 1;
-              if (sj[t ^ 1] > j || j >= nt[t ^ 1]) umma_commit(BAR(slot_empty[sk]));
               progress = true;
             }
           } else if (pj[t] < sj[t]) {
@@ -233,14 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_test_wait(BAR(p_ready[t]), j & 1)) {
               tc_fence_after();
               const uint64_t va = dRing_mn + sv * kTileDesc;
+              const bool rel = pj[t ^ 1] > j || j >= nt[t ^ 1];
               // O_X += P_X V_j (P_X in TMEM as bf16 pairs over S_X, 8 columns per k-step)
+              if (elect_one()) {
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, va + kstep_mnmajor(kk),
-                        kIdPV, (j > 0 || kk > 0));
-              umma_commit(BAR(pv_done[t]));
+                for (int kk = 0; kk < 8; ++kk)
+                  umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, va + kstep_mnmajor(kk),
+                          kIdPV, (j > 0 || kk > 0));
+                umma_commit(BAR(pv_done[t]));
+                if (rel) umma_commit(BAR(slot_empty[sv]));
+              }
+              __syncwarp();
               pj[t] = j + 1;
-              if (pj[t ^ 1] > j || j >= nt[t ^ 1]) umma_commit(BAR(slot_empty[sv]));
               progress = true;
             }
           }
@@ -258,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        umma_commit(BAR(drain));
+        if (elect_one()) umma_commit(BAR(drain));
+        __syncwarp();
         mbar_drain_wait(BAR(drain), 0);
       }
     }

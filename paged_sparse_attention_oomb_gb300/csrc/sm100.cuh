@@ -245,6 +245,16 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
+// One lane of a converged warp (the same lane every time): lets a whole warp
+// run an issue loop in lockstep while a single thread issues the MMAs.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulator.
 // a_mn / b_mn: operand stored MN-major (transposed) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn, bool b_mn) {
