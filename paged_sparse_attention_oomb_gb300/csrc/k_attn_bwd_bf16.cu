@@ -247,7 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop in lockstep (its decisions are
+    // warp-uniform); one elected lane issues the MMAs and their commits.
+    {
       constexpr uint32_t kIdKQ = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, 128, false, true);  // dV, dK
       constexpr uint32_t kIdDQ = idesc_bf16_f32(128, 128, true, true);    // dQ^T
@@ -268,10 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n > 0 && !mbar_wait_spin(BAR(pt_consumed), (n - 1) & 1, wc, kWhereBwdMma)) return false;
         tc_fence_after();
         const uint64_t a = opaque(dK_k), qa = opaque(dQ_k + s * kTileDesc);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(t_r0, a + kstep_kmajor(kk), qa + kstep_kmajor(kk), kIdKQ, kk > 0);
-        umma_commit(BAR(s_full));
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(t_r0, a + kstep_kmajor(kk), qa + kstep_kmajor(kk), kIdKQ, kk > 0);
+          umma_commit(BAR(s_full));
+        }
+        __syncwarp();
         return true;
       };
       // Issue order: S^T(0); then per n: dP^T(n), dV(n), S^T(n+1), dK(n), dQ^T(n).
@@ -288,24 +293,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         {
           const uint64_t a = opaque(dV_k), da = opaque(dDO_k + s * kTileDesc);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(t_r1, a + kstep_kmajor(kk), da + kstep_kmajor(kk), kIdKQ, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ss(t_r1, a + kstep_kmajor(kk), da + kstep_kmajor(kk), kIdKQ, kk > 0);
+            umma_commit(BAR(dp_full));
+          }
+          __syncwarp();
         }
-        umma_commit(BAR(dp_full));
         // MMA3: dV += P^T dO  (P^T in TMEM R0 as bf16 pairs, 8 columns per k-step;
         // query columns [64 h, 64 h + 64) sit at R0 columns [64 h, 64 h + 32))
         if (!(ok = mbar_wait_spin(BAR(p_ready), ph, wc, kWhereBwdMma))) break;
         tc_fence_after();
         {
           const uint64_t da = opaque(dDO_mn + s * kTileDesc);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts(t_dv, t_r0 + 64 * (kk >> 2) + 8 * (kk & 3), da + kstep_mnmajor(kk), kIdAcc,
-                    (n > 0 || kk > 0));
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ts(t_dv, t_r0 + 64 * (kk >> 2) + 8 * (kk & 3), da + kstep_mnmajor(kk), kIdAcc,
+                      (n > 0 || kk > 0));
+            umma_commit(BAR(pt_consumed));
+            umma_commit(BAR(do_empty[s]));
+          }
+          __syncwarp();
         }
-        umma_commit(BAR(pt_consumed));
-        umma_commit(BAR(do_empty[s]));
         // MMA1 of the next iteration
         if (n + 1 < n_iter && !(ok = issue_s(n + 1))) break;
         // MMA4: dK += dS^T Q ; MMA5: dQ^T = K^T dS^T
@@ -313,24 +324,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         {
           const uint64_t a = opaque(dDS_k), qa = opaque(dQ_mn + s * kTileDesc);
+          const uint64_t a2 = opaque(dK_mn), b2 = opaque(dDS_mn);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(t_dk, a + kstep_kmajor(kk), qa + kstep_mnmajor(kk), kIdAcc, (n > 0 || kk > 0));
-        }
-        umma_commit(BAR(q_empty[s]));
-        {
-          const uint64_t a = opaque(dK_mn), b = opaque(dDS_mn);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ss(t_dk, a + kstep_kmajor(kk), qa + kstep_mnmajor(kk), kIdAcc, (n > 0 || kk > 0));
+            umma_commit(BAR(q_empty[s]));
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(t_r1, a + kstep_mnmajor(kk), b + kstep_mnmajor(kk), kIdDQ, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ss(t_r1, a2 + kstep_mnmajor(kk), b2 + kstep_mnmajor(kk), kIdDQ, kk > 0);
+            umma_commit(BAR(dq_full));
+            umma_commit(BAR(ds_free));
+          }
+          __syncwarp();
         }
-        umma_commit(BAR(dq_full));
-        umma_commit(BAR(ds_free));
       }
       if (ok) {
-        umma_commit(BAR(acc_done));
+        if (elect_one()) umma_commit(BAR(acc_done));
+        __syncwarp();
       } else {
-        umma_commit(BAR(drain));
+        if (elect_one()) umma_commit(BAR(drain));
+        __syncwarp();
         mbar_drain_wait(BAR(drain), 0);
       }
     }
