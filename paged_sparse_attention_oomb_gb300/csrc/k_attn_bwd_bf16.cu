@@ -184,12 +184,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<72>();            // producer / MMA warpgroup gives registers to the drain
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(BAR(kv_full), 2 * kTileBytes);
+    // The whole warp runs the loop in lockstep; one elected lane issues.
+    {
+      const bool leader = elect_one();
+      if (leader) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_arrive_expect_tx(BAR(kv_full), 2 * kTileBytes);
+      }
       for (int u = 0; u < ppt; ++u) {
         bool valid;
         int lp = tile_page(u, &valid);
@@ -203,11 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           slot = 0;
         }
         const int row = (slot * p.hkv + g) * p.page_size;
-        for (int hf = 0; hf < 2; ++hf) {
-          const uint32_t off = hf * kHalfBytes + u * p.page_size * 128;
-          tma_load_2d(sbase + kKOff + off, &tm_k, BAR(kv_full), hf * 64, row);
-          tma_load_2d(sbase + kVOff + off, &tm_v, BAR(kv_full), hf * 64, row);
+        if (leader) {
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t off = hf * kHalfBytes + u * p.page_size * 128;
+            tma_load_2d(sbase + kKOff + off, &tm_k, BAR(kv_full), hf * 64, row);
+            tma_load_2d(sbase + kVOff + off, &tm_v, BAR(kv_full), hf * 64, row);
+          }
         }
+        __syncwarp();
       }
       int nq_issued = 0, ndo_issued = 0;
       for (int n = 0; n < n_iter; ++n) {
@@ -220,22 +227,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(BAR(q_empty[s]), phe, wc, kWhereBwdProducer)) break;
         const uint32_t vb = sbase + kVecOff + s * 1024;
         const long voff = static_cast<long>(h) * padded + qi * 128;
-        mbar_arrive_expect_tx(BAR(q_full[s]), kTileBytes + 1024);
-        tma_load_3d(sbase + kQOff + s * kTileBytes, &tm_q, BAR(q_full[s]), 0, h, qi * 128);
-        tma_load_3d(sbase + kQOff + s * kTileBytes + kHalfBytes, &tm_q, BAR(q_full[s]), 64, h,
-                    qi * 128);
-        bulk_load(vb, p.lse2 + voff, 512, BAR(q_full[s]));
-        bulk_load(vb + 512, p.delta + voff, 512, BAR(q_full[s]));
+        if (leader) {
+          mbar_arrive_expect_tx(BAR(q_full[s]), kTileBytes + 1024);
+          tma_load_3d(sbase + kQOff + s * kTileBytes, &tm_q, BAR(q_full[s]), 0, h, qi * 128);
+          tma_load_3d(sbase + kQOff + s * kTileBytes + kHalfBytes, &tm_q, BAR(q_full[s]), 64, h,
+                      qi * 128);
+          bulk_load(vb, p.lse2 + voff, 512, BAR(q_full[s]));
+          bulk_load(vb + 512, p.delta + voff, 512, BAR(q_full[s]));
+        }
+        __syncwarp();
         ++nq_issued;
         if (!mbar_wait(BAR(do_empty[s]), phe, wc, kWhereBwdProducer)) break;
-        mbar_arrive_expect_tx(BAR(do_full[s]), kTileBytes);
-        tma_load_3d(sbase + kDOOff + s * kTileBytes, &tm_do, BAR(do_full[s]), 0, h, qi * 128);
-        tma_load_3d(sbase + kDOOff + s * kTileBytes + kHalfBytes, &tm_do, BAR(do_full[s]), 64, h,
-                    qi * 128);
+        if (leader) {
+          mbar_arrive_expect_tx(BAR(do_full[s]), kTileBytes);
+          tma_load_3d(sbase + kDOOff + s * kTileBytes, &tm_do, BAR(do_full[s]), 0, h, qi * 128);
+          tma_load_3d(sbase + kDOOff + s * kTileBytes + kHalfBytes, &tm_do, BAR(do_full[s]), 64,
+                      h, qi * 128);
+        }
+        __syncwarp();
         ++ndo_issued;
       }
       if (bars->abort_flag) {
-        // unwinding: let every copy this thread issued land before the CTA exits
+        // unwinding: let every copy this warp issued land before the CTA exits
         mbar_drain_wait(BAR(kv_full), 0);
         for (int s = 0; s < 2; ++s) {
           const int lq = (nq_issued - 1 - s) >= 0 ? ((nq_issued - 1 - s) / 2) * 2 + s : -1;

@@ -128,15 +128,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(BAR(q_full), (has_b ? 2u : 1u) * kTileBytes);
-      for (int t = 0; t < (has_b ? 2 : 1); ++t)
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(sbase + kQOff + t * kTileBytes + hf * kHalfBytes, &tm_q, BAR(q_full),
-                      hf * 64, h, (qt_a + t) * 128);
+    // The whole warp runs the loop in lockstep; one elected lane issues.
+    {
+      const bool leader = elect_one();
+      if (leader) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_arrive_expect_tx(BAR(q_full), (has_b ? 2u : 1u) * kTileBytes);
+        for (int t = 0; t < (has_b ? 2 : 1); ++t)
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(sbase + kQOff + t * kTileBytes + hf * kHalfBytes, &tm_q, BAR(q_full),
+                        hf * 64, h, (qt_a + t) * 128);
+      }
+      __syncwarp();
       const int32_t* sel_g = p.sel + static_cast<long>(g) * p.n_sel;
       int issued = 0;                              // ring loads issued (K_0, V_0, K_1, ...)
       for (int j = 0; j < n_tiles; ++j) {
@@ -168,17 +173,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t phe = ((q / kSlots) & 1) ^ 1;
           if (!(ok = mbar_wait(BAR(slot_empty[sl]), phe, wc, kWhereFwdProducer))) break;
           const uint32_t dst = sbase + kRingOff + sl * kTileBytes;
-          mbar_arrive_expect_tx(BAR(slot_full[sl]), kTileBytes);
-          for (int u = 0; u < ppt; ++u)
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_2d(dst + hf * kHalfBytes + u * p.page_size * 128, kv ? &tm_v : &tm_k,
-                          BAR(slot_full[sl]), hf * 64, rows[u]);
+          if (leader) {
+            mbar_arrive_expect_tx(BAR(slot_full[sl]), kTileBytes);
+            for (int u = 0; u < ppt; ++u)
+              for (int hf = 0; hf < 2; ++hf)
+                tma_load_2d(dst + hf * kHalfBytes + u * p.page_size * 128, kv ? &tm_v : &tm_k,
+                            BAR(slot_full[sl]), hf * 64, rows[u]);
+          }
+          __syncwarp();
           ++issued;
         }
         if (!ok) break;
       }
       if (bars->abort_flag) {
-        // unwinding: let every copy this thread issued land before the CTA exits
+        // unwinding: let every copy this warp issued land before the CTA exits
         mbar_drain_wait(BAR(q_full), 0);
         for (int sl = 0; sl < kSlots; ++sl) {
           int last = -1;
