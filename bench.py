@@ -127,6 +127,13 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+# DRAM bytes (read + write) of one backward call -- bwd_prep_kernel +
+# sparse_attn_bwd_kernel + dq_convert_kernel -- from one ncu capture of the
+# current kernels (dram__bytes_read.sum + dram__bytes_write.sum, one pass).
+# Must be re-captured whenever those kernels change.
+BWD_DRAM_BYTES = {"qwen7b_ctx4m_k128": 2_132_424_192}
+
+
 def run_ours(args, rank, world, dev):
     from paged_sparse_attention_oomb_gb300 import oomb
 
@@ -271,7 +278,9 @@ def run_ours(args, rank, world, dev):
         "roofline": {"kernel": "oomb_sparse_attn_bwd (delta prep + sparse_attn_bwd_kernel + dq convert)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_t,
                      "peak_source": f"{pk_src} bf16_tflops_sustained", "unit": "TFLOP/s",
-                     "frac": achieved / peak_t, "traffic": None},
+                     "frac": achieved / peak_t,
+                     "traffic": BWD_DRAM_BYTES.get(wl.name),
+                     "traffic_source": "profiles/dram_traffic_qwen7b_ctx4m_k128.md (ncu, one launch)"},
         "e2e": {"value": world * flops / e2e_ms / 1e9, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * (1 + 3 + 1 + 3),
