@@ -117,16 +117,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same contract as mbar_wait, polling without suspending: for the single
-// thread that issues the MMAs, whose wake-up latency is on the critical path.
+// Same contract as mbar_wait, without the long suspend hint: for the warp that
+// issues the MMAs, whose wake-up latency is on the critical path.
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                                int where) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   uint32_t n = 0;
   while (true) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((++n & 255u) == 0) {
+    // try_wait parks the warp in hardware until the phase completes (or a
+    // short system time limit passes): no issue slots taken from the warps
+    // sharing this SM sub-partition
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 15u) == 0) {
       if (*c.abort_flag) return false;
       if (global_timer_ns() - t0 > c.limit_ns) {
         raise_status(c.status, kStatusTimeout, where);
