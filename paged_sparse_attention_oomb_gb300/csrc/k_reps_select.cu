@@ -260,21 +260,21 @@ __global__ void __launch_bounds__(256) page_scores_kernel(const float* __restric
   const int sub = lane / L, li = lane % L;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const long rows = static_cast<long>(num_pages) * hkv;
-  const long cand_rows = static_cast<long>(n_cand) * hkv;
-  for (long r0 = static_cast<long>(wid) * RPW * U; r0 < rows;
-       r0 += static_cast<long>(warps_total) * RPW * U) {
+  // rows = (page, KV head) pairs; below 2^31 for every supported pool
+  const int rows = num_pages * hkv;
+  const int cand_rows = n_cand * hkv;
+  for (int r0 = wid * RPW * U; r0 < rows; r0 += warps_total * RPW * U) {
     float4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const long r = r0 + u * RPW + sub;
-      v[u] = (r < cand_rows) ? __ldcs(reinterpret_cast<const float4*>(reps) + r * L + li)
+      const int r = r0 + u * RPW + sub;
+      v[u] = (r < cand_rows) ? __ldcs(reinterpret_cast<const float4*>(reps) + static_cast<long>(r) * L + li)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const long r = r0 + u * RPW + sub;
-      const int g = static_cast<int>(r % hkv);
+      const int r = r0 + u * RPW + sub;
+      const int g = r % hkv;
       const float4 qv = qs[g * L + li];
       float s = v[u].x * qv.x;
       s = fmaf(v[u].y, qv.y, s);
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(256) page_scores_kernel(const float* __restric
 #pragma unroll
       for (int off = L / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
       if (li == 0 && r < rows) {
-        const long l = r / hkv;
+        const int l = r / hkv;
         scores[static_cast<long>(g) * num_pages + l] = (r < cand_rows) ? s : -INFINITY;
       }
     }
