@@ -4,27 +4,28 @@
 // "Page-level Sparse Attention": the chunk attends the pages chosen by their
 // representative vectors plus its own pages.
 //
-// One CTA computes two consecutive 128-row query tiles (A, B) of one query
-// head.  Both read the same key tiles -- first the selected pages (ceil(n_sel
-// * P / 128) tiles, masked only in a ragged last tile), then the chunk's own
-// pages up to each tile's diagonal -- so every K/V tile is fetched once for 256
-// query rows.  Roles (320 threads):
-//   warp 0      TMA producer: Q_A, Q_B once; then K_j, V_j page by page through
-//               the page table (one 2-D box per page and 64-column half) into a
-//               5-slot shared ring; also allocates TMEM.
-//   warp 1      MMA issuer (one thread, polling): per key tile j
-//                 S_A = Q_A K_j^T, S_B = Q_B K_j^T        (SS, into TMEM)
-//                 O_A += P_A V_j, O_B += P_B V_j          (P from TMEM)
-//               issuing for whichever tile is ready next.
-//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B, one thread per
-//               query row: the row of S is read from TMEM into registers
-//               once, row maximum, exponentials in base 2, P written back
-//               over S as bf16 pairs.  O is rescaled in TMEM only
-//               when a row maximum grows by more than 2^8 (the final
-//               normalisation uses the same running maximum, so this is exact).
-// While one tile's softmax runs the tensor pipe works on the other tile.
-// TMEM (512 columns): S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384),
-// O_B [384,512).
+// One CTA computes one 128-row query tile of one query head over its key
+// tiles -- first the selected pages (ceil(n_sel * P / 128) tiles, masked only
+// in a ragged last tile), then the chunk's own pages up to the diagonal.  The
+// scores of three consecutive key tiles live in three TMEM buffers, so the
+// MMA S(j+2) = Q K_{j+2}^T only waits for O += P(j-1) V_{j-1} -- an MMA issued
+// one tile earlier -- and the softmax of tile j+1 can follow the softmax of
+// tile j without waiting for the O update of tile j.  Roles (192 threads):
+//   warp 0      TMA producer: Q once; then K_j, V_j page by page through the
+//               page table (one 2-D box per page and 64-column half) into a
+//               6-slot shared ring; also allocates TMEM.
+//   warp 1      MMA issuer (a whole warp in lockstep, one elected lane issues):
+//                 S(j) = Q K_j^T into buffer j % 3      (SS)
+//                 O += P(j) V_j, P(j) in buffer j % 3   (P from TMEM)
+//               in the order S(0), S(1), then per j: O += P(j) V_j, S(j+2).
+//   warps 2..5  softmax, one thread per query row: the row of S is read from
+//               TMEM into registers once, row maximum, exponentials in base 2,
+//               P written back over S as bf16 pairs.  O is rescaled in TMEM
+//               only when a row maximum grows by more than 2^8 (the final
+//               normalisation uses the same running maximum, so this is
+//               exact); the rescale first waits for the previous O update.
+// TMEM (512 columns allocated): S0 [0,128), S1 [128,256), S2 [256,384),
+// O [384,512).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -37,18 +38,25 @@
 namespace oomb {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kSlots = 5;                         // K/V ring
-constexpr uint32_t kQOff = 0;                     // Q_A, Q_B
-constexpr uint32_t kRingOff = 2 * kTileBytes;
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kSlots = 6;                         // K/V ring (3 key tiles)
+constexpr int kSBufs = 3;                         // score buffers in TMEM
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kRingOff = kTileBytes;
 constexpr uint32_t kBarOff = kRingOff + kSlots * kTileBytes;
 constexpr uint32_t kSmemBytes = kBarOff + 256;    // base is 1024-aligned by declaration
+constexpr uint32_t kOCol = 384;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 struct Bars {
   uint64_t q_full;
   uint64_t slot_full[kSlots], slot_empty[kSlots];
-  uint64_t s_full[2], p_ready[2], pv_done[2];
+  // pv_done[b]: the O update that read buffer b is complete.  One barrier per
+  // buffer keeps every waiter at most one phase ahead of the barrier it tests
+  // (a single barrier could lag two O updates behind a waiter, and a parity
+  // test two phases ahead reads as complete).
+  uint64_t s_full[kSBufs], p_ready[kSBufs], pv_done[kSBufs];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -62,7 +70,7 @@ struct FwdParams {
   float* lse;
   int* status;
   int n_sel, hq, hkv, page_size, chunk_len, chunk_start, num_slots;
-  int n_qtiles, n_pairs, t_sel;        // query tiles, tile pairs, selected key tiles
+  int n_qtiles, t_sel;                 // query tiles, selected key tiles
   float scale_log2;
   uint64_t wait_ns;
 };
@@ -88,15 +96,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) raise_status(p.status, kStatusBounds, kWhereFwdProducer);
     return;
   }
-  // heaviest pairs (most own key tiles) first
-  const int pr = p.n_pairs - 1 - static_cast<int>(blockIdx.x) / p.hq;
+  // heaviest query tiles (most own key tiles) first
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / p.hq;
   const int h = static_cast<int>(blockIdx.x) % p.hq;
   const int g = h / (p.hq / p.hkv);
-  const int qt_a = 2 * pr, qt_b = 2 * pr + 1;
-  const bool has_b = qt_b < p.n_qtiles;
-  const int n_a = p.t_sel + qt_a + 1;              // key tiles of tile A
-  const int n_b = has_b ? p.t_sel + qt_b + 1 : 0;  // key tiles of tile B
-  const int n_tiles = has_b ? n_b : n_a;
+  const int n_tiles = p.t_sel + qt + 1;            // key tiles of this query tile
   const int ppt = 128 / p.page_size;               // pages per key tile
   const int own_page0 = p.chunk_start / p.page_size;
   const int n_own_pages = p.chunk_len / p.page_size;
@@ -107,9 +111,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(slot_full[i]), 1);
       mbar_init(BAR(slot_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(BAR(s_full[i]), 1);
-      mbar_init(BAR(p_ready[i]), 128);
+      mbar_init(BAR(p_ready[i]), kSoftmaxThreads);
       mbar_init(BAR(pv_done[i]), 1);
     }
     mbar_init(BAR(drain), 1);
@@ -129,173 +133,143 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop in lockstep; one elected lane issues.
-    {
-      const bool leader = elect_one();
-      if (leader) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(BAR(q_full), (has_b ? 2u : 1u) * kTileBytes);
-        for (int t = 0; t < (has_b ? 2 : 1); ++t)
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_3d(sbase + kQOff + t * kTileBytes + hf * kHalfBytes, &tm_q, BAR(q_full),
-                        hf * 64, h, (qt_a + t) * 128);
-      }
-      __syncwarp();
-      const int32_t* sel_g = p.sel + static_cast<long>(g) * p.n_sel;
-      int issued = 0;                              // ring loads issued (K_0, V_0, K_1, ...)
-      for (int j = 0; j < n_tiles; ++j) {
-        int rows[8];
-        for (int u = 0; u < ppt; ++u) {
-          int lp;
-          if (j < p.t_sel) {
-            const int pi = j * ppt + u;
-            lp = sel_g[pi < p.n_sel ? pi : 0];
-            if (lp < 0 || lp >= own_page0) {
-              raise_status(p.status, kStatusBounds, kWhereFwdProducer);
-              lp = own_page0;
-            }
-          } else {
-            lp = own_page0 + (j - p.t_sel) * ppt + u;
-            if (lp >= own_page0 + n_own_pages) lp = own_page0;
-          }
-          int slot = p.pt[lp];
-          if (slot < 0 || slot >= p.num_slots) {
+    const bool leader = elect_one();
+    if (leader) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(BAR(q_full), kTileBytes);
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_3d(sbase + kQOff + hf * kHalfBytes, &tm_q, BAR(q_full), hf * 64, h, qt * 128);
+    }
+    __syncwarp();
+    const int32_t* sel_g = p.sel + static_cast<long>(g) * p.n_sel;
+    int issued = 0;                                // ring loads issued (K_0, V_0, K_1, ...)
+    for (int j = 0; j < n_tiles; ++j) {
+      int rows[8];
+      for (int u = 0; u < ppt; ++u) {
+        int lp;
+        if (j < p.t_sel) {
+          const int pi = j * ppt + u;
+          lp = sel_g[pi < p.n_sel ? pi : 0];
+          if (lp < 0 || lp >= own_page0) {
             raise_status(p.status, kStatusBounds, kWhereFwdProducer);
-            slot = 0;
+            lp = own_page0;
           }
-          rows[u] = (slot * p.hkv + g) * p.page_size;
+        } else {
+          lp = own_page0 + (j - p.t_sel) * ppt + u;
+          if (lp >= own_page0 + n_own_pages) lp = own_page0;
         }
-        bool ok = true;
-        for (int kv = 0; kv < 2 && ok; ++kv) {
-          const int q = 2 * j + kv;
-          const int sl = q % kSlots;
-          const uint32_t phe = ((q / kSlots) & 1) ^ 1;
-          if (!(ok = mbar_wait(BAR(slot_empty[sl]), phe, wc, kWhereFwdProducer))) break;
-          const uint32_t dst = sbase + kRingOff + sl * kTileBytes;
-          if (leader) {
-            mbar_arrive_expect_tx(BAR(slot_full[sl]), kTileBytes);
-            for (int u = 0; u < ppt; ++u)
-              for (int hf = 0; hf < 2; ++hf)
-                tma_load_2d(dst + hf * kHalfBytes + u * p.page_size * 128, kv ? &tm_v : &tm_k,
-                            BAR(slot_full[sl]), hf * 64, rows[u]);
-          }
-          __syncwarp();
-          ++issued;
+        int slot = p.pt[lp];
+        if (slot < 0 || slot >= p.num_slots) {
+          raise_status(p.status, kStatusBounds, kWhereFwdProducer);
+          slot = 0;
         }
-        if (!ok) break;
+        rows[u] = (slot * p.hkv + g) * p.page_size;
       }
-      if (bars->abort_flag) {
-        // unwinding: let every copy this warp issued land before the CTA exits
-        mbar_drain_wait(BAR(q_full), 0);
-        for (int sl = 0; sl < kSlots; ++sl) {
-          int last = -1;
-          for (int q = sl; q < issued; q += kSlots) last = q;
-          if (last >= 0) mbar_drain_wait(BAR(slot_full[sl]), (last / kSlots) & 1);
+      bool ok = true;
+      for (int kv = 0; kv < 2 && ok; ++kv) {
+        const int q = 2 * j + kv;
+        const int sl = q % kSlots;
+        const uint32_t phe = ((q / kSlots) & 1) ^ 1;
+        if (!(ok = mbar_wait(BAR(slot_empty[sl]), phe, wc, kWhereFwdProducer))) break;
+        const uint32_t dst = sbase + kRingOff + sl * kTileBytes;
+        if (leader) {
+          mbar_arrive_expect_tx(BAR(slot_full[sl]), kTileBytes);
+          for (int u = 0; u < ppt; ++u)
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_2d(dst + hf * kHalfBytes + u * p.page_size * 128, kv ? &tm_v : &tm_k,
+                          BAR(slot_full[sl]), hf * 64, rows[u]);
         }
+        __syncwarp();
+        ++issued;
+      }
+      if (!ok) break;
+    }
+    if (bars->abort_flag) {
+      // unwinding: let every copy this warp issued land before the CTA exits
+      mbar_drain_wait(BAR(q_full), 0);
+      for (int sl = 0; sl < kSlots; ++sl) {
+        int last = -1;
+        for (int q = sl; q < issued; q += kSlots) last = q;
+        if (last >= 0) mbar_drain_wait(BAR(slot_full[sl]), (last / kSlots) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Per tile X the sequence is S_X(0), PV_X(0), S_X(1), PV_X(1), ...; the
-    // issuer polls both tiles and issues whichever next step is ready, so
-    // neither softmax group waits behind the other.  S_X(j) overwrites P_X(j-1),
-    // so it waits for PV_X(j-1) to complete (pv_done).  A ring slot is released
-    // once both tiles have issued the MMAs that read it.  The whole warp runs
-    // the loop in lockstep (its decisions are warp-uniform); one elected lane
-    // issues the MMAs and commits.
-    {
-      constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
-      bool ok = mbar_wait_spin(BAR(q_full), 0, wc, kWhereFwdMma);
-      const int nt[2] = {n_a, n_b};
-      const uint64_t d0 = desc_kmajor0(sbase);
-      const uint64_t dQ0 = d0 + desc_off(kQOff);
-      const uint64_t dRing_k = d0 + desc_off(kRingOff), dRing_mn = d0 + kDescMn + desc_off(kRingOff);
-      int sj[2] = {0, 0};                          // S issued for tiles [0, sj)
-      int pj[2] = {0, 0};                          // PV issued for tiles [0, pj)
-      uint64_t t_last = global_timer_ns();
-      uint32_t polls = 0;
-      while (ok && (pj[0] < nt[0] || pj[1] < nt[1])) {
-        bool progress = false;
+    // The whole warp runs the loop in lockstep (its decisions are warp-uniform);
+    // one elected lane issues the MMAs and their commits.
+    constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
+    const uint64_t d0 = desc_kmajor0(sbase);
+    const uint64_t dQ = d0 + desc_off(kQOff);
+    const uint64_t dRing_k = d0 + desc_off(kRingOff), dRing_mn = d0 + kDescMn + desc_off(kRingOff);
+    bool ok = mbar_wait_spin(BAR(q_full), 0, wc, kWhereFwdMma);
+    // S(j) = Q K_j^T into buffer j % 3.  The buffer last held P(j-3), read by
+    // the O update of tile j-3, which must be complete.
+    auto issue_s = [&](int j) -> bool {
+      const int sk = (2 * j) % kSlots, b = j % kSBufs;
+      if (!mbar_wait_spin(BAR(slot_full[sk]), ((2 * j) / kSlots) & 1, wc, kWhereFwdMma))
+        return false;
+      if (j >= kSBufs && !mbar_wait_spin(BAR(pv_done[b]), ((j - kSBufs) / kSBufs) & 1, wc,
+                                         kWhereFwdMma))
+        return false;
+      tc_fence_after();
+      const uint64_t qa = opaque(dQ), ka = opaque(dRing_k + sk * kTileDesc);
+      if (elect_one()) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (sj[t] == pj[t] && sj[t] < nt[t]) {
-            const int j = sj[t];
-            const int sk = (2 * j) % kSlots;
-            if (mbar_test_wait(BAR(slot_full[sk]), ((2 * j) / kSlots) & 1) &&
-                (j == 0 || mbar_test_wait(BAR(pv_done[t]), (j - 1) & 1))) {
-              tc_fence_after();
-              const uint64_t qa = dQ0 + t * kTileDesc;
-              const uint64_t ka = dRing_k + sk * kTileDesc;
-              const bool rel = sj[t ^ 1] > j || j >= nt[t ^ 1];
-              if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                  umma_ss(tmem + t * 128, qa + kstep_kmajor(kk), ka + kstep_kmajor(kk), kIdQK, kk > 0);
-                umma_commit(BAR(s_full[t]));
-                if (rel) umma_commit(BAR(slot_empty[sk]));
-              }
-              __syncwarp();
-              sj[t] = j + 1;
-              progress = true;
-            }
-          } else if (pj[t] < sj[t]) {
-            const int j = pj[t];
-            const int sv = (2 * j + 1) % kSlots;
-            if (mbar_test_wait(BAR(slot_full[sv]), ((2 * j + 1) / kSlots) & 1) &&
-                mbar_test_wait(BAR(p_ready[t]), j & 1)) {
-              tc_fence_after();
-              const uint64_t va = dRing_mn + sv * kTileDesc;
-              const bool rel = pj[t ^ 1] > j || j >= nt[t ^ 1];
-              // O_X += P_X V_j (P_X in TMEM as bf16 pairs over S_X, 8 columns per k-step)
-              if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                  umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, va + kstep_mnmajor(kk),
-                          kIdPV, (j > 0 || kk > 0));
-                umma_commit(BAR(pv_done[t]));
-                if (rel) umma_commit(BAR(slot_empty[sv]));
-              }
-              __syncwarp();
-              pj[t] = j + 1;
-              progress = true;
-            }
-          }
-        }
-        if (progress) {
-          t_last = global_timer_ns();
-        } else if ((++polls & 255u) == 0) {
-          if (bars->abort_flag) {
-            ok = false;
-          } else if (global_timer_ns() - t_last > wc.limit_ns) {
-            raise_status(p.status, kStatusTimeout, kWhereFwdMma);
-            bars->abort_flag = 1;
-            ok = false;
-          }
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + b * 128, qa + kstep_kmajor(kk), ka + kstep_kmajor(kk), kIdQK, kk > 0);
+        umma_commit(BAR(s_full[b]));
+        umma_commit(BAR(slot_empty[sk]));
       }
-      if (!ok) {
-        if (elect_one()) umma_commit(BAR(drain));
-        __syncwarp();
-        mbar_drain_wait(BAR(drain), 0);
+      __syncwarp();
+      return true;
+    };
+    // O += P(j) V_j  (P(j) in buffer j % 3 as bf16 pairs, 8 columns per k-step)
+    auto issue_pv = [&](int j) -> bool {
+      const int sv = (2 * j + 1) % kSlots, b = j % kSBufs;
+      if (!mbar_wait_spin(BAR(slot_full[sv]), ((2 * j + 1) / kSlots) & 1, wc, kWhereFwdMma))
+        return false;
+      if (!mbar_wait_spin(BAR(p_ready[b]), (j / kSBufs) & 1, wc, kWhereFwdMma)) return false;
+      tc_fence_after();
+      const uint64_t va = opaque(dRing_mn + sv * kTileDesc);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + kOCol, tmem + b * 128 + kk * 8, va + kstep_mnmajor(kk), kIdPV,
+                  (j > 0 || kk > 0));
+        umma_commit(BAR(pv_done[b]));
+        umma_commit(BAR(slot_empty[sv]));
       }
+      __syncwarp();
+      return true;
+    };
+    // O += P(j) V_j goes first: S(j+2) waits for the O update of tile j-1, which
+    // is done by then, while the O update of tile j is what the pipe needs next
+    for (int j = 0; ok && j < n_tiles && j < 2; ++j) ok = issue_s(j);
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      if (!(ok = issue_pv(j))) break;
+      if (j + 2 < n_tiles && !(ok = issue_s(j + 2))) break;
+    }
+    if (!ok) {
+      if (elect_one()) umma_commit(BAR(drain));
+      __syncwarp();
+      mbar_drain_wait(BAR(drain), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int tsel = (warp - 2) >> 2;              // 0: tile A, 1: tile B
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;                  // row of the query tile
-    const int qt = qt_a + tsel;
     const int t = qt * 128 + r;                    // chunk row
-    const int n_mine = tsel == 0 ? n_a : n_b;
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + tsel * 128;
-    const uint32_t t_o = tmem + lane_base + 256 + tsel * 128;
+    const uint32_t t_o = tmem + lane_base + kOCol;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_mine; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full[tsel]), j & 1, wc, kWhereFwdSoftmax));
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j % kSBufs;
+      const uint32_t t_s = tmem + lane_base + b * 128;
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full[b]), (j / kSBufs) & 1, wc, kWhereFwdSoftmax));
       if (!ok) break;
       tc_fence_after();
       // the whole row of S in registers: one TMEM round trip per tile
@@ -343,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
         }
       }
-      // P = exp2(s * scale_log2 - m) -> bf16 pairs into S's first 64 columns
-      // (S is already in registers), 8 partial row sums
+      // P = exp2(s * scale_log2 - m) -> bf16 pairs into the buffer's first 64
+      // columns (S is already in registers), 8 partial row sums
       const float neg_m = -m;
       float rs[8];
 #pragma unroll
@@ -363,7 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(t_s + c4 * 16, pk);
       }
       if (any_need) {
-        // O_X is stable here: S_X of tile j was issued after PV_X of tile j-1 completed
+        // O must be stable: wait for the O update of tile j-1 (the one of tile j
+        // waits for this thread's p_ready)
+        const int jp = j - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(BAR(pv_done[jp % kSBufs]), (jp / kSBufs) & 1, wc,
+                                               kWhereFwdSoftmax));
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll 1
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t rr[32];
@@ -376,13 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
       tc_fence_before();
-      mbar_arrive(BAR(p_ready[tsel]));
+      mbar_arrive(BAR(p_ready[b]));
     }
-    if (ok && n_mine > 0) {
-      const int jl = n_mine - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(pv_done[tsel]), jl & 1, wc, kWhereFwdSoftmax));
+    if (ok && n_tiles > 0) {
+      const int jl = n_tiles - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(pv_done[jl % kSBufs]), (jl / kSBufs) & 1, wc,
+                                             kWhereFwdSoftmax));
     }
-    if (ok && n_mine > 0) {
+    if (ok && n_tiles > 0) {
       tc_fence_after();
       const float inv = 1.f / l;
       const bool row_ok = t < p.chunk_len;
@@ -450,7 +431,6 @@ cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t*
   p.chunk_start = chunk_start;
   p.num_slots = kv.num_slots;
   p.n_qtiles = (chunk_len + 127) / 128;
-  p.n_pairs = (p.n_qtiles + 1) / 2;
   p.t_sel = (n_sel * kv.page_size + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = wait_ns;
@@ -461,7 +441,7 @@ cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t*
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  sparse_attn_fwd_kernel<<<p.n_pairs * hq, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  sparse_attn_fwd_kernel<<<p.n_qtiles * hq, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
