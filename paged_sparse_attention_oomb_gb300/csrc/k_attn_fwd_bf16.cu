@@ -10,7 +10,7 @@
 // scores of three consecutive key tiles live in three TMEM buffers, so the
 // MMA S(j+2) = Q K_{j+2}^T only waits for O += P(j-1) V_{j-1} -- an MMA issued
 // one tile earlier -- and the softmax of tile j+1 can follow the softmax of
-// tile j without waiting for the O update of tile j.  Roles (192 threads):
+// tile j without waiting for the O update of tile j.  Roles (320 threads):
 //   warp 0      TMA producer: Q once; then K_j, V_j page by page through the
 //               page table (one 2-D box per page and 64-column half) into a
 //               6-slot shared ring; also allocates TMEM.
@@ -18,9 +18,11 @@
 //                 S(j) = Q K_j^T into buffer j % 3      (SS)
 //                 O += P(j) V_j, P(j) in buffer j % 3   (P from TMEM)
 //               in the order S(0), S(1), then per j: O += P(j) V_j, S(j+2).
-//   warps 2..5  softmax, one thread per query row: the row of S is read from
-//               TMEM into registers once, row maximum, exponentials in base 2,
-//               P written back over S as bf16 pairs.  O is rescaled in TMEM
+//   warps 2..9  softmax, two threads per query row (warps w and w + 4 share a
+//               TMEM lane quarter and split the 128 key columns): the half row
+//               of S is read from TMEM into registers once, the row maximum is
+//               completed through shared memory, exponentials in base 2, P
+//               written back over S as bf16 pairs.  O is rescaled in TMEM
 //               only when a row maximum grows by more than 2^8 (the final
 //               normalisation uses the same running maximum, so this is
 //               exact); the rescale first waits for the previous O update.
@@ -38,14 +40,15 @@
 namespace oomb {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
 constexpr int kSlots = 6;                         // K/V ring (3 key tiles)
 constexpr int kSBufs = 3;                         // score buffers in TMEM
 constexpr uint32_t kQOff = 0;
 constexpr uint32_t kRingOff = kTileBytes;
 constexpr uint32_t kBarOff = kRingOff + kSlots * kTileBytes;
-constexpr uint32_t kSmemBytes = kBarOff + 256;    // base is 1024-aligned by declaration
+constexpr uint32_t kXchgOff = kBarOff + 256;      // row-max / row-sum exchange [2][4][2][32] floats
+constexpr uint32_t kSmemBytes = kXchgOff + 2 * 4 * 2 * 32 * 4;  // base is 1024-aligned
 constexpr uint32_t kOCol = 384;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
@@ -57,6 +60,7 @@ struct Bars {
   // (a single barrier could lag two O updates behind a waiter, and a parity
   // test two phases ahead reads as complete).
   uint64_t s_full[kSBufs], p_ready[kSBufs], pv_done[kSBufs];
+  uint64_t pair[4];           // the two softmax warps of a TMEM lane quarter
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -116,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(p_ready[i]), kSoftmaxThreads);
       mbar_init(BAR(pv_done[i]), 1);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(BAR(pair[i]), 64);
     mbar_init(BAR(drain), 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -226,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    // O += P(j) V_j  (P(j) in buffer j % 3 as bf16 pairs, 8 columns per k-step)
+    // O += P(j) V_j  (P(j) in buffer j % 3 as bf16 pairs, 8 columns per k-step;
+    // keys [64 c, 64 c + 64) sit at buffer columns [64 c, 64 c + 32))
     auto issue_pv = [&](int j) -> bool {
       const int sv = (2 * j + 1) % kSlots, b = j % kSBufs;
       if (!mbar_wait_spin(BAR(slot_full[sv]), ((2 * j + 1) / kSlots) & 1, wc, kWhereFwdMma))
@@ -237,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kOCol, tmem + b * 128 + kk * 8, va + kstep_mnmajor(kk), kIdPV,
-                  (j > 0 || kk > 0));
+          umma_ts(tmem + kOCol, tmem + b * 128 + 64 * (kk >> 2) + 8 * (kk & 3),
+                  va + kstep_mnmajor(kk), kIdPV, (j > 0 || kk > 0));
         umma_commit(BAR(pv_done[b]));
         umma_commit(BAR(slot_empty[sv]));
       }
@@ -259,23 +265,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
+    // Two warps per TMEM lane quarter (the same 32 query rows): warp half
+    // ch = 0 takes key columns [0, 64), ch = 1 columns [64, 128).  Their
+    // partial row maxima (and at the end their partial row sums) meet in
+    // shared memory behind a per-quarter mbarrier (bounded waits).
     const int q4 = warp & 3;
+    const int ch = (warp - 2) >> 2;
     const int r = q4 * 32 + lane;                  // row of the query tile
     const int t = qt * 128 + r;                    // chunk row
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t t_o = tmem + lane_base + kOCol;
-    float m = -INFINITY, l = 0.f;
+    const uint32_t t_o = tmem + lane_base + kOCol + 64 * ch;   // this warp's O columns
+    float* xchg = reinterpret_cast<float*>(smem + kXchgOff);  // [2][4][2][32]
+    auto slot = [&](int par, int c) -> float* { return xchg + ((par * 4 + q4) * 2 + c) * 32 + lane; };
+    float m = -INFINITY, l = 0.f;                  // l: this warp's partial row sum
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j % kSBufs;
-      const uint32_t t_s = tmem + lane_base + b * 128;
+      const uint32_t t_s = tmem + lane_base + b * 128 + 64 * ch;
       ok = __all_sync(0xffffffffu, mbar_wait(BAR(s_full[b]), (j / kSBufs) & 1, wc, kWhereFwdSoftmax));
       if (!ok) break;
       tc_fence_after();
-      // the whole row of S in registers: one TMEM round trip per tile
-      uint32_t sr[128];
-      tmem_ld128(t_s, sr);
-      // valid columns are [0, lim); `masked` is uniform over the warp group
+      uint32_t sr[64];
+      tmem_ld64(t_s, sr);
+      // valid key columns are [0, lim); `masked` is uniform over the warp
       int lim = 128;
       bool masked = false;
       if (j < p.t_sel) {
@@ -290,20 +302,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < 64; ++c)
+          if (64 * ch + c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      // row maximum of the raw scores (scale > 0 commutes with max), 8 chains
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
 #pragma unroll
-      for (int c = 8; c < 128; c += 8)
+      for (int c = 8; c < 64; c += 8)
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(sr[c + i]));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+      const float mp = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // exchange the partial maxima of the row with the other half
+      *slot(j & 1, ch) = mp;
+      mbar_arrive(BAR(pair[q4]));
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(pair[q4]), j & 1, wc, kWhereFwdSoftmax));
+      if (!ok) break;
+      const float mt = fmaxf(mp, *slot(j & 1, ch ^ 1)) * p.scale_log2;
       // lazy rescale: m moves only when the row maximum grows by more than 2^8
+      // (both halves take the same decision from the same row maximum)
       float alpha = 1.f;
       bool any_need = false;
       if (j == 0) {
@@ -317,25 +335,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
         }
       }
-      // P = exp2(s * scale_log2 - m) -> bf16 pairs into the buffer's first 64
+      // P = exp2(s * scale_log2 - m) -> bf16 pairs into this warp's first 32
       // columns (S is already in registers), 8 partial row sums
       const float neg_m = -m;
       float rs[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float e0 = ex2(fmaf(__uint_as_float(sr[32 * c4 + i]), p.scale_log2, neg_m));
-          const float e1 = ex2(fmaf(__uint_as_float(sr[32 * c4 + i + 1]), p.scale_log2, neg_m));
-          rs[i & 7] += e0;
-          rs[(i & 7) + 1] += e1;
-          pk[i >> 1] = pack_bf16(e0, e1);
-        }
-        tmem_st16(t_s + c4 * 16, pk);
+      for (int i = 0; i < 64; i += 2) {
+        const float e0 = ex2(fmaf(__uint_as_float(sr[i]), p.scale_log2, neg_m));
+        const float e1 = ex2(fmaf(__uint_as_float(sr[i + 1]), p.scale_log2, neg_m));
+        rs[i & 7] += e0;
+        rs[(i & 7) + 1] += e1;
+        pk[i >> 1] = pack_bf16(e0, e1);
       }
+      tmem_st32(t_s, pk);
       if (any_need) {
         // O must be stable: wait for the O update of tile j-1 (the one of tile j
         // waits for this thread's p_ready)
@@ -345,12 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t rr[32];
-          tmem_ld32(t_o + c4 * 32, rr);
+          tmem_ld32(t_o + c2 * 32, rr);
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-          tmem_st32(t_o + c4 * 32, rr);
+          tmem_st32(t_o + c2 * 32, rr);
         }
       }
       tmem_st_wait();
@@ -364,14 +379,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              kWhereFwdSoftmax));
     }
     if (ok && n_tiles > 0) {
+      // full row sum from the two halves (one more phase of the pair barrier)
+      *slot(n_tiles & 1, ch) = l;
+      mbar_arrive(BAR(pair[q4]));
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(pair[q4]), n_tiles & 1, wc, kWhereFwdSoftmax));
+    }
+    if (ok && n_tiles > 0) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float lt = l + *slot(n_tiles & 1, ch ^ 1);
+      const float inv = 1.f / lt;
       const bool row_ok = t < p.chunk_len;
-      uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<long>(t) * p.hq + h) * 128);
+      uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<long>(t) * p.hq + h) * 128 + 64 * ch);
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t rr[32];
-        tmem_ld32(t_o + c4 * 32, rr);
+        tmem_ld32(t_o + c2 * 32, rr);
         if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -380,12 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             v.y = pack_bf16(__uint_as_float(rr[8 * i + 2]) * inv, __uint_as_float(rr[8 * i + 3]) * inv);
             v.z = pack_bf16(__uint_as_float(rr[8 * i + 4]) * inv, __uint_as_float(rr[8 * i + 5]) * inv);
             v.w = pack_bf16(__uint_as_float(rr[8 * i + 6]) * inv, __uint_as_float(rr[8 * i + 7]) * inv);
-            orow[c4 * 4 + i] = v;
+            orow[c2 * 4 + i] = v;
           }
         }
       }
-      if (row_ok)
-        p.lse[static_cast<long>(h) * p.chunk_len + t] = (m + __log2f(l)) * 0.69314718055994530942f;
+      if (row_ok && ch == 0)
+        p.lse[static_cast<long>(h) * p.chunk_len + t] = (m + __log2f(lt)) * 0.69314718055994530942f;
     }
   }
   tc_fence_before();
