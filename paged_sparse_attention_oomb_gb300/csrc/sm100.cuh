@@ -269,20 +269,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 constexpr uint32_t kHalfBytes = 128 * 128;   // one 64-column half of a tile128
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;
 
-// tile128 as a K-major operand: rows are M (or N), columns are K.  k-step kk
-// covers columns [16 kk, 16 kk + 16).
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
-  return sdesc_sw128(tile + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-}
-// tile128 as an MN-major operand: rows are K, columns are M (or N).  k-step kk
-// covers rows [16 kk, 16 kk + 16).
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
-  return sdesc_sw128(tile + kk * 2048, kHalfBytes, 1024);
-}
-
-// The same descriptors split into a per-tile base (computed once) and a
-// per-k-step constant added to the start-address field (shared addresses are
-// below 256 KiB, so the 14-bit field never carries).  Keeps the MMA-issuing
+// tile128 operand descriptors, split into a per-tile base (computed once) and a
+// per-k-step constant added to the start-address field.  K-major (rows are M or
+// N, columns are K): k-step kk covers columns [16 kk, 16 kk + 16) at byte
+// offset (kk / 4) * 16 KiB + (kk % 4) * 32; leading byte offset 16, stride 1024.
+// MN-major (rows are K, columns are M or N): k-step kk covers rows
+// [16 kk, 16 kk + 16) at byte offset kk * 2048; leading byte offset one
+// 64-column half, stride 1024.  The split is exact because shared addresses are
+// below 256 KiB, so the 14-bit field never carries.  Keeps the MMA-issuing
 // thread to a handful of instructions per MMA: it shares its SM sub-partition
 // with busy compute warps.
 __device__ __forceinline__ uint64_t desc_kmajor0(uint32_t tile) {
@@ -374,22 +368,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
       : "r"(taddr), "r"(taddr + 64)
       : "memory");
 }
-// 32 columns at `ta` and 16 columns at `tb` of this thread's lane, one wait.
-__device__ __forceinline__ void tmem_ld32_16(uint32_t ta, uint32_t (&a)[32], uint32_t tb,
-                                             uint32_t (&b)[16]) {
-  __syncwarp();
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%48];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%49];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : OOMB_O8(a, 0), OOMB_O8(a, 8), OOMB_O8(a, 16), OOMB_O8(a, 24), OOMB_O8(b, 0),
-        OOMB_O8(b, 8)
-      : "r"(ta), "r"(tb)
-      : "memory");
-}
 #undef OOMB_O8
 // Warpgroup register reallocation (all four warps of the warpgroup execute it).
 template <uint32_t N>
@@ -399,10 +377,6 @@ __device__ __forceinline__ void regs_increase() {
 template <uint32_t N>
 __device__ __forceinline__ void regs_decrease() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-// Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 #define OOMB_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
                    "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
@@ -416,16 +390,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 #undef OOMB_W8
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  __syncwarp();
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -452,12 +416,6 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ void red_add_f32(float* addr, float a) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
 }
 
 }  // namespace oomb
