@@ -127,11 +127,55 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+CHUNK_PASS_WORKLOAD = "qwen7b_dense_ctx32k"
+
+
+def chunk_pass_flops(wl):
+    """14 * D * Hq * unmasked pairs, summed over the chunks of a whole pass:
+    chunk c attends min(top_k, c * C / P) past pages plus its causal own keys."""
+    c, p = wl.chunk_len, wl.page_size
+    pairs = sum(min(wl.top_k, ci * c // p) * p * c + c * (c + 1) // 2
+                for ci in range(wl.context // c))
+    return 14.0 * wl.head_dim * wl.num_q_heads * pairs
+
+
+def measure_chunk_pass(dev, peak_t, passes=3):
+    """The chunk-recurrent pass over the whole 32K-token sequence (8 chunks of
+    4096, every past page selected): forward over the chunks in order, with the
+    representatives of each chunk's pages computed after its forward, then the
+    backward in reverse order accumulating dK/dV in place -- one call of
+    ``oomb.chunk_recurrent_pass``, timed with CUDA events."""
+    from paged_sparse_attention_oomb_gb300 import oomb
+    wl = WORKLOADS[CHUNK_PASS_WORKLOAD]
+    x = make_inputs(wl, seed=0, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    shape = (wl.context, wl.num_q_heads, wl.head_dim)
+    q_full = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+    do_full = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+    kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, torch.zeros_like(x.k_pool),
+                      torch.zeros_like(x.v_pool))
+    oomb.chunk_recurrent_pass(q_full, do_full, kv, wl.chunk_len, wl.top_k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(passes):
+        oomb.chunk_recurrent_pass(q_full, do_full, kv, wl.chunk_len, wl.top_k)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / passes
+    flops = chunk_pass_flops(wl)
+    return {"workload": wl.name, "context": wl.context, "chunks": wl.context // wl.chunk_len,
+            "chunk_len": wl.chunk_len, "passes": passes, "ms_per_pass": ms,
+            "TFLOP/s": flops / ms / 1e9, "frac_bf16": flops / ms / 1e9 / peak_t,
+            "what": "reps + selection + fwd per chunk in order, bwd in reverse; dK/dV in place"}
+
+
 # DRAM bytes (read + write) of one backward call -- bwd_prep_kernel +
 # sparse_attn_bwd_kernel + dq_convert_kernel -- from one ncu capture of the
 # current kernels (dram__bytes_read.sum + dram__bytes_write.sum, one pass).
 # Must be re-captured whenever those kernels change.
-BWD_DRAM_BYTES = {"qwen7b_ctx4m_k128": 2_162_659_840}
+BWD_DRAM_BYTES = {}
 
 
 def run_ours(args, rank, world, dev):
@@ -235,6 +279,8 @@ def run_ours(args, rank, world, dev):
 
     flops = attn_flops(wl)
     pk, pk_src = peaks()
+    chunk_pass = (measure_chunk_pass(dev, pk["bf16_tflops_sustained"])
+                  if args.chunk_pass and wl.dtype == "bf16" else None)
     pairs_total = pairs_per_head(wl) * hq
     bwd_flops = 10.0 * d * pairs_total
     fwd_flops = 4.0 * d * pairs_total
@@ -275,6 +321,7 @@ def run_ours(args, rank, world, dev):
         "tokens_per_s_per_chunk": world * c / (ms / 1e3),
         "frac_of_bf16_peak": flops / ms / 1e9 / peak_t,
         "kernels": kern,
+        "chunk_pass": chunk_pass,
         "roofline": {"kernel": "oomb_sparse_attn_bwd (delta prep + sparse_attn_bwd_kernel + dq convert)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_t,
                      "peak_source": f"{pk_src} bf16_tflops_sustained", "unit": "TFLOP/s",
@@ -374,6 +421,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-chunk-pass", dest="chunk_pass", action="store_false",
+                    help="skip the whole-sequence chunk-recurrent pass measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -166,6 +166,25 @@ oomb_status oomb_sparse_attn_fwd(const void *q, const oomb_paged_kv *kv, const i
                                  int32_t chunk_start, float scale, void *o, float *lse, void *ws,
                                  size_t ws_bytes, void *stream);
 
+/* Step 3 with step 1 of the chunk's own pages fused in (Chunk-Recurrent
+ * Training Framework: the pages a chunk writes become candidates for the
+ * chunks after it, so their representatives are needed as soon as the
+ * chunk's forward is done).  Computes exactly what oomb_sparse_attn_fwd
+ * computes and, in addition, reps[l][g][*] for the chunk's own pages
+ * l in [chunk_start/P, (chunk_start+chunk_len)/P) and every KV head g --
+ * the same values oomb_page_reps writes for those pages (bf16: bit-identical;
+ * the forward kernel sums the K tiles it has already loaded into shared
+ * memory in oomb_page_reps's order, so the chunk's keys are not read again).
+ * reps: float [num_pages][Hkv][D], 16-byte aligned; other rows are not
+ * touched.  fp32 pools: the representatives come from the representatives
+ * kernel launched after the forward on the same stream (not fused).
+ * Arguments, workspace and errors as oomb_sparse_attn_fwd. */
+oomb_status oomb_sparse_attn_fwd_own_reps(const void *q, const oomb_paged_kv *kv,
+                                          const int32_t *sel, int32_t n_sel,
+                                          int32_t num_q_heads, int32_t chunk_len,
+                                          int32_t chunk_start, float scale, void *o, float *lse,
+                                          float *reps, void *ws, size_t ws_bytes, void *stream);
+
 /* Step 4 -- sparse attention backward with in-place paged gradient
  * accumulation (Paged Memory Management: gradients of the KV cache are
  * paged and accumulated in place; Page-level Sparse Attention: the selection

@@ -427,15 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t rr[64];
           tmem_ld64(t_r0 + 64 * ch, rr);
           if (warp_valid && !diag) {               // no mask: the common case
+            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
-            for (int i = 0; i < 64; i += 4) {
+            for (int i = 0; i < 64; i += 4) {       // scaling on packed FP32 pairs
               const float4 l = lse4[i >> 2];
-              const float e0 = ex2(fmaf(__uint_as_float(rr[i]), p.scale_log2, -l.x));
-              const float e1 = ex2(fmaf(__uint_as_float(rr[i + 1]), p.scale_log2, -l.y));
-              const float e2 = ex2(fmaf(__uint_as_float(rr[i + 2]), p.scale_log2, -l.z));
-              const float e3 = ex2(fmaf(__uint_as_float(rr[i + 3]), p.scale_log2, -l.w));
-              pk[i >> 1] = pack_bf16(e0, e1);
-              pk[(i >> 1) + 1] = pack_bf16(e2, e3);
+              float x0, x1, x2, x3;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])), sc2,
+                               f2_pack(-l.x, -l.y)), x0, x1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])),
+                               sc2, f2_pack(-l.z, -l.w)), x2, x3);
+              pk[i >> 1] = pack_bf16(ex2(x0), ex2(x1));
+              pk[(i >> 1) + 1] = pack_bf16(ex2(x2), ex2(x3));
             }
           } else {
 #pragma unroll
@@ -476,13 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
             const float4 dl = dl4[(32 * cc + i) >> 2];
-            const float dv[4] = {dl.x, dl.y, dl.z, dl.w};
+            const uint64_t dv2[2] = {f2_pack(dl.x, dl.y), f2_pack(dl.z, dl.w)};
             float d[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4; j += 2) {        // two columns per packed FP32 pair
               const uint32_t pw = pk[16 * cc + ((i + j) >> 1)];
-              const float pv = __uint_as_float(((i + j) & 1) ? (pw & 0xFFFF0000u) : (pw << 16));
-              d[j] = pv * (__uint_as_float(dp[i + j]) - dv[j]);
+              const uint64_t p2 = f2_pack(__uint_as_float(pw << 16), __uint_as_float(pw & 0xFFFF0000u));
+              const uint64_t x2 = f2_sub(
+                  f2_pack(__uint_as_float(dp[i + j]), __uint_as_float(dp[i + j + 1])), dv2[j >> 1]);
+              f2_unpack(f2_mul(p2, x2), d[j], d[j + 1]);
             }
             w[i >> 1] = pack_bf16(d[0], d[1]);
             w[(i >> 1) + 1] = pack_bf16(d[2], d[3]);

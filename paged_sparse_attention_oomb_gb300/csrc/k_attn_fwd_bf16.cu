@@ -72,6 +72,7 @@ struct FwdParams {
   const int32_t* pt;
   __nv_bfloat16* o;
   float* lse;
+  float* reps;                         // own-page representatives, or null
   int* status;
   int n_sel, hq, hkv, page_size, chunk_len, chunk_start, num_slots;
   int n_qtiles, t_sel;                 // query tiles, selected key tiles
@@ -191,6 +192,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
     }
+    if (p.reps != nullptr && h % (p.hq / p.hkv) == 0 && !bars->abort_flag) {
+      // Step 1 for the chunk's own pages, from the K tile already in shared
+      // memory: the last key tile of this CTA is own tile qt, and the first
+      // query head of each group writes the representatives of its pages.
+      // Same summation order as page_reps_kernel (16 row groups, rows
+      // rg, rg + 16, ... in order, then the groups in order), so the values
+      // are bit-identical to a separate representatives pass.
+      const int q = 2 * (n_tiles - 1);
+      const int sl = q % kSlots;
+      if (mbar_wait(BAR(slot_full[sl]), (q / kSlots) & 1, wc, kWhereFwdProducer)) {
+        const uint32_t tile = sbase + kRingOff + sl * kTileBytes;
+        // this lane's 4 columns [4 lane, 4 lane + 4): half, 16-byte chunk, offset in chunk
+        const uint32_t col_off = (lane >> 4) * kHalfBytes + (lane & 1) * 8;
+        const int chunk = (lane & 15) >> 1;
+        const float inv_p = 1.0f / static_cast<float>(p.page_size);
+        for (int u = 0; u < ppt; ++u) {
+          const int op = qt * ppt + u;                 // own page index in the chunk
+          if (op >= n_own_pages) break;
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int rg = 0; rg < 16; ++rg) {
+            float a4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int rr = rg; rr < p.page_size; rr += 16) {
+              const int row = u * p.page_size + rr;
+              const uint32_t addr = tile + col_off + row * 128 + ((chunk ^ (row & 7)) << 4);
+              uint32_t w0, w1;
+              asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(addr));
+              a4[0] += __uint_as_float(w0 << 16);
+              a4[1] += __uint_as_float(w0 & 0xFFFF0000u);
+              a4[2] += __uint_as_float(w1 << 16);
+              a4[3] += __uint_as_float(w1 & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s4[e] += a4[e];
+          }
+          float4* dst = reinterpret_cast<float4*>(
+              p.reps + (static_cast<long>(own_page0 + op) * p.hkv + g) * 128) + lane;
+          *dst = make_float4(s4[0] * inv_p, s4[1] * inv_p, s4[2] * inv_p, s4[3] * inv_p);
+        }
+      }
+    }
     if (bars->abort_flag) {
       // unwinding: let every copy this warp issued land before the CTA exits
       mbar_drain_wait(BAR(q_full), 0);
@@ -307,13 +348,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
+      for (int i = 0; i < 8; ++i)
+        mx[i] = fmax3(__uint_as_float(sr[i]), __uint_as_float(sr[8 + i]),
+                      __uint_as_float(sr[16 + i]));
 #pragma unroll
-      for (int c = 8; c < 64; c += 8)
+      for (int c = 24; c < 56; c += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(sr[c + i]));
-      const float mp = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int i = 0; i < 8; ++i)
+          mx[i] = fmax3(mx[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(sr[56 + i]));
+      const float mp = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7]));
       // exchange the partial maxima of the row with the other half
       *slot(j & 1, ch) = mp;
       mbar_arrive(BAR(pair[q4]));
@@ -336,20 +382,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // P = exp2(s * scale_log2 - m) -> bf16 pairs into this warp's first 32
-      // columns (S is already in registers), 8 partial row sums
+      // columns (S is already in registers); the scaling and the 8 partial row
+      // sums on packed FP32 pairs
       const float neg_m = -m;
-      float rs[8];
+      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(neg_m, neg_m);
+      uint64_t rs2[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+      for (int i = 0; i < 4; ++i) rs2[i] = 0ull;
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 64; i += 2) {
-        const float e0 = ex2(fmaf(__uint_as_float(sr[i]), p.scale_log2, neg_m));
-        const float e1 = ex2(fmaf(__uint_as_float(sr[i + 1]), p.scale_log2, neg_m));
-        rs[i & 7] += e0;
-        rs[(i & 7) + 1] += e1;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sc2, nm2),
+                  x0, x1);
+        const float e0 = ex2(x0), e1 = ex2(x1);
+        rs2[(i >> 1) & 3] = f2_add(rs2[(i >> 1) & 3], f2_pack(e0, e1));
         pk[i >> 1] = pack_bf16(e0, e1);
       }
+      float rs[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) f2_unpack(rs2[i], rs[2 * i], rs[2 * i + 1]);
       tmem_st32(t_s, pk);
       if (any_need) {
         // O must be stable: wait for the O update of tile j-1 (the one of tile j
@@ -423,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t* sel, int n_sel,
                                  int hq, int chunk_len, int chunk_start, float scale, void* o,
-                                 float* lse, int* status, uint64_t wait_ns, cudaStream_t st) {
+                                 float* lse, float* own_reps, int* status, uint64_t wait_ns,
+                                 cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {128, static_cast<uint64_t>(hq), static_cast<uint64_t>(chunk_len)};
@@ -444,6 +497,7 @@ cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t*
   p.pt = kv.page_table;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
+  p.reps = own_reps;
   p.status = status;
   p.n_sel = n_sel;
   p.hq = hq;

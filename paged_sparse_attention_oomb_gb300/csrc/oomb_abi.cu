@@ -280,10 +280,11 @@ oomb_status oomb_select_topk_noalloc(const void* q, int32_t num_q_heads, int32_t
   return e == cudaSuccess ? OOMB_OK : cuda_fail(e, "oomb_select_topk_noalloc");
 }
 
-oomb_status oomb_sparse_attn_fwd(const void* q, const oomb_paged_kv* kv, const int32_t* sel,
-                                 int32_t n_sel, int32_t num_q_heads, int32_t chunk_len,
-                                 int32_t chunk_start, float scale, void* o, float* lse, void* ws,
-                                 size_t ws_bytes, void* stream) {
+static oomb_status attn_fwd(const char* name, const void* q, const oomb_paged_kv* kv,
+                            const int32_t* sel, int32_t n_sel, int32_t num_q_heads,
+                            int32_t chunk_len, int32_t chunk_start, float scale, void* o,
+                            float* lse, float* own_reps, void* ws, size_t ws_bytes,
+                            void* stream) {
   oomb_status s = check_kv(kv);
   if (s != OOMB_OK) return s;
   s = check_chunk(kv, num_q_heads, chunk_len, chunk_start);
@@ -301,14 +302,37 @@ oomb_status oomb_sparse_attn_fwd(const void* q, const oomb_paged_kv* kv, const i
   const float sc = resolve_scale(scale, kv->head_dim);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (kv->dtype == OOMB_BF16)
+  if (kv->dtype == OOMB_BF16) {
     e = oomb::launch_attn_fwd_bf16(q, desc(kv), sel, n_sel, num_q_heads, chunk_len, chunk_start,
-                                   sc, o, lse, static_cast<int*>(ws), g_wait_ns, st);
-  else
+                                   sc, o, lse, own_reps, static_cast<int*>(ws), g_wait_ns, st);
+  } else {
     e = oomb::launch_attn_fwd_fp32(static_cast<const float*>(q), desc(kv), sel, n_sel,
                                    num_q_heads, chunk_len, chunk_start, sc,
                                    static_cast<float*>(o), lse, static_cast<int*>(ws), st);
-  return e == cudaSuccess ? OOMB_OK : cuda_fail(e, "oomb_sparse_attn_fwd launch");
+    if (e == cudaSuccess && own_reps != nullptr)
+      e = oomb::launch_page_reps(desc(kv), false, chunk_start / kv->page_size,
+                                 chunk_len / kv->page_size, own_reps, static_cast<int*>(ws), st);
+  }
+  return e == cudaSuccess ? OOMB_OK : cuda_fail(e, name);
+}
+
+oomb_status oomb_sparse_attn_fwd(const void* q, const oomb_paged_kv* kv, const int32_t* sel,
+                                 int32_t n_sel, int32_t num_q_heads, int32_t chunk_len,
+                                 int32_t chunk_start, float scale, void* o, float* lse, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  return attn_fwd("oomb_sparse_attn_fwd", q, kv, sel, n_sel, num_q_heads, chunk_len, chunk_start,
+                  scale, o, lse, nullptr, ws, ws_bytes, stream);
+}
+
+oomb_status oomb_sparse_attn_fwd_own_reps(const void* q, const oomb_paged_kv* kv,
+                                          const int32_t* sel, int32_t n_sel,
+                                          int32_t num_q_heads, int32_t chunk_len,
+                                          int32_t chunk_start, float scale, void* o, float* lse,
+                                          float* reps, void* ws, size_t ws_bytes, void* stream) {
+  if (!reps) return fail(OOMB_ERR_INVALID_ARG, "reps must be set");
+  if (!aligned(reps, 16)) return fail(OOMB_ERR_INVALID_ARG, "reps must be 16-byte aligned");
+  return attn_fwd("oomb_sparse_attn_fwd_own_reps", q, kv, sel, n_sel, num_q_heads, chunk_len,
+                  chunk_start, scale, o, lse, reps, ws, ws_bytes, stream);
 }
 
 oomb_status oomb_sparse_attn_bwd(const void* q, const void* o, const void* dout, const float* lse,

@@ -71,9 +71,12 @@ cudaError_t launch_attn_bwd_fp32(const float* q, const float* o, const float* do
                                  float* dq, void* ws, cudaStream_t st);
 
 // --- k_attn_fwd_bf16.cu
+// own_reps: if not null, the representatives of the chunk's own pages are
+// also written there (rows of the logical pages, [num_pages][hkv][128]).
 cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t* sel, int n_sel,
                                  int hq, int chunk_len, int chunk_start, float scale, void* o,
-                                 float* lse, int* status, uint64_t wait_ns, cudaStream_t st);
+                                 float* lse, float* own_reps, int* status, uint64_t wait_ns,
+                                 cudaStream_t st);
 
 // --- k_attn_bwd_bf16.cu
 size_t bf16_bwd_ws_bytes(int hq, int chunk_len, int head_dim);

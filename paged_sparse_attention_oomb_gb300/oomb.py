@@ -26,7 +26,7 @@ OOMB_OP_ATTN_FWD, OOMB_OP_ATTN_BWD = 3, 4
 EXPORTED = [
     "oomb_workspace_bytes", "oomb_validate_page_table_host", "oomb_validate_page_table",
     "oomb_page_reps", "oomb_select_topk", "oomb_select_topk_noalloc", "oomb_sparse_attn_fwd",
-    "oomb_sparse_attn_bwd",
+    "oomb_sparse_attn_fwd_own_reps", "oomb_sparse_attn_bwd",
     "oomb_device_status", "oomb_set_wait_limit_ns", "oomb_debug_wait_unset_flag",
     "oomb_status_string", "oomb_last_error",
 ]
@@ -72,6 +72,8 @@ def load():
         "oomb_select_topk_noalloc": (ctypes.c_int, [vp, i32, i32, i32, vp, kvp, i32, vp, vp, vp]),
         "oomb_sparse_attn_fwd": (ctypes.c_int, [vp, kvp, vp, i32, i32, i32, i32, ctypes.c_float,
                                                 vp, vp, vp, sz, vp]),
+        "oomb_sparse_attn_fwd_own_reps": (ctypes.c_int, [vp, kvp, vp, i32, i32, i32, i32,
+                                                         ctypes.c_float, vp, vp, vp, vp, sz, vp]),
         "oomb_sparse_attn_bwd": (ctypes.c_int, [vp, vp, vp, vp, kvp, vp, i32, i32, i32, i32,
                                                 ctypes.c_float, vp, vp, sz, vp]),
         "oomb_device_status": (ctypes.c_int, [vp, vp, vp]),
@@ -182,6 +184,17 @@ def oomb_sparse_attn_fwd(q, kv: PagedKV, sel, n_sel, chunk_start, o, lse, ws, sc
                                        ws.numel(), _stream(stream)))
 
 
+def oomb_sparse_attn_fwd_own_reps(q, kv: PagedKV, sel, n_sel, chunk_start, o, lse, reps, ws,
+                                  scale=0.0, stream=None):
+    """The forward plus the representatives of the chunk's own pages into ``reps``."""
+    s = kv.struct()
+    c, hq, _ = q.shape
+    _check(load().oomb_sparse_attn_fwd_own_reps(_ptr(q), ctypes.byref(s), _ptr(sel), n_sel, hq,
+                                                c, chunk_start, float(scale), _ptr(o), _ptr(lse),
+                                                _ptr(reps), _ptr(ws), ws.numel(),
+                                                _stream(stream)))
+
+
 def oomb_sparse_attn_bwd(q, o, dout, lse, kv: PagedKV, sel, n_sel, chunk_start, dq, ws,
                          scale=0.0, stream=None):
     s = kv.struct()
@@ -272,7 +285,6 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
         raise OombError(OOMB_ERR_INVALID_ARG, "sequence must be whole chunks of whole pages")
     dev = q_full.device
     reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
-    ws_r = workspace(OOMB_OP_PAGE_REPS, kv)
     ws_s = workspace(OOMB_OP_SELECT_TOPK, kv, hq, chunk_len, top_k)
     ws_f = workspace(OOMB_OP_ATTN_FWD, kv, hq, chunk_len)
     ws_b = workspace(OOMB_OP_ATTN_BWD, kv, hq, chunk_len)
@@ -288,9 +300,8 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
         if n_sel:
             oomb_select_topk(q, t0, reps, kv, n_sel, sel, ws_s, stream=stream)
         lse = torch.empty((hq, chunk_len), dtype=torch.float32, device=dev)
-        oomb_sparse_attn_fwd(q, kv, sel, n_sel, t0, o_full[t0:t0 + chunk_len], lse, ws_f, scale,
-                             stream)
-        oomb_page_reps(kv, t0 // p, chunk_len // p, reps, ws_r, stream)
+        oomb_sparse_attn_fwd_own_reps(q, kv, sel, n_sel, t0, o_full[t0:t0 + chunk_len], lse, reps,
+                                      ws_f, scale, stream)
         lses.append(lse)
         sels.append((sel, n_sel))
     for c in reversed(range(n_chunks)):
@@ -299,7 +310,7 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
         oomb_sparse_attn_bwd(q_full[t0:t0 + chunk_len], o_full[t0:t0 + chunk_len],
                              dout_full[t0:t0 + chunk_len], lses[c], kv, sel, n_sel, t0,
                              dq_full[t0:t0 + chunk_len], ws_b, scale, stream)
-    for w in (ws_r, ws_s, ws_f, ws_b):
+    for w in (ws_s, ws_f, ws_b):
         code, where, blk = oomb_device_status(w, stream)
         if code != OOMB_OK:
             raise OombError(code, f"device status (where {where}, block {blk})")

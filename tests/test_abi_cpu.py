@@ -100,6 +100,17 @@ def test_bad_call_rejected(lib, args, msg):
     assert msg in oomb.oomb_last_error()
 
 
+@pytest.mark.parametrize("reps,msg", [(0, "reps must be set"), (FAKE + 4, "16-byte")])
+def test_fwd_own_reps_checks_reps(lib, reps, msg):
+    kv = _kv()
+    rc = lib.oomb_sparse_attn_fwd_own_reps(ctypes.c_void_p(FAKE), ctypes.byref(kv),
+                                           ctypes.c_void_p(FAKE), 8, 28, 256, 3840, 0.0,
+                                           ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                                           ctypes.c_void_p(reps) if reps else None,
+                                           ctypes.c_void_p(FAKE), 1 << 30, None)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and msg in oomb.oomb_last_error()
+
+
 def test_bwd_requires_grad_buffers(lib):
     kv = _kv(dk=0)
     rc = lib.oomb_sparse_attn_bwd(*(ctypes.c_void_p(FAKE),) * 4, ctypes.byref(kv),

@@ -170,6 +170,46 @@ def test_chunk_recurrent_pass(top_k):
     compare(to_numpy64(kv.dv)[pt], dv_o, "bf16", "chunk-recurrent dV")
 
 
+OWN_REPS = [
+    W("bf16_p64_ragged_c576_k13", "bf16", 4, 2, 4096, 64, 576, 13),   # 9 own pages: last tile 1 page
+    W("bf16_p128_c384_k5", "bf16", 8, 1, 2048, 128, 384, 5),
+    W("bf16_p16_c208_k37", "bf16", 2, 2, 1024, 16, 208, 37),
+    W("bf16_first_chunk", "bf16", 4, 2, 2048, 64, 1024, 8, start=0),
+    W("fp32_ragged_c176_k7", "fp32", 4, 2, 512, 16, 176, 7),
+]
+
+
+@pytest.mark.parametrize("wl", OWN_REPS, ids=[w.name for w in OWN_REPS])
+def test_fwd_own_reps(wl):
+    """The forward with the chunk's own representatives fused in: O and LSE
+    bit-identical to the plain forward, the own pages' representatives
+    bit-identical to the representatives pass (and within fp32 of the
+    oracle), every other row untouched."""
+    x = make_inputs(wl, seed=4, device=DEV)
+    kv = gpu_kv(x)
+    reps = gpu_reps(kv)
+    sel_g, _ = gpu_select(x, kv, reps, wl.top_k)
+    n_sel = min(wl.top_k, wl.num_candidates)
+    st = sel_g[:, :max(n_sel, 1)].contiguous()
+    o_ref, lse_ref = gpu_fwd(x, kv, st, n_sel)
+    o = torch.empty_like(x.q)
+    lse = torch.empty_like(lse_ref)
+    fused = torch.full_like(reps, float("nan"))
+    ws = oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv, wl.num_q_heads, wl.chunk_len)
+    oomb.oomb_sparse_attn_fwd_own_reps(x.q, kv, st, n_sel, wl.start, o, lse, fused, ws)
+    code, where, blk = oomb.oomb_device_status(ws)
+    assert code == oomb.OOMB_OK, (code, where, blk)
+    assert torch.equal(o.view(torch.int16) if o.dtype == torch.bfloat16 else o,
+                       o_ref.view(torch.int16) if o_ref.dtype == torch.bfloat16 else o_ref)
+    assert torch.equal(lse, lse_ref)
+    p0 = wl.start // wl.page_size
+    p1 = (wl.start + wl.chunk_len) // wl.page_size
+    assert torch.equal(fused[p0:p1], reps[p0:p1])
+    assert torch.isnan(fused[:p0]).all() and torch.isnan(fused[p1:]).all()
+    reps64 = oracle.page_reps(to_numpy64(x.k_pool), to_numpy64(x.page_table))
+    compare(fused[p0:p1].cpu().numpy(), reps64[p0:p1], "fp32", f"{wl.name} own reps")
+
+
 def test_deterministic_selection_and_forward():
     wl = W("det", "bf16", 8, 2, 8192, 64, 512, 31)
     x = make_inputs(wl, seed=9, device=DEV)
