@@ -139,6 +139,67 @@ def chunk_pass_flops(wl):
     return 14.0 * wl.head_dim * wl.num_q_heads * pairs
 
 
+def measure_offload(wl, x, kv, reps, dev, n_chunks=2, passes=3):
+    """The last ``n_chunks`` chunks of the workload as a chunk-recurrent pass
+    (forward in order, backward in reverse), once with the pools resident in
+    HBM and once with the K, V, dK, dV pools in pinned host memory behind a
+    device page cache (oomb_offload_*), the next chunk's tiles brought in on a
+    second stream while the current chunk computes.  Both passes are timed
+    with CUDA events; the difference is the offload overhead."""
+    from paged_sparse_attention_oomb_gb300 import oomb
+    c, p, hkv = wl.chunk_len, wl.page_size, wl.num_kv_heads
+    start = wl.context - n_chunks * c
+    g = torch.Generator(device=dev)
+    g.manual_seed(2)
+    shape = (n_chunks * c, wl.num_q_heads, wl.head_dim)
+    q = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+    do = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+    t_host0 = time.time()
+    host = oomb.PagedKV(torch.empty(x.k_pool.shape, dtype=x.k_pool.dtype, pin_memory=True),
+                        torch.empty(x.k_pool.shape, dtype=x.k_pool.dtype, pin_memory=True),
+                        x.page_table.cpu(),
+                        torch.empty(x.k_pool.shape, dtype=x.k_pool.dtype, pin_memory=True),
+                        torch.empty(x.k_pool.shape, dtype=x.k_pool.dtype, pin_memory=True))
+    host.k.copy_(x.k_pool)
+    host.v.copy_(x.v_pool)
+    host.dk.zero_()
+    host.dv.zero_()
+    setup_s = time.time() - t_host0
+    per_chunk = wl.top_k * hkv + c // p
+    cache = oomb.OffloadCache(host, 2 * per_chunk + 64, dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(passes):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / passes
+
+    ms_res = timed(lambda: oomb.chunk_recurrent_pass(q, do, kv, c, wl.top_k, start=start,
+                                                     reps=reps))
+    before = cache.stats()
+    ms_off = timed(lambda: oomb.chunk_recurrent_pass_offloaded(q, do, cache, c, wl.top_k,
+                                                               start=start, reps=reps))
+    after = cache.stats()
+    n_pass = passes + 1
+    res = {"workload": f"{wl.name}, last {n_chunks} chunks", "chunks": n_chunks,
+           "cache_slots": cache.cache_slots,
+           "cache_bytes": 4 * cache.ck.numel() * cache.ck.element_size(),
+           "host_pool_bytes": 4 * host.k.numel() * host.k.element_size(),
+           "ms_per_pass_resident": ms_res, "ms_per_pass_offloaded": ms_off,
+           "overhead": ms_off / ms_res - 1.0,
+           "bytes_in_per_pass": (after["bytes_in"] - before["bytes_in"]) / n_pass,
+           "bytes_out_per_pass": (after["bytes_out"] - before["bytes_out"]) / n_pass,
+           "host_setup_s": setup_s,
+           "what": "fwd in order + bwd in reverse; next chunk's tiles fetched on a second stream"}
+    cache.close()
+    return res
+
+
 def measure_chunk_pass(dev, peak_t, passes=3):
     """The chunk-recurrent pass over the whole 32K-token sequence (8 chunks of
     4096, every past page selected): forward over the chunks in order, with the
@@ -281,6 +342,8 @@ def run_ours(args, rank, world, dev):
     pk, pk_src = peaks()
     chunk_pass = (measure_chunk_pass(dev, pk["bf16_tflops_sustained"])
                   if args.chunk_pass and wl.dtype == "bf16" else None)
+    offload = (measure_offload(wl, x, kv, reps, dev)
+               if args.offload and wl.dtype == "bf16" and wl.n_sel > 0 else None)
     pairs_total = pairs_per_head(wl) * hq
     bwd_flops = 10.0 * d * pairs_total
     fwd_flops = 4.0 * d * pairs_total
@@ -322,6 +385,7 @@ def run_ours(args, rank, world, dev):
         "frac_of_bf16_peak": flops / ms / 1e9 / peak_t,
         "kernels": kern,
         "chunk_pass": chunk_pass,
+        "offload": offload,
         "roofline": {"kernel": "oomb_sparse_attn_bwd (delta prep + sparse_attn_bwd_kernel + dq convert)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_t,
                      "peak_source": f"{pk_src} bf16_tflops_sustained", "unit": "TFLOP/s",
@@ -423,6 +487,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunk-pass", dest="chunk_pass", action="store_false",
                     help="skip the whole-sequence chunk-recurrent pass measurement")
+    ap.add_argument("--no-offload", dest="offload", action="store_false",
+                    help="skip the host-offload measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -32,7 +32,13 @@
  *       K/V pools and dK/dV pools  [num_slots][Hkv][P][D]   (one page of one
  *                                   KV head is a contiguous P x D tile)
  *       page_table                 int32 [num_pages], logical page -> slot,
- *                                   injective, every entry < num_slots
+ *                                   injective on the pages a call reads, each
+ *                                   of those entries in [0, num_slots); the
+ *                                   other entries are not read (a page cache
+ *                                   may hold fewer slots than pages and mark
+ *                                   absent pages -1).  An entry a kernel reads
+ *                                   out of range is recorded as
+ *                                   OOMB_ERR_DEVICE_BOUNDS, never followed.
  *       q, o, dout, dq             [chunk_len][Hq][D]
  *       lse                        float [Hq][chunk_len], natural log
  *       reps                       float [num_pages][Hkv][D], logical order
@@ -200,6 +206,74 @@ oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *dout,
                                  const oomb_paged_kv *kv, const int32_t *sel, int32_t n_sel,
                                  int32_t num_q_heads, int32_t chunk_len, int32_t chunk_start,
                                  float scale, void *dq, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Host-tier pools with a device page cache (the method's fourth optimisation,
+ * "Async CPU offloading": the KV cache and its gradients stay in host memory
+ * and only the pages a chunk attends are brought to the GPU, ahead of the
+ * kernels that read them).
+ *
+ * The K, V, dK and dV pools of every page live in pinned host memory
+ * ([num_host_slots][Hkv][P][D], caller-owned, allocated with cudaHostAlloc or
+ * registered; the GPU reads and writes them directly over the CPU-GPU link).
+ * A cache of cache_slots page slots ([cache_slots][Hkv][P][D] for each of
+ * K, V, dK, dV) lives in caller-owned device memory.  The unit moved is one
+ * (page, KV head) tile of P x D elements; a cache slot holds one logical page
+ * and only the tiles of the KV heads that use it.
+ *
+ * oomb_offload_acquire(sel_host, chunk_start, chunk_len, with_grads) makes
+ * resident every tile the chunk's kernels read: (sel[g][i], g) for every KV
+ * head g and i < n_sel, and all heads of the chunk's own pages.  Missing K/V
+ * tiles (and, with with_grads, dK/dV tiles) are copied host -> cache; a slot
+ * that must be reused first writes its modified dK/dV tiles back to the host
+ * pools.  Gradient tiles are write-back: acquire with with_grads marks them
+ * modified (the backward that follows adds into them in place) and they
+ * return to the host pools on reuse of their slot or on oomb_offload_flush.
+ * The host pools therefore end bit-identical to a run with every page in HBM.
+ * Then the call writes the device page table `page_table_dev` (int32
+ * [num_pages]: cache slot of every resident page, -1 elsewhere).  The chunk's
+ * kernels then take an oomb_paged_kv with the cache pools, num_slots =
+ * cache_slots and page_table = page_table_dev.
+ *
+ * Moves are kernels on `stream` (one CTA per tile, zero-copy host access);
+ * the call returns after enqueueing them.  Slots used by this acquire and by
+ * the one before it are never reused, so the acquire for chunk c+1 may run on
+ * another stream while the kernels of chunk c are in flight; kernels of older
+ * acquires must have completed (the caller orders the streams with events),
+ * and each in-flight chunk needs its own page_table_dev.  The call blocks the
+ * host only until the moves enqueued two calls earlier have completed (two
+ * pinned staging buffers).  Errors: OOMB_ERR_INVALID_ARG if a page index is
+ * out of range, a host slot is out of range, or the chunk's pages do not fit
+ * in the cache next to those of the previous acquire.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  void *k, *v, *dk, *dv;          /* host tier: pinned host pools; dk/dv may be NULL (forward only) */
+  const int32_t *host_page_table; /* HOST int32 [num_pages]: logical page -> host slot, injective */
+  int32_t num_pages, num_host_slots, page_size, num_kv_heads, head_dim;
+  oomb_dtype dtype;
+  void *cache_k, *cache_v, *cache_dk, *cache_dv;  /* device tier [cache_slots][Hkv][P][D] */
+  int32_t cache_slots;
+} oomb_offload_desc;
+
+typedef struct oomb_offload oomb_offload;   /* opaque; host memory of the library */
+
+/* Checks the description (the host pools must be pinned host memory and the
+ * cache pools device memory), copies the host page table and allocates the
+ * handle's host state and pinned staging buffers.  No device memory. */
+oomb_status oomb_offload_create(const oomb_offload_desc *desc, oomb_offload **out);
+oomb_status oomb_offload_acquire(oomb_offload *h, const int32_t *sel_host, int32_t n_sel,
+                                 int32_t chunk_start, int32_t chunk_len, int32_t with_grads,
+                                 int32_t *page_table_dev, void *stream);
+/* Writes every modified dK/dV tile back to the host pools (enqueued on
+ * `stream`, after the kernels that modified them).  drop != 0 also forgets
+ * every cached tile (for a caller that rewrites host K/V pages). */
+oomb_status oomb_offload_flush(oomb_offload *h, int32_t drop, void *stream);
+/* Counters since create: out[0] tiles copied host -> cache, out[1] tiles
+ * written back, out[2] bytes host -> cache, out[3] bytes cache -> host,
+ * out[4] acquires, out[5] slots reused. */
+oomb_status oomb_offload_stats(const oomb_offload *h, int64_t *out);
+/* Frees the handle (waits for its staging buffers' last moves). */
+void oomb_offload_destroy(oomb_offload *h);
 
 /* Reads and clears the device status word at the start of ws (synchronises
  * `stream`).  Returns OOMB_OK, OOMB_ERR_TIMEOUT or OOMB_ERR_DEVICE_BOUNDS;

@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "liboomb.so")
 
 SOURCES = ["oomb_abi.cu", "k_reps_select.cu", "k_attn_fp32.cu", "k_attn_fwd_bf16.cu",
-           "k_attn_bwd_bf16.cu"]
+           "k_attn_bwd_bf16.cu", "oomb_offload.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I" + INCLUDE, "-I" + CSRC]

@@ -25,6 +25,18 @@ oomb_status fail(oomb_status s, const char* fmt, ...) {
   return s;
 }
 
+}  // namespace
+
+oomb_status oomb::report(oomb_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+namespace {
+
 oomb_status cuda_fail(cudaError_t e, const char* what) {
   return fail(OOMB_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -37,10 +49,9 @@ oomb_status check_kv(const oomb_paged_kv* kv) {
     return fail(OOMB_ERR_INVALID_ARG, "kv->k, kv->v and kv->page_table must be set");
   if (kv->dtype != OOMB_BF16 && kv->dtype != OOMB_FP32)
     return fail(OOMB_ERR_INVALID_ARG, "kv->dtype %d is not OOMB_BF16 or OOMB_FP32", kv->dtype);
-  if (kv->num_pages <= 0 || kv->num_slots < kv->num_pages)
-    return fail(OOMB_ERR_INVALID_ARG,
-                "need num_pages > 0 and num_slots >= num_pages (got %d, %d)", kv->num_pages,
-                kv->num_slots);
+  if (kv->num_pages <= 0 || kv->num_slots <= 0)
+    return fail(OOMB_ERR_INVALID_ARG, "need num_pages > 0 and num_slots > 0 (got %d, %d)",
+                kv->num_pages, kv->num_slots);
   const int P = kv->page_size;
   if (P != 16 && P != 32 && P != 64 && P != 128)
     return fail(OOMB_ERR_UNSUPPORTED, "page_size %d not in {16, 32, 64, 128}", P);

@@ -6,7 +6,13 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "oomb.h"
+
 namespace oomb {
+
+// Records a host-side error message for oomb_last_error() and returns `s`
+// (defined in oomb_abi.cu).
+oomb_status report(oomb_status s, const char* fmt, ...);
 
 // Workspace: a 256-byte status block first.
 //   int[0] status code (0 = ok), int[1] where, int[2] block

@@ -1,0 +1,401 @@
+// Host-tier page pools with a device page cache: the C-ABI calls
+// oomb_offload_* declared in include/oomb.h.
+// Method: "Out of the Memory Barrier" technical summary, section 2, the
+// fourth optimisation ("Async CPU offloading"): the KV cache and its
+// gradients need not all sit in GPU memory; pages move between host and GPU
+// asynchronously, ahead of the kernels that use them.
+//
+// Design (one GB300 with its Grace host): the pools of every page are pinned
+// host memory, which the GPU reads and writes directly over the CPU-GPU link.
+// A chunk's tiles -- (page, KV head) blocks of P x D elements -- are moved by
+// one kernel per direction, one CTA per tile, from a task list the host
+// writes into a pinned staging buffer; no per-tile copy call.  The host keeps
+// the cache directory: which logical page sits in which cache slot, which KV
+// heads of it are loaded (K/V, gradients), which gradient tiles are modified,
+// and when the slot was last used.  Slots used by the current and the
+// previous acquire are never reused, so the next chunk's tiles can be brought
+// in on another stream while the current chunk computes.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <utility>
+#include <vector>
+
+#include "oomb.h"
+#include "oomb_internal.h"
+
+namespace {
+
+struct TileCopy {
+  const uint4* src;
+  uint4* dst;
+};
+
+// One CTA per tile of n16 16-byte words: 8 loads in flight per thread, then
+// the 8 stores.  Either side may be pinned host memory (zero-copy) or device
+// memory.
+__global__ void __launch_bounds__(256) tile_copy_kernel(const TileCopy* __restrict__ tasks,
+                                                        int n16) {
+  const TileCopy t = tasks[blockIdx.x];
+  for (int base = threadIdx.x; base < n16; base += 256 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = base + i * 256;
+      if (k < n16) v[i] = t.src[k];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = base + i * 256;
+      if (k < n16) t.dst[k] = v[i];
+    }
+  }
+}
+
+// Pinned staging for one acquire or flush: its task list and page table
+// mirror, and the event recorded after the moves that read them.
+struct Staging {
+  TileCopy* tasks = nullptr;
+  TileCopy* tasks_dev = nullptr;
+  int32_t* pt = nullptr;
+  cudaEvent_t done = nullptr;
+  bool used = false;
+};
+
+bool is_host_pinned(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+bool is_device(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice;
+}
+
+}  // namespace
+
+struct oomb_offload {
+  oomb_offload_desc d;
+  size_t tile_bytes = 0;                 // P * D * element size
+  uint32_t all_heads = 0;
+  std::vector<int32_t> host_pt;          // logical page -> host slot
+  std::vector<int32_t> slot_of_page;     // logical page -> cache slot, -1: not resident
+  std::vector<int32_t> page_of_slot;     // cache slot -> logical page, -1: free
+  std::vector<uint32_t> kv_valid;        // per slot: KV heads whose K and V tiles are loaded
+  std::vector<uint32_t> g_valid;         // per slot: KV heads whose dK and dV tiles are loaded
+  std::vector<uint32_t> dirty;           // per slot: KV heads whose dK/dV tiles are modified
+  std::vector<uint64_t> last_use;        // per slot: acquire number of its last use
+  std::vector<uint32_t> need;            // per page: KV heads the current acquire needs
+  uint64_t epoch = 0;
+  size_t cap_tasks = 0;
+  Staging stage[2];
+  int next_stage = 0;
+  int64_t stats[6] = {0, 0, 0, 0, 0, 0};
+};
+
+namespace {
+
+char* tile_ptr(void* pool, const oomb_offload* h, int slot, int g) {
+  return static_cast<char*>(pool) +
+         (static_cast<size_t>(slot) * h->d.num_kv_heads + g) * h->tile_bytes;
+}
+
+oomb_status take_stage(oomb_offload* h, Staging** out) {
+  Staging& st = h->stage[h->next_stage];
+  h->next_stage ^= 1;
+  if (st.used) {
+    cudaError_t e = cudaEventSynchronize(st.done);
+    if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload staging wait: %s",
+                                              cudaGetErrorString(e));
+  }
+  *out = &st;
+  return OOMB_OK;
+}
+
+// Launch the copies tasks[first, first + n) of a staging buffer.
+cudaError_t launch_copies(const oomb_offload* h, const Staging& st, size_t first, size_t n,
+                          cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  tile_copy_kernel<<<static_cast<unsigned>(n), 256, 0, s>>>(
+      st.tasks_dev + first, static_cast<int>(h->tile_bytes / 16));
+  return cudaGetLastError();
+}
+
+void add_writeback(oomb_offload* h, Staging& st, size_t& n, int slot) {
+  const int page = h->page_of_slot[slot];
+  const int hs = h->host_pt[page];
+  for (int g = 0; g < h->d.num_kv_heads; ++g) {
+    if (!(h->dirty[slot] >> g & 1u)) continue;
+    st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(h->d.cache_dk, h, slot, g)),
+                     reinterpret_cast<uint4*>(tile_ptr(h->d.dk, h, hs, g))};
+    st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(h->d.cache_dv, h, slot, g)),
+                     reinterpret_cast<uint4*>(tile_ptr(h->d.dv, h, hs, g))};
+    h->stats[1] += 2;
+    h->stats[3] += 2 * static_cast<int64_t>(h->tile_bytes);
+  }
+  h->dirty[slot] = 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) {
+  if (!d || !out) return oomb::report(OOMB_ERR_INVALID_ARG, "desc and out must be set");
+  *out = nullptr;
+  if (d->dtype != OOMB_BF16 && d->dtype != OOMB_FP32)
+    return oomb::report(OOMB_ERR_INVALID_ARG, "dtype %d", static_cast<int>(d->dtype));
+  if (d->num_pages <= 0 || d->num_host_slots < d->num_pages || d->cache_slots <= 0)
+    return oomb::report(OOMB_ERR_INVALID_ARG,
+                        "need num_pages > 0, num_host_slots >= num_pages, cache_slots > 0");
+  if (d->num_kv_heads <= 0 || d->num_kv_heads > 32)
+    return oomb::report(OOMB_ERR_UNSUPPORTED, "num_kv_heads must be in [1, 32]");
+  if (d->page_size <= 0 || d->head_dim <= 0)
+    return oomb::report(OOMB_ERR_INVALID_ARG, "page_size and head_dim must be positive");
+  const size_t elem = d->dtype == OOMB_BF16 ? 2 : 4;
+  const size_t tile = static_cast<size_t>(d->page_size) * d->head_dim * elem;
+  if (tile % 16) return oomb::report(OOMB_ERR_UNSUPPORTED, "tile bytes must be a multiple of 16");
+  if (!d->k || !d->v || !d->cache_k || !d->cache_v || !d->host_page_table)
+    return oomb::report(OOMB_ERR_INVALID_ARG, "k, v, cache_k, cache_v, host_page_table must be set");
+  if ((d->dk == nullptr) != (d->cache_dk == nullptr) || (d->dv == nullptr) != (d->cache_dv == nullptr) ||
+      (d->dk == nullptr) != (d->dv == nullptr))
+    return oomb::report(OOMB_ERR_INVALID_ARG, "dk, dv, cache_dk, cache_dv: all set or all NULL");
+  const void* host_pools[4] = {d->k, d->v, d->dk, d->dv};
+  const void* dev_pools[4] = {d->cache_k, d->cache_v, d->cache_dk, d->cache_dv};
+  for (int i = 0; i < 4; ++i) {
+    if (host_pools[i] && (!is_host_pinned(host_pools[i]) ||
+                          reinterpret_cast<uintptr_t>(host_pools[i]) % 16))
+      return oomb::report(OOMB_ERR_INVALID_ARG,
+                          "host pool %d must be pinned host memory, 16-byte aligned", i);
+    if (dev_pools[i] && (!is_device(dev_pools[i]) ||
+                         reinterpret_cast<uintptr_t>(dev_pools[i]) % 16))
+      return oomb::report(OOMB_ERR_INVALID_ARG,
+                          "cache pool %d must be device memory, 16-byte aligned", i);
+  }
+  oomb_offload* h = new (std::nothrow) oomb_offload();
+  if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "out of host memory");
+  h->d = *d;
+  h->tile_bytes = tile;
+  h->all_heads = d->num_kv_heads == 32 ? 0xFFFFFFFFu : ((1u << d->num_kv_heads) - 1u);
+  h->host_pt.assign(d->host_page_table, d->host_page_table + d->num_pages);
+  {
+    std::vector<char> seen(d->num_host_slots, 0);
+    for (int l = 0; l < d->num_pages; ++l) {
+      const int s = h->host_pt[l];
+      if (s < 0 || s >= d->num_host_slots || seen[s]) {
+        delete h;
+        return oomb::report(OOMB_ERR_INVALID_ARG,
+                            "host page table: page %d -> slot %d is out of range or repeated", l, s);
+      }
+      seen[s] = 1;
+    }
+  }
+  h->slot_of_page.assign(d->num_pages, -1);
+  h->page_of_slot.assign(d->cache_slots, -1);
+  h->kv_valid.assign(d->cache_slots, 0);
+  h->g_valid.assign(d->cache_slots, 0);
+  h->dirty.assign(d->cache_slots, 0);
+  h->last_use.assign(d->cache_slots, 0);
+  h->need.assign(d->num_pages, 0);
+  // per slot and KV head: an acquire writes back at most 2 tiles (dK, dV) and
+  // fetches at most 4 (K, V, dK, dV); a flush writes back at most 2
+  h->cap_tasks = static_cast<size_t>(d->cache_slots) * d->num_kv_heads * 6 + 16;
+  for (auto& st : h->stage) {
+    cudaError_t e = cudaHostAlloc(&st.tasks, h->cap_tasks * sizeof(TileCopy), cudaHostAllocMapped);
+    if (e == cudaSuccess)
+      e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&st.tasks_dev), st.tasks, 0);
+    if (e == cudaSuccess)
+      e = cudaHostAlloc(&st.pt, static_cast<size_t>(d->num_pages) * sizeof(int32_t),
+                        cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      oomb_offload_destroy(h);
+      return oomb::report(OOMB_ERR_CUDA, "offload staging: %s", cudaGetErrorString(e));
+    }
+  }
+  *out = h;
+  return OOMB_OK;
+}
+
+oomb_status oomb_offload_acquire(oomb_offload* h, const int32_t* sel_host, int32_t n_sel,
+                                 int32_t chunk_start, int32_t chunk_len, int32_t with_grads,
+                                 int32_t* page_table_dev, void* stream) {
+  if (!h || !page_table_dev) return oomb::report(OOMB_ERR_INVALID_ARG, "handle and page_table_dev");
+  const oomb_offload_desc& d = h->d;
+  const int P = d.page_size, hkv = d.num_kv_heads;
+  if (chunk_start < 0 || chunk_len <= 0 || chunk_start % P || chunk_len % P ||
+      chunk_start + chunk_len > d.num_pages * P)
+    return oomb::report(OOMB_ERR_INVALID_ARG, "chunk [%d, %d) is not whole pages inside the cache",
+                        chunk_start, chunk_start + chunk_len);
+  if (n_sel < 0 || (n_sel > 0 && !sel_host))
+    return oomb::report(OOMB_ERR_INVALID_ARG, "n_sel %d / sel_host", n_sel);
+  if (with_grads && !d.dk)
+    return oomb::report(OOMB_ERR_INVALID_ARG, "with_grads needs the dK/dV pools");
+  // 1. the tiles this chunk reads: (sel[g][i], g) and every head of its own pages
+  std::vector<int32_t> pages;
+  pages.reserve(static_cast<size_t>(n_sel) * hkv + chunk_len / P);
+  auto want = [&](int l, uint32_t mask) {
+    if (h->need[l] == 0) pages.push_back(l);
+    h->need[l] |= mask;
+  };
+  const int own0 = chunk_start / P, own1 = (chunk_start + chunk_len) / P;
+  for (int g = 0; g < hkv; ++g)
+    for (int i = 0; i < n_sel; ++i) {
+      const int l = sel_host[static_cast<size_t>(g) * n_sel + i];
+      if (l < 0 || l >= own0) {
+        for (int x : pages) h->need[x] = 0;
+        return oomb::report(OOMB_ERR_INVALID_ARG, "sel[%d][%d] = %d is not a page before the chunk",
+                            g, i, l);
+      }
+      want(l, 1u << g);
+    }
+  for (int l = own0; l < own1; ++l) want(l, h->all_heads);
+  if (static_cast<int>(pages.size()) > d.cache_slots) {
+    for (int x : pages) h->need[x] = 0;
+    return oomb::report(OOMB_ERR_INVALID_ARG, "the chunk needs %zu cache slots, the cache has %d",
+                        pages.size(), d.cache_slots);
+  }
+  // 2. slots: resident pages keep theirs; the others take free slots, then the
+  //    least recently used slots not used by this acquire or the one before it
+  const uint64_t ep = ++h->epoch;
+  int missing = 0;
+  for (int l : pages) {
+    const int s = h->slot_of_page[l];
+    if (s >= 0) h->last_use[s] = ep;
+    else ++missing;
+  }
+  std::vector<std::pair<uint64_t, int>> cand;
+  if (missing > 0) {
+    for (int s = 0; s < d.cache_slots; ++s)
+      if (h->page_of_slot[s] < 0) cand.push_back({0, s});
+      else if (h->last_use[s] + 1 < ep) cand.push_back({h->last_use[s], s});
+    if (static_cast<int>(cand.size()) < missing) {
+      for (int x : pages) h->need[x] = 0;
+      return oomb::report(OOMB_ERR_INVALID_ARG,
+                          "cache of %d slots: %d pages to bring in, %zu slots free or reusable "
+                          "(slots of this chunk and the previous one are kept)",
+                          d.cache_slots, missing, cand.size());
+    }
+    std::partial_sort(cand.begin(), cand.begin() + missing, cand.end());
+  }
+  Staging* st = nullptr;
+  oomb_status rs = take_stage(h, &st);
+  if (rs != OOMB_OK) {
+    for (int x : pages) h->need[x] = 0;
+    return rs;
+  }
+  size_t n = 0;
+  int c = 0;
+  for (int l : pages) {
+    if (h->slot_of_page[l] >= 0) continue;
+    const int s = cand[c++].second;
+    const int old = h->page_of_slot[s];
+    if (old >= 0) {                              // reuse: modified gradients go home first
+      add_writeback(h, *st, n, s);
+      h->slot_of_page[old] = -1;
+      ++h->stats[5];
+    }
+    h->page_of_slot[s] = l;
+    h->slot_of_page[l] = s;
+    h->kv_valid[s] = h->g_valid[s] = h->dirty[s] = 0;
+    h->last_use[s] = ep;
+  }
+  const size_t n_wb = n;
+  // 3. fetch the missing tiles
+  for (int l : pages) {
+    const int s = h->slot_of_page[l];
+    const int hs = h->host_pt[l];
+    const uint32_t m = h->need[l];
+    h->need[l] = 0;
+    const uint32_t kv_miss = m & ~h->kv_valid[s];
+    const uint32_t g_miss = with_grads ? (m & ~h->g_valid[s]) : 0u;
+    for (int g = 0; g < hkv; ++g) {
+      if (kv_miss >> g & 1u) {
+        st->tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.k, h, hs, g)),
+                          reinterpret_cast<uint4*>(tile_ptr(d.cache_k, h, s, g))};
+        st->tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.v, h, hs, g)),
+                          reinterpret_cast<uint4*>(tile_ptr(d.cache_v, h, s, g))};
+      }
+      if (g_miss >> g & 1u) {
+        st->tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.dk, h, hs, g)),
+                          reinterpret_cast<uint4*>(tile_ptr(d.cache_dk, h, s, g))};
+        st->tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.dv, h, hs, g)),
+                          reinterpret_cast<uint4*>(tile_ptr(d.cache_dv, h, s, g))};
+      }
+    }
+    h->kv_valid[s] |= m;
+    if (with_grads) {
+      h->g_valid[s] |= m;
+      h->dirty[s] |= m;                          // the backward adds into them in place
+    }
+  }
+  const int64_t n_fetch = static_cast<int64_t>(n - n_wb);
+  h->stats[0] += n_fetch;
+  h->stats[2] += n_fetch * static_cast<int64_t>(h->tile_bytes);
+  ++h->stats[4];
+  // 4. page table of this chunk: cache slot of every resident page
+  std::memcpy(st->pt, h->slot_of_page.data(), static_cast<size_t>(d.num_pages) * sizeof(int32_t));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_copies(h, *st, 0, n_wb, s);       // write-backs before the fetches
+  if (e == cudaSuccess) e = launch_copies(h, *st, n_wb, n - n_wb, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(page_table_dev, st->pt, static_cast<size_t>(d.num_pages) * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaEventRecord(st->done, s);
+  st->used = true;
+  if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload acquire: %s", cudaGetErrorString(e));
+  return OOMB_OK;
+}
+
+oomb_status oomb_offload_flush(oomb_offload* h, int32_t drop, void* stream) {
+  if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "handle");
+  Staging* st = nullptr;
+  oomb_status rs = take_stage(h, &st);
+  if (rs != OOMB_OK) return rs;
+  size_t n = 0;
+  for (int s = 0; s < h->d.cache_slots; ++s)
+    if (h->page_of_slot[s] >= 0 && h->dirty[s]) add_writeback(h, *st, n, s);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_copies(h, *st, 0, n, s);
+  if (e == cudaSuccess) e = cudaEventRecord(st->done, s);
+  st->used = true;
+  if (drop) {
+    for (int sl = 0; sl < h->d.cache_slots; ++sl) {
+      if (h->page_of_slot[sl] >= 0) h->slot_of_page[h->page_of_slot[sl]] = -1;
+      h->page_of_slot[sl] = -1;
+      h->kv_valid[sl] = h->g_valid[sl] = h->dirty[sl] = 0;
+      h->last_use[sl] = 0;
+    }
+  }
+  if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload flush: %s", cudaGetErrorString(e));
+  return OOMB_OK;
+}
+
+oomb_status oomb_offload_stats(const oomb_offload* h, int64_t* out) {
+  if (!h || !out) return oomb::report(OOMB_ERR_INVALID_ARG, "handle and out");
+  for (int i = 0; i < 6; ++i) out[i] = h->stats[i];
+  return OOMB_OK;
+}
+
+void oomb_offload_destroy(oomb_offload* h) {
+  if (!h) return;
+  for (auto& st : h->stage) {
+    if (st.used && st.done) cudaEventSynchronize(st.done);
+    if (st.done) cudaEventDestroy(st.done);
+    if (st.tasks) cudaFreeHost(st.tasks);
+    if (st.pt) cudaFreeHost(st.pt);
+  }
+  delete h;
+}
+
+}  // extern "C"

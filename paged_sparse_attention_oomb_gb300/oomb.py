@@ -27,6 +27,8 @@ EXPORTED = [
     "oomb_workspace_bytes", "oomb_validate_page_table_host", "oomb_validate_page_table",
     "oomb_page_reps", "oomb_select_topk", "oomb_select_topk_noalloc", "oomb_sparse_attn_fwd",
     "oomb_sparse_attn_fwd_own_reps", "oomb_sparse_attn_bwd",
+    "oomb_offload_create", "oomb_offload_acquire", "oomb_offload_flush", "oomb_offload_stats",
+    "oomb_offload_destroy",
     "oomb_device_status", "oomb_set_wait_limit_ns", "oomb_debug_wait_unset_flag",
     "oomb_status_string", "oomb_last_error",
 ]
@@ -40,6 +42,17 @@ class OombError(RuntimeError):
 
 _STATUS_NAMES = {0: "OOMB_OK", 1: "OOMB_ERR_INVALID_ARG", 2: "OOMB_ERR_UNSUPPORTED",
                  3: "OOMB_ERR_CUDA", 4: "OOMB_ERR_TIMEOUT", 5: "OOMB_ERR_DEVICE_BOUNDS"}
+
+
+class OombOffloadDesc(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+                ("dv", ctypes.c_void_p), ("host_page_table", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_host_slots", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("cache_k", ctypes.c_void_p), ("cache_v", ctypes.c_void_p),
+                ("cache_dk", ctypes.c_void_p), ("cache_dv", ctypes.c_void_p),
+                ("cache_slots", ctypes.c_int32)]
 
 
 class OombPagedKV(ctypes.Structure):
@@ -76,6 +89,12 @@ def load():
                                                          ctypes.c_float, vp, vp, vp, vp, sz, vp]),
         "oomb_sparse_attn_bwd": (ctypes.c_int, [vp, vp, vp, vp, kvp, vp, i32, i32, i32, i32,
                                                 ctypes.c_float, vp, vp, sz, vp]),
+        "oomb_offload_create": (ctypes.c_int, [ctypes.POINTER(OombOffloadDesc),
+                                                ctypes.POINTER(ctypes.c_void_p)]),
+        "oomb_offload_acquire": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp]),
+        "oomb_offload_flush": (ctypes.c_int, [vp, i32, vp]),
+        "oomb_offload_stats": (ctypes.c_int, [vp, vp]),
+        "oomb_offload_destroy": (None, [vp]),
         "oomb_device_status": (ctypes.c_int, [vp, vp, vp]),
         "oomb_set_wait_limit_ns": (None, [ctypes.c_uint64]),
         "oomb_debug_wait_unset_flag": (ctypes.c_int, [vp, sz, vp]),
@@ -263,28 +282,36 @@ def sparse_attention_step(q, dout, kv: PagedKV, chunk_start, top_k, reps=None, s
 
 
 def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale=0.0,
-                         stream=None):
-    """One chunk-recurrent pass over a whole sequence, through the C ABI only.
+                         stream=None, start=0, reps=None):
+    """One chunk-recurrent pass over a sequence, through the C ABI only.
 
     Chunk-Recurrent Training Framework item: the sequence is processed chunk by
     chunk.  Forward, chunks in order: chunk c selects its Top-K past pages from
     the representatives of the pages written so far, attends them plus its own
-    pages, and then the representatives of its own pages are computed (they
-    become candidates for the later chunks).  Backward, chunks in reverse: the
-    same selections are reused and every chunk adds its dK/dV into the paged
-    gradient buffers of ``kv`` in place.  O and LSE of each chunk are kept for
-    its backward (the attention itself is recomputed inside the backward).
+    pages, and the same forward call writes the representatives of its own
+    pages (they become candidates for the later chunks).  Backward, chunks in
+    reverse: the same selections are reused and every chunk adds its dK/dV into
+    the paged gradient buffers of ``kv`` in place.  O and LSE of each chunk are
+    kept for its backward (the attention itself is recomputed inside the
+    backward).
 
-    q_full, dout_full: ``[T, Hq, D]`` with T = num_pages * P.  Returns
+    q_full, dout_full: ``[T, Hq, D]``, the tokens at positions [start, start + T)
+    (T a multiple of chunk_len, start a multiple of P).  reps: float
+    ``[num_pages, Hkv, D]`` holding the representatives of the pages before
+    ``start`` (computed here from the pool if None).  Returns
     ``(o_full, dq_full, sels)``; sels[c] is ``[Hkv, n_sel_c]``.
     """
     t, hq, d = q_full.shape
     ns, hkv, p, _ = kv.k.shape
     n_pages = kv.page_table.numel()
-    if t != n_pages * p or t % chunk_len or chunk_len % p:
+    if t % chunk_len or chunk_len % p or start % p or start + t > n_pages * p:
         raise OombError(OOMB_ERR_INVALID_ARG, "sequence must be whole chunks of whole pages")
     dev = q_full.device
-    reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
+    if reps is None:
+        reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
+        if start:
+            ws_r = workspace(OOMB_OP_PAGE_REPS, kv)
+            oomb_page_reps(kv, 0, start // p, reps, ws_r, stream)
     ws_s = workspace(OOMB_OP_SELECT_TOPK, kv, hq, chunk_len, top_k)
     ws_f = workspace(OOMB_OP_ATTN_FWD, kv, hq, chunk_len)
     ws_b = workspace(OOMB_OP_ATTN_BWD, kv, hq, chunk_len)
@@ -293,25 +320,206 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
     lses, sels = [], []
     n_chunks = t // chunk_len
     for c in range(n_chunks):
-        t0 = c * chunk_len
-        q = q_full[t0:t0 + chunk_len]
+        r0 = c * chunk_len
+        t0 = start + r0
+        q = q_full[r0:r0 + chunk_len]
         n_sel = min(top_k, t0 // p)
         sel = torch.zeros((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
         if n_sel:
             oomb_select_topk(q, t0, reps, kv, n_sel, sel, ws_s, stream=stream)
         lse = torch.empty((hq, chunk_len), dtype=torch.float32, device=dev)
-        oomb_sparse_attn_fwd_own_reps(q, kv, sel, n_sel, t0, o_full[t0:t0 + chunk_len], lse, reps,
+        oomb_sparse_attn_fwd_own_reps(q, kv, sel, n_sel, t0, o_full[r0:r0 + chunk_len], lse, reps,
                                       ws_f, scale, stream)
         lses.append(lse)
         sels.append((sel, n_sel))
     for c in reversed(range(n_chunks)):
-        t0 = c * chunk_len
+        r0 = c * chunk_len
         sel, n_sel = sels[c]
-        oomb_sparse_attn_bwd(q_full[t0:t0 + chunk_len], o_full[t0:t0 + chunk_len],
-                             dout_full[t0:t0 + chunk_len], lses[c], kv, sel, n_sel, t0,
-                             dq_full[t0:t0 + chunk_len], ws_b, scale, stream)
+        oomb_sparse_attn_bwd(q_full[r0:r0 + chunk_len], o_full[r0:r0 + chunk_len],
+                             dout_full[r0:r0 + chunk_len], lses[c], kv, sel, n_sel, start + r0,
+                             dq_full[r0:r0 + chunk_len], ws_b, scale, stream)
     for w in (ws_s, ws_f, ws_b):
         code, where, blk = oomb_device_status(w, stream)
         if code != OOMB_OK:
             raise OombError(code, f"device status (where {where}, block {blk})")
     return o_full, dq_full, [s[:, :n] for s, n in sels]
+
+
+# ---------------------------------------------------------------------------
+# Host-tier pools with a device page cache (oomb_offload_* in oomb.h).
+# ---------------------------------------------------------------------------
+class OffloadCache:
+    """A device cache of ``cache_slots`` page slots in front of host pools.
+
+    host: a PagedKV whose k, v (and dk, dv) are pinned CPU tensors
+    ``[num_host_slots, Hkv, P, D]`` and whose page_table is a CPU int32 tensor
+    (logical page -> host slot).  The cache pools are allocated here on
+    ``device`` (torch); the library's handle holds only host state.
+    """
+
+    def __init__(self, host: PagedKV, cache_slots: int, device="cuda"):
+        ns, hkv, p, d = host.k.shape
+        self.host = host
+        self.num_pages = host.page_table.numel()
+        self.page_size, self.hkv, self.head_dim = p, hkv, d
+        self.cache_slots = cache_slots
+        shape = (cache_slots, hkv, p, d)
+        self.ck = torch.empty(shape, dtype=host.k.dtype, device=device)
+        self.cv = torch.empty(shape, dtype=host.k.dtype, device=device)
+        grads = host.dk is not None
+        self.cdk = torch.empty(shape, dtype=host.k.dtype, device=device) if grads else None
+        self.cdv = torch.empty(shape, dtype=host.k.dtype, device=device) if grads else None
+        self._pt_host = host.page_table.to(torch.int32).contiguous()
+        dt = OOMB_BF16 if host.k.dtype == torch.bfloat16 else OOMB_FP32
+        ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+        desc = OombOffloadDesc(ptr(host.k), ptr(host.v), ptr(host.dk), ptr(host.dv),
+                               self._pt_host.data_ptr(), self.num_pages, ns, p, hkv, d, dt,
+                               ptr(self.ck), ptr(self.cv), ptr(self.cdk), ptr(self.cdv),
+                               cache_slots)
+        h = ctypes.c_void_p()
+        _check(load().oomb_offload_create(ctypes.byref(desc), ctypes.byref(h)))
+        self._h = h
+
+    def device_kv(self, page_table_dev) -> PagedKV:
+        """The cache as a PagedKV for the chunk whose acquire wrote page_table_dev."""
+        return PagedKV(self.ck, self.cv, page_table_dev, self.cdk, self.cdv)
+
+    def acquire(self, sel_host, n_sel, chunk_start, chunk_len, with_grads, page_table_dev,
+                stream=None):
+        """sel_host: CPU int32 ``[Hkv, n_sel]`` (or None when n_sel == 0)."""
+        sp = None
+        if n_sel:
+            sel_host = sel_host[:, :n_sel].to(torch.int32).contiguous()
+            sp = ctypes.c_void_p(sel_host.data_ptr())
+        _check(load().oomb_offload_acquire(self._h, sp, n_sel, chunk_start, chunk_len,
+                                           1 if with_grads else 0, _ptr(page_table_dev),
+                                           _stream(stream)))
+
+    def flush(self, drop=False, stream=None):
+        _check(load().oomb_offload_flush(self._h, 1 if drop else 0, _stream(stream)))
+
+    def stats(self) -> dict:
+        out = (ctypes.c_int64 * 6)()
+        _check(load().oomb_offload_stats(self._h, out))
+        keys = ["tiles_in", "tiles_out", "bytes_in", "bytes_out", "acquires", "slots_reused"]
+        return dict(zip(keys, list(out)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().oomb_offload_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk_len, top_k,
+                                   scale=0.0, start=0, reps=None, prefetch=True):
+    """chunk_recurrent_pass with the pools in host memory behind ``cache``.
+
+    Fourth optimisation of the method (asynchronous CPU offloading): each
+    chunk's tiles are brought into the device cache by oomb_offload_acquire;
+    with ``prefetch`` the acquire of the next chunk (and, in the forward, the
+    representatives of the current chunk's pages and the next chunk's
+    selection) runs on a second stream while the current chunk computes.
+    O, the selections and the host dK/dV are bit-identical to
+    chunk_recurrent_pass on resident pools (the same kernels run on bit copies
+    of the same tiles, and every modified gradient tile is written back by the
+    final flush); dQ is equal up to the order of its fp32 atomic sums.
+
+    reps: float ``[num_pages, Hkv, D]`` on the device with the representatives
+    of the pages before ``start`` (required when start > 0: those pages are in
+    host memory).  Returns ``(o_full, dq_full, sels)`` like chunk_recurrent_pass.
+    """
+    t, hq, d = q_full.shape
+    p, hkv, n_pages = cache.page_size, cache.hkv, cache.num_pages
+    if t % chunk_len or chunk_len % p or start % p or start + t > n_pages * p:
+        raise OombError(OOMB_ERR_INVALID_ARG, "sequence must be whole chunks of whole pages")
+    if start and reps is None:
+        raise OombError(OOMB_ERR_INVALID_ARG, "reps of the pages before start are required")
+    dev = q_full.device
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev) if prefetch else comp
+    pts = [torch.full((n_pages,), -1, dtype=torch.int32, device=dev) for _ in range(2)]
+    if reps is None:
+        reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
+    kv0 = cache.device_kv(pts[0])
+    ws_r = workspace(OOMB_OP_PAGE_REPS, kv0)
+    ws_s = workspace(OOMB_OP_SELECT_TOPK, kv0, hq, chunk_len, top_k)
+    ws_f = workspace(OOMB_OP_ATTN_FWD, kv0, hq, chunk_len)
+    ws_b = workspace(OOMB_OP_ATTN_BWD, kv0, hq, chunk_len)
+    o_full = torch.empty_like(q_full)
+    dq_full = torch.empty_like(q_full)
+    n_chunks = t // chunk_len
+    sels, lses = [None] * n_chunks, [None] * n_chunks
+    ready, done = [None] * n_chunks, [None] * n_chunks
+
+    def select(c):
+        # on the current stream; needs the representatives of pages < t0 / P
+        t0 = start + c * chunk_len
+        n_sel = min(top_k, t0 // p)
+        sel = torch.zeros((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
+        if n_sel:
+            oomb_select_topk(q_full[c * chunk_len:(c + 1) * chunk_len], t0, reps, kv0, n_sel, sel,
+                             ws_s, stream=torch.cuda.current_stream(dev))
+        return sel, sel.cpu(), n_sel            # the copy synchronises the current stream
+
+    def acquire(c, grads):
+        t0 = start + c * chunk_len
+        sel, sel_h, n_sel = sels[c]
+        cache.acquire(sel_h, n_sel, t0, chunk_len, grads, pts[c % 2],
+                      torch.cuda.current_stream(dev))
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.current_stream(dev))
+        ready[c] = ev
+
+    # forward, chunks in order
+    with torch.cuda.stream(copy):
+        sels[0] = select(0)
+        acquire(0, False)
+    for c in range(n_chunks):
+        r0 = c * chunk_len
+        comp.wait_event(ready[c])
+        sel, _, n_sel = sels[c]
+        lses[c] = torch.empty((hq, chunk_len), dtype=torch.float32, device=dev)
+        oomb_sparse_attn_fwd(q_full[r0:r0 + chunk_len], cache.device_kv(pts[c % 2]), sel, n_sel,
+                             start + r0, o_full[r0:r0 + chunk_len], lses[c], ws_f, scale, comp)
+        done[c] = torch.cuda.Event()
+        done[c].record(comp)
+        if c + 1 < n_chunks:
+            with torch.cuda.stream(copy):
+                # this chunk's pages are resident: their representatives, then the
+                # next chunk's selection and tiles
+                oomb_page_reps(cache.device_kv(pts[c % 2]), (start + r0) // p, chunk_len // p,
+                               reps, ws_r, copy)
+                sels[c + 1] = select(c + 1)
+                if c >= 1:
+                    copy.wait_event(done[c - 1])  # slots of chunk c-1 may be reused now
+                acquire(c + 1, False)
+    # backward, chunks in reverse
+    with torch.cuda.stream(copy):
+        copy.wait_event(done[n_chunks - 1])
+        acquire(n_chunks - 1, True)
+    for c in reversed(range(n_chunks)):
+        r0 = c * chunk_len
+        comp.wait_event(ready[c])
+        sel, _, n_sel = sels[c]
+        oomb_sparse_attn_bwd(q_full[r0:r0 + chunk_len], o_full[r0:r0 + chunk_len],
+                             dout_full[r0:r0 + chunk_len], lses[c], cache.device_kv(pts[c % 2]),
+                             sel, n_sel, start + r0, dq_full[r0:r0 + chunk_len], ws_b, scale, comp)
+        done[c] = torch.cuda.Event()
+        done[c].record(comp)
+        if c >= 1:
+            with torch.cuda.stream(copy):
+                if c + 1 < n_chunks:
+                    copy.wait_event(done[c + 1])  # slots of chunk c+1 may be reused now
+                acquire(c - 1, True)
+    cache.flush(stream=comp)
+    for w in (ws_r, ws_f, ws_b):
+        code, where, blk = oomb_device_status(w, comp)
+        if code != OOMB_OK:
+            raise OombError(code, f"device status (where {where}, block {blk})")
+    return o_full, dq_full, [s[0][:, :s[2]] for s in sels]

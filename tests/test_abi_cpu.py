@@ -72,7 +72,7 @@ def _fwd(lib, kv, q=FAKE, n_sel=0, hq=28, clen=256, cstart=3840, ws=FAKE, ws_byt
     (dict(page_size=48), 2, "page_size"),
     (dict(head_dim=64), 2, "head_dim"),
     (dict(dtype=7), 1, "dtype"),
-    (dict(num_slots=10), 1, "num_slots"),
+    (dict(num_slots=0), 1, "num_slots"),
     (dict(num_kv_heads=0), 2, "num_kv_heads"),
     (dict(k=FAKE + 8), 1, "aligned"),
     (dict(page_table=0), 1, "page_table"),
@@ -109,6 +109,25 @@ def test_fwd_own_reps_checks_reps(lib, reps, msg):
                                            ctypes.c_void_p(reps) if reps else None,
                                            ctypes.c_void_p(FAKE), 1 << 30, None)
     assert rc == oomb.OOMB_ERR_INVALID_ARG and msg in oomb.oomb_last_error()
+
+
+def test_offload_create_checks_memory_kinds(lib):
+    """The host pools must be pinned host memory and the cache pools device
+    memory; a plain host buffer is refused before anything is allocated."""
+    buf = (ctypes.c_uint8 * (1 << 16))()
+    pt = (ctypes.c_int32 * 4)(0, 1, 2, 3)
+    a = ctypes.addressof(buf)
+    d = oomb.OombOffloadDesc(a, a, None, None, ctypes.addressof(pt), 4, 4, 16, 1, 128,
+                             oomb.OOMB_BF16, a, a, None, None, 2)
+    h = ctypes.c_void_p()
+    rc = lib.oomb_offload_create(ctypes.byref(d), ctypes.byref(h))
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "pinned host memory" in oomb.oomb_last_error()
+    assert not h.value
+    d.cache_slots = 0
+    assert lib.oomb_offload_create(ctypes.byref(d), ctypes.byref(h)) == oomb.OOMB_ERR_INVALID_ARG
+    d.cache_slots, d.dk = 2, a                     # dk without dv / cache grads
+    rc = lib.oomb_offload_create(ctypes.byref(d), ctypes.byref(h))
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "all set or all NULL" in oomb.oomb_last_error()
 
 
 def test_bwd_requires_grad_buffers(lib):

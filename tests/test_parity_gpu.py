@@ -210,6 +210,69 @@ def test_fwd_own_reps(wl):
     compare(fused[p0:p1].cpu().numpy(), reps64[p0:p1], "fp32", f"{wl.name} own reps")
 
 
+def _offload_case(seed):
+    wl = W("offl", "bf16", 4, 2, 4096, 64, 512, 3)     # 64 pages; a chunk needs <= 3 * 2 + 8 pages
+    x = make_inputs(wl, seed=seed, device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed + 1)
+    q_full = torch.randn((4096, 4, 128), generator=g, device=DEV).to(torch.bfloat16)
+    do_full = torch.randn((4096, 4, 128), generator=g, device=DEV).to(torch.bfloat16)
+    dk0 = torch.randn(x.k_pool.shape, generator=g, device=DEV).to(torch.bfloat16)
+    dv0 = torch.randn(x.k_pool.shape, generator=g, device=DEV).to(torch.bfloat16)
+    return wl, x, q_full, do_full, dk0, dv0
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+
+@pytest.mark.parametrize("prefetch", [False, True])
+def test_offload_chunk_pass_matches_resident(prefetch):
+    """Pools in pinned host memory behind a device cache that must reuse slots
+    (28 slots for 64 pages): the chunk-recurrent pass gives bit-identical O,
+    selections and host dK/dV to the same pass on resident pools, starting
+    from nonzero gradients (in-place accumulation through the cache), and the
+    same dQ up to the order of its fp32 atomic sums."""
+    wl, x, q_full, do_full, dk0, dv0 = _offload_case(21)
+    kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, dk0.clone(), dv0.clone())
+    o_r, dq_r, sels_r = oomb.chunk_recurrent_pass(q_full, do_full, kv, 512, 3)
+    host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
+                        x.page_table.cpu(), dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
+    cache = oomb.OffloadCache(host, 28, DEV)
+    o_o, dq_o, sels_o = oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 512, 3,
+                                                            prefetch=prefetch)
+    torch.cuda.synchronize()
+    for a, b in zip(sels_r, sels_o):
+        assert torch.equal(a, b)
+    assert torch.equal(_bits(o_r), _bits(o_o))
+    # dQ sums the key tiles' contributions with fp32 atomics, in no fixed order:
+    # equal up to that rounding, not bit for bit
+    a, b = dq_r.float(), dq_o.float()
+    assert float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(a)) < 1e-3
+    assert float((a - b).abs().max()) <= 2 ** -7 * float(a.abs().max())
+    assert torch.equal(_bits(kv.dk.cpu()), _bits(host.dk))
+    assert torch.equal(_bits(kv.dv.cpu()), _bits(host.dv))
+    st = cache.stats()
+    assert st["slots_reused"] > 0 and st["tiles_out"] > 0, st
+    assert st["bytes_in"] == st["tiles_in"] * 64 * 128 * 2
+    cache.close()
+
+
+def test_offload_cache_too_small_is_refused():
+    wl, x, q_full, do_full, dk0, dv0 = _offload_case(22)
+    host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
+                        x.page_table.cpu(), dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
+    cache = oomb.OffloadCache(host, 10, DEV)           # the last chunk alone needs 14
+    pt = torch.full((wl.num_pages,), -1, dtype=torch.int32, device=DEV)
+    with pytest.raises(oomb.OombError) as e:
+        cache.acquire(None, 0, 0, 1024, False, pt)     # 16 own pages
+    assert e.value.code == oomb.OOMB_ERR_INVALID_ARG and "cache slots" in str(e.value)
+    cache.acquire(None, 0, 0, 512, False, pt)          # 8 own pages fit
+    torch.cuda.synchronize()
+    assert sorted(pt[:8].tolist()) == list(range(8)) and torch.all(pt[8:] == -1)
+    cache.close()
+
+
 def test_deterministic_selection_and_forward():
     wl = W("det", "bf16", 8, 2, 8192, 64, 512, 31)
     x = make_inputs(wl, seed=9, device=DEV)
