@@ -241,8 +241,8 @@ oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *dout,
  * another stream while the kernels of chunk c are in flight; kernels of older
  * acquires must have completed (the caller orders the streams with events),
  * and each in-flight chunk needs its own page_table_dev.  The call blocks the
- * host only until the moves enqueued two calls earlier have completed (two
- * pinned staging buffers).  Errors: OOMB_ERR_INVALID_ARG if a page index is
+ * host only until the moves enqueued four calls earlier (acquire, flush or
+ * writeback) have completed (four pinned staging buffers).  Errors: OOMB_ERR_INVALID_ARG if a page index is
  * out of range, a host slot is out of range, or the chunk's pages do not fit
  * in the cache next to those of the previous acquire.
  * ------------------------------------------------------------------------- */
@@ -268,6 +268,14 @@ oomb_status oomb_offload_acquire(oomb_offload *h, const int32_t *sel_host, int32
  * `stream`, after the kernels that modified them).  drop != 0 also forgets
  * every cached tile (for a caller that rewrites host K/V pages). */
 oomb_status oomb_offload_flush(oomb_offload *h, int32_t drop, void *stream);
+/* Writes the modified dK/dV tiles of pages [first_page, first_page + n_pages)
+ * back to the host pools now (enqueued on `stream`; the caller orders it after
+ * the kernels that modified them) and marks them clean.  For pages whose
+ * gradients are final before the pass ends -- in a backward over the chunks in
+ * reverse order, a chunk's own pages once its backward is done -- so that the
+ * final flush has less to move. */
+oomb_status oomb_offload_writeback(oomb_offload *h, int32_t first_page, int32_t n_pages,
+                                   void *stream);
 /* Counters since create: out[0] tiles copied host -> cache, out[1] tiles
  * written back, out[2] bytes host -> cache, out[3] bytes cache -> host,
  * out[4] acquires, out[5] slots reused. */

@@ -98,7 +98,7 @@ struct oomb_offload {
   std::vector<uint32_t> need;            // per page: KV heads the current acquire needs
   uint64_t epoch = 0;
   size_t cap_tasks = 0;
-  Staging stage[2];
+  Staging stage[4];
   int next_stage = 0;
   int64_t stats[6] = {0, 0, 0, 0, 0, 0};
 };
@@ -112,7 +112,7 @@ char* tile_ptr(void* pool, const oomb_offload* h, int slot, int g) {
 
 oomb_status take_stage(oomb_offload* h, Staging** out) {
   Staging& st = h->stage[h->next_stage];
-  h->next_stage ^= 1;
+  h->next_stage = (h->next_stage + 1) % 4;
   if (st.used) {
     cudaError_t e = cudaEventSynchronize(st.done);
     if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload staging wait: %s",
@@ -378,6 +378,28 @@ oomb_status oomb_offload_flush(oomb_offload* h, int32_t drop, void* stream) {
     }
   }
   if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload flush: %s", cudaGetErrorString(e));
+  return OOMB_OK;
+}
+
+oomb_status oomb_offload_writeback(oomb_offload* h, int32_t first_page, int32_t n_pages,
+                                   void* stream) {
+  if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "handle");
+  if (first_page < 0 || n_pages < 0 || first_page + n_pages > h->d.num_pages)
+    return oomb::report(OOMB_ERR_INVALID_ARG, "pages [%d, %d) outside [0, %d)", first_page,
+                        first_page + n_pages, h->d.num_pages);
+  Staging* st = nullptr;
+  oomb_status rs = take_stage(h, &st);
+  if (rs != OOMB_OK) return rs;
+  size_t n = 0;
+  for (int l = first_page; l < first_page + n_pages; ++l) {
+    const int s = h->slot_of_page[l];
+    if (s >= 0 && h->dirty[s]) add_writeback(h, *st, n, s);
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_copies(h, *st, 0, n, cs);
+  if (e == cudaSuccess) e = cudaEventRecord(st->done, cs);
+  st->used = true;
+  if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload writeback: %s", cudaGetErrorString(e));
   return OOMB_OK;
 }
 

@@ -27,8 +27,8 @@ EXPORTED = [
     "oomb_workspace_bytes", "oomb_validate_page_table_host", "oomb_validate_page_table",
     "oomb_page_reps", "oomb_select_topk", "oomb_select_topk_noalloc", "oomb_sparse_attn_fwd",
     "oomb_sparse_attn_fwd_own_reps", "oomb_sparse_attn_bwd",
-    "oomb_offload_create", "oomb_offload_acquire", "oomb_offload_flush", "oomb_offload_stats",
-    "oomb_offload_destroy",
+    "oomb_offload_create", "oomb_offload_acquire", "oomb_offload_flush", "oomb_offload_writeback",
+    "oomb_offload_stats", "oomb_offload_destroy",
     "oomb_device_status", "oomb_set_wait_limit_ns", "oomb_debug_wait_unset_flag",
     "oomb_status_string", "oomb_last_error",
 ]
@@ -93,6 +93,7 @@ def load():
                                                 ctypes.POINTER(ctypes.c_void_p)]),
         "oomb_offload_acquire": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp]),
         "oomb_offload_flush": (ctypes.c_int, [vp, i32, vp]),
+        "oomb_offload_writeback": (ctypes.c_int, [vp, i32, i32, vp]),
         "oomb_offload_stats": (ctypes.c_int, [vp, vp]),
         "oomb_offload_destroy": (None, [vp]),
         "oomb_device_status": (ctypes.c_int, [vp, vp, vp]),
@@ -398,6 +399,10 @@ class OffloadCache:
     def flush(self, drop=False, stream=None):
         _check(load().oomb_offload_flush(self._h, 1 if drop else 0, _stream(stream)))
 
+    def writeback(self, first_page, n_pages, stream=None):
+        """Write the modified gradient tiles of these pages back now."""
+        _check(load().oomb_offload_writeback(self._h, first_page, n_pages, _stream(stream)))
+
     def stats(self) -> dict:
         out = (ctypes.c_int64 * 6)()
         _check(load().oomb_offload_stats(self._h, out))
@@ -421,14 +426,18 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     """chunk_recurrent_pass with the pools in host memory behind ``cache``.
 
     Fourth optimisation of the method (asynchronous CPU offloading): each
-    chunk's tiles are brought into the device cache by oomb_offload_acquire;
-    with ``prefetch`` the acquire of the next chunk (and, in the forward, the
-    representatives of the current chunk's pages and the next chunk's
-    selection) runs on a second stream while the current chunk computes.
-    O, the selections and the host dK/dV are bit-identical to
+    chunk's tiles are brought into the device cache by oomb_offload_acquire.
+    With ``prefetch``, a second stream does the moves while the compute stream
+    runs the attention: in the forward, the representatives of chunk c's
+    pages, chunk c+1's selection and its acquire overlap chunk c's forward (and
+    the last chunk's gradient tiles come in during the forward of the chunk
+    before it); in the backward, chunk c-1's acquire overlaps chunk c's
+    backward, and chunk c's own pages -- final once its backward is done, since
+    no earlier chunk reads them -- go back to the host during the backward of
+    chunk c-1.  O, the selections and the host dK/dV are bit-identical to
     chunk_recurrent_pass on resident pools (the same kernels run on bit copies
-    of the same tiles, and every modified gradient tile is written back by the
-    final flush); dQ is equal up to the order of its fp32 atomic sums.
+    of the same tiles, and every modified gradient tile is written back); dQ is
+    equal up to the order of its fp32 atomic sums.
 
     reps: float ``[num_pages, Hkv, D]`` on the device with the representatives
     of the pages before ``start`` (required when start > 0: those pages are in
@@ -443,7 +452,10 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     dev = q_full.device
     comp = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev) if prefetch else comp
+    # device page tables: chunks c and c+1 in flight use pts[c % 2]; the last
+    # chunk's backward uses pt_last (written while its forward may still run)
     pts = [torch.full((n_pages,), -1, dtype=torch.int32, device=dev) for _ in range(2)]
+    pt_last = torch.full((n_pages,), -1, dtype=torch.int32, device=dev)
     if reps is None:
         reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
     kv0 = cache.device_kv(pts[0])
@@ -454,8 +466,18 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     o_full = torch.empty_like(q_full)
     dq_full = torch.empty_like(q_full)
     n_chunks = t // chunk_len
+    last = n_chunks - 1
     sels, lses = [None] * n_chunks, [None] * n_chunks
     ready, done = [None] * n_chunks, [None] * n_chunks
+    ready_last = [None]
+
+    def cur():
+        return torch.cuda.current_stream(dev)
+
+    def mark():
+        ev = torch.cuda.Event()
+        ev.record(cur())
+        return ev
 
     def select(c):
         # on the current stream; needs the representatives of pages < t0 / P
@@ -464,22 +486,26 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
         sel = torch.zeros((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
         if n_sel:
             oomb_select_topk(q_full[c * chunk_len:(c + 1) * chunk_len], t0, reps, kv0, n_sel, sel,
-                             ws_s, stream=torch.cuda.current_stream(dev))
+                             ws_s, stream=cur())
         return sel, sel.cpu(), n_sel            # the copy synchronises the current stream
 
-    def acquire(c, grads):
-        t0 = start + c * chunk_len
-        sel, sel_h, n_sel = sels[c]
-        cache.acquire(sel_h, n_sel, t0, chunk_len, grads, pts[c % 2],
-                      torch.cuda.current_stream(dev))
-        ev = torch.cuda.Event()
-        ev.record(torch.cuda.current_stream(dev))
-        ready[c] = ev
+    def acquire(c, grads, pt):
+        _, sel_h, n_sel = sels[c]
+        cache.acquire(sel_h, n_sel, start + c * chunk_len, chunk_len, grads, pt, cur())
+
+    def acquire_fwd(c):
+        acquire(c, False, pts[c % 2])
+        ready[c] = mark()
+        if c == last:
+            # the last chunk's gradient tiles: same pages, so no slot is reused
+            # while the forwards before it run
+            acquire(c, True, pt_last)
+            ready_last[0] = mark()
 
     # forward, chunks in order
     with torch.cuda.stream(copy):
         sels[0] = select(0)
-        acquire(0, False)
+        acquire_fwd(0)
     for c in range(n_chunks):
         r0 = c * chunk_len
         comp.wait_event(ready[c])
@@ -498,25 +524,30 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
                 sels[c + 1] = select(c + 1)
                 if c >= 1:
                     copy.wait_event(done[c - 1])  # slots of chunk c-1 may be reused now
-                acquire(c + 1, False)
+                acquire_fwd(c + 1)
+    fwd_done = done[last]
     # backward, chunks in reverse
-    with torch.cuda.stream(copy):
-        copy.wait_event(done[n_chunks - 1])
-        acquire(n_chunks - 1, True)
     for c in reversed(range(n_chunks)):
         r0 = c * chunk_len
-        comp.wait_event(ready[c])
+        comp.wait_event(ready_last[0] if c == last else ready[c])
         sel, _, n_sel = sels[c]
+        pt = pt_last if c == last else pts[c % 2]
         oomb_sparse_attn_bwd(q_full[r0:r0 + chunk_len], o_full[r0:r0 + chunk_len],
-                             dout_full[r0:r0 + chunk_len], lses[c], cache.device_kv(pts[c % 2]),
+                             dout_full[r0:r0 + chunk_len], lses[c], cache.device_kv(pt),
                              sel, n_sel, start + r0, dq_full[r0:r0 + chunk_len], ws_b, scale, comp)
         done[c] = torch.cuda.Event()
         done[c].record(comp)
-        if c >= 1:
-            with torch.cuda.stream(copy):
-                if c + 1 < n_chunks:
-                    copy.wait_event(done[c + 1])  # slots of chunk c+1 may be reused now
-                acquire(c - 1, True)
+        with torch.cuda.stream(copy):
+            if c >= 1:
+                # slots (and the page table) of the chunk before in comp order may be
+                # reused now: the last forward for c == last, else backward c + 1
+                copy.wait_event(fwd_done if c == last else done[c + 1])
+                acquire(c - 1, True, pts[(c - 1) % 2])
+                ready[c - 1] = mark()
+            # chunk c's own pages are final: no earlier chunk reads them
+            copy.wait_event(done[c])
+            cache.writeback((start + r0) // p, chunk_len // p, copy)
+    comp.wait_stream(copy)
     cache.flush(stream=comp)
     for w in (ws_r, ws_f, ws_b):
         code, where, blk = oomb_device_status(w, comp)
