@@ -258,6 +258,32 @@ def test_offload_chunk_pass_matches_resident(prefetch):
     cache.close()
 
 
+def test_offload_chunk_pass_fp32():
+    """The same through the fp32 path (head_dim 64, P = 16, fp32 pools): 8 chunks
+    of 128 rows, Top-8, 32 cache slots for 64 pages."""
+    wl = W("offl32", "fp32", 2, 1, 1024, 16, 128, 8)
+    x = make_inputs(wl, seed=23, device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(24)
+    q_full = torch.randn((1024, 2, 64), generator=g, device=DEV)
+    do_full = torch.randn((1024, 2, 64), generator=g, device=DEV)
+    dk0 = torch.randn(x.k_pool.shape, generator=g, device=DEV)
+    dv0 = torch.randn(x.k_pool.shape, generator=g, device=DEV)
+    kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, dk0.clone(), dv0.clone())
+    o_r, dq_r, sels_r = oomb.chunk_recurrent_pass(q_full, do_full, kv, 128, 8)
+    host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
+                        x.page_table.cpu(), dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
+    cache = oomb.OffloadCache(host, 32, DEV)
+    o_o, dq_o, sels_o = oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 128, 8)
+    torch.cuda.synchronize()
+    for a, b in zip(sels_r, sels_o):
+        assert torch.equal(a, b)
+    assert torch.equal(o_r, o_o) and torch.equal(dq_r, dq_o)
+    assert torch.equal(kv.dk.cpu(), host.dk) and torch.equal(kv.dv.cpu(), host.dv)
+    assert cache.stats()["slots_reused"] > 0
+    cache.close()
+
+
 def test_offload_cache_too_small_is_refused():
     wl, x, q_full, do_full, dk0, dv0 = _offload_case(22)
     host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
