@@ -451,7 +451,9 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
         raise OombError(OOMB_ERR_INVALID_ARG, "reps of the pages before start are required")
     dev = q_full.device
     comp = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev) if prefetch else comp
+    # the moves run at high priority: their CTAs are scheduled as soon as an SM
+    # frees up between attention CTAs, rather than after the whole attention grid
+    copy = torch.cuda.Stream(dev, priority=-1) if prefetch else comp
     # device page tables: chunks c and c+1 in flight use pts[c % 2]; the last
     # chunk's backward uses pt_last (written while its forward may still run)
     pts = [torch.full((n_pages,), -1, dtype=torch.int32, device=dev) for _ in range(2)]
