@@ -139,7 +139,7 @@ def chunk_pass_flops(wl):
     return 14.0 * wl.head_dim * wl.num_q_heads * pairs
 
 
-def measure_offload(wl, x, kv, reps, dev, n_chunks=2, passes=3):
+def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=3):
     """The last ``n_chunks`` chunks of the workload as a chunk-recurrent pass
     (forward in order, backward in reverse), once with the pools resident in
     HBM and once with the K, V, dK, dV pools in pinned host memory behind a

@@ -35,20 +35,22 @@ struct TileCopy {
 
 // One CTA per tile of n16 16-byte words: 8 loads in flight per thread, then
 // the 8 stores.  Either side may be pinned host memory (zero-copy) or device
-// memory.
-__global__ void __launch_bounds__(256) tile_copy_kernel(const TileCopy* __restrict__ tasks,
-                                                        int n16) {
+// memory.  128 threads: small enough (in threads and registers) to share an SM
+// with a forward-attention CTA.
+constexpr int kCopyThreads = 128;
+__global__ void __launch_bounds__(kCopyThreads) tile_copy_kernel(
+    const TileCopy* __restrict__ tasks, int n16) {
   const TileCopy t = tasks[blockIdx.x];
-  for (int base = threadIdx.x; base < n16; base += 256 * 8) {
+  for (int base = threadIdx.x; base < n16; base += kCopyThreads * 8) {
     uint4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int k = base + i * 256;
+      const int k = base + i * kCopyThreads;
       if (k < n16) v[i] = t.src[k];
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int k = base + i * 256;
+      const int k = base + i * kCopyThreads;
       if (k < n16) t.dst[k] = v[i];
     }
   }
@@ -126,7 +128,17 @@ oomb_status take_stage(oomb_offload* h, Staging** out) {
 cudaError_t launch_copies(const oomb_offload* h, const Staging& st, size_t first, size_t n,
                           cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  tile_copy_kernel<<<static_cast<unsigned>(n), 256, 0, s>>>(
+  // Same shared-memory carveout as the attention kernels, so that a copy CTA
+  // can share an SM with one of theirs instead of waiting for the SM to drain.
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaError_t e = cudaFuncSetAttribute(tile_copy_kernel,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    carveout_set = true;
+  }
+  tile_copy_kernel<<<static_cast<unsigned>(n), kCopyThreads, 0, s>>>(
       st.tasks_dev + first, static_cast<int>(h->tile_bytes / 16));
   return cudaGetLastError();
 }
