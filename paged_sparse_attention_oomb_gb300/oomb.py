@@ -282,6 +282,95 @@ def sparse_attention_step(q, dout, kv: PagedKV, chunk_start, top_k, reps=None, s
     return dict(reps=reps, sel=sel[:, :n_sel], o=o, lse=lse, dq=dq)
 
 
+class StepPipeline:
+    """Steps of the path on chunks whose inputs and outputs live in pinned host
+    memory, with the copies overlapped: step i+1's Q and dO go host -> device on
+    one copy stream while step i computes, and step i's O, LSE and dQ go device ->
+    host on another while step i+1 computes (the copy engines, not the SMs).
+    Device buffers are double-buffered.  Every step is representatives of all
+    pages -> Top-K selection -> forward -> backward (dK/dV in place), the same
+    four C ABI calls as sparse_attention_step; results are identical to running
+    the steps one after another (dQ up to the order of its fp32 atomic sums).
+
+    step(q_h, do_h, o_h, lse_h, dq_h) enqueues one step and returns at once; the
+    host buffers must stay untouched until finish() (or two steps later).
+    """
+
+    def __init__(self, kv: PagedKV, chunk_start, chunk_len, num_q_heads, top_k, scale=0.0):
+        ns, hkv, p, d = kv.k.shape
+        dev = kv.k.device
+        self.kv, self.chunk_start, self.top_k, self.scale = kv, chunk_start, top_k, scale
+        self.n_pages = kv.page_table.numel()
+        self.n_sel = min(top_k, chunk_start // p)
+        shape = (chunk_len, num_q_heads, d)
+        dt = kv.k.dtype
+        self.q = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
+        self.do = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
+        self.o = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
+        self.dq = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
+        self.lse = [torch.empty((num_q_heads, chunk_len), dtype=torch.float32, device=dev)
+                    for _ in range(2)]
+        self.reps = torch.empty((self.n_pages, hkv, d), dtype=torch.float32, device=dev)
+        self.sel = torch.empty((hkv, max(self.n_sel, 1)), dtype=torch.int32, device=dev)
+        self.ws_r = workspace(OOMB_OP_PAGE_REPS, kv)
+        self.ws_s = workspace(OOMB_OP_SELECT_TOPK, kv, num_q_heads, chunk_len, top_k)
+        self.ws_f = workspace(OOMB_OP_ATTN_FWD, kv, num_q_heads, chunk_len)
+        self.ws_b = workspace(OOMB_OP_ATTN_BWD, kv, num_q_heads, chunk_len)
+        self.comp = torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.comp_done = [None, None]     # compute of the step that last used buffer b
+        self.out_done = [None, None]      # copy-out of the step that last used buffer b
+        self.i = 0
+
+    def step(self, q_h, do_h, o_h, lse_h, dq_h):
+        b = self.i & 1
+        with torch.cuda.stream(self.h2d):
+            if self.comp_done[b] is not None:
+                self.h2d.wait_event(self.comp_done[b])   # step i-2 has read buffer b
+            self.q[b].copy_(q_h, non_blocking=True)
+            self.do[b].copy_(do_h, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(self.h2d)
+        self.comp.wait_event(ready)
+        if self.out_done[b] is not None:
+            self.comp.wait_event(self.out_done[b])       # step i-2's outputs are home
+        kv, st = self.kv, self.comp
+        oomb_page_reps(kv, 0, self.n_pages, self.reps, self.ws_r, st)
+        oomb_select_topk(self.q[b], self.chunk_start, self.reps, kv, self.top_k, self.sel,
+                         self.ws_s, stream=st)
+        oomb_sparse_attn_fwd(self.q[b], kv, self.sel, self.n_sel, self.chunk_start, self.o[b],
+                             self.lse[b], self.ws_f, self.scale, st)
+        oomb_sparse_attn_bwd(self.q[b], self.o[b], self.do[b], self.lse[b], kv, self.sel,
+                             self.n_sel, self.chunk_start, self.dq[b], self.ws_b, self.scale, st)
+        done = torch.cuda.Event()
+        done.record(self.comp)
+        self.comp_done[b] = done
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(done)
+            o_h.copy_(self.o[b], non_blocking=True)
+            lse_h.copy_(self.lse[b], non_blocking=True)
+            dq_h.copy_(self.dq[b], non_blocking=True)
+            out = torch.cuda.Event()
+            out.record(self.d2h)
+        self.out_done[b] = out
+        self.i += 1
+
+    def begin(self):
+        """Order the next copies after everything already on the compute stream."""
+        self.h2d.wait_stream(self.comp)
+        self.d2h.wait_stream(self.comp)
+
+    def finish(self):
+        """Make the compute stream wait for every copy; then check the status words."""
+        self.comp.wait_stream(self.d2h)
+        self.comp.wait_stream(self.h2d)
+        for w in (self.ws_r, self.ws_s, self.ws_f, self.ws_b):
+            code, where, blk = oomb_device_status(w, self.comp)
+            if code != OOMB_OK:
+                raise OombError(code, f"device status (where {where}, block {blk})")
+
+
 def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale=0.0,
                          stream=None, start=0, reps=None):
     """One chunk-recurrent pass over a sequence, through the C ABI only.

@@ -284,6 +284,41 @@ def test_offload_chunk_pass_fp32():
     cache.close()
 
 
+def test_step_pipeline_matches_sequential_steps():
+    """Three steps with host-resident inputs and outputs through StepPipeline
+    (copies overlapped with the neighbouring steps' compute) give the same O,
+    LSE and accumulated dK/dV as three sparse_attention_step calls one after
+    another, and the same dQ up to the order of its fp32 atomic sums."""
+    wl = W("pipe", "bf16", 4, 2, 4096, 64, 512, 5)
+    x = make_inputs(wl, seed=31, device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(32)
+    qs = [torch.randn(x.q.shape, generator=g, device=DEV).to(torch.bfloat16) for _ in range(3)]
+    dos = [torch.randn(x.q.shape, generator=g, device=DEV).to(torch.bfloat16) for _ in range(3)]
+    kv_a = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, torch.zeros_like(x.k_pool),
+                        torch.zeros_like(x.v_pool))
+    ref = [oomb.sparse_attention_step(q, do, kv_a, wl.start, wl.top_k) for q, do in zip(qs, dos)]
+    kv_b = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, torch.zeros_like(x.k_pool),
+                        torch.zeros_like(x.v_pool))
+    pipe = oomb.StepPipeline(kv_b, wl.start, wl.chunk_len, wl.num_q_heads, wl.top_k)
+    outs = []
+    for q, do in zip(qs, dos):
+        q_h, do_h = q.cpu().pin_memory(), do.cpu().pin_memory()
+        o_h = torch.empty_like(q_h).pin_memory()
+        dq_h = torch.empty_like(q_h).pin_memory()
+        lse_h = torch.empty((wl.num_q_heads, wl.chunk_len), dtype=torch.float32).pin_memory()
+        pipe.step(q_h, do_h, o_h, lse_h, dq_h)
+        outs.append((o_h, lse_h, dq_h, q_h, do_h))
+    pipe.finish()
+    torch.cuda.synchronize()
+    for r, (o_h, lse_h, dq_h, _, _) in zip(ref, outs):
+        assert torch.equal(_bits(r["o"].cpu()), _bits(o_h))
+        assert torch.equal(r["lse"].cpu(), lse_h)
+        a, b = r["dq"].float().cpu(), dq_h.float()
+        assert float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(a)) < 1e-3
+    assert torch.equal(_bits(kv_a.dk), _bits(kv_b.dk)) and torch.equal(_bits(kv_a.dv), _bits(kv_b.dv))
+
+
 def test_offload_cache_too_small_is_refused():
     wl, x, q_full, do_full, dk0, dv0 = _offload_case(22)
     host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
