@@ -235,7 +235,7 @@ oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *dout,
  * kernels then take an oomb_paged_kv with the cache pools, num_slots =
  * cache_slots and page_table = page_table_dev.
  *
- * Moves are kernels on `stream` (one CTA per tile, zero-copy host access);
+ * Moves are enqueued on `stream` (see dev_staging below for the two ways);
  * the call returns after enqueueing them.  Slots used by this acquire and by
  * the one before it are never reused, so the acquire for chunk c+1 may run on
  * another stream while the kernels of chunk c are in flight; kernels of older
@@ -253,6 +253,16 @@ typedef struct {
   oomb_dtype dtype;
   void *cache_k, *cache_v, *cache_dk, *cache_dv;  /* device tier [cache_slots][Hkv][P][D] */
   int32_t cache_slots;
+  /* Optional device staging buffer (caller-owned, 16-byte aligned).  If set,
+   * tiles move through it and a pinned host staging buffer of the same size
+   * that the library allocates: tiles are gathered on the host (a stream
+   * callback with a few threads) and cross the CPU-GPU link in one copy-engine
+   * transfer per round of dev_staging_bytes, leaving the SMs to the attention
+   * kernels; successive calls are ordered on the GPU (they share the staging
+   * buffers).  If NULL, a copy kernel reads and writes the host pools
+   * directly (zero-copy), which needs SMs. */
+  void *dev_staging;
+  int64_t dev_staging_bytes;
 } oomb_offload_desc;
 
 typedef struct oomb_offload oomb_offload;   /* opaque; host memory of the library */

@@ -18,8 +18,12 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <condition_variable>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <thread>
 #include <utility>
 #include <vector>
 
@@ -56,11 +60,97 @@ __global__ void __launch_bounds__(kCopyThreads) tile_copy_kernel(
   }
 }
 
-// Pinned staging for one acquire or flush: its task list and page table
-// mirror, and the event recorded after the moves that read them.
+// Host threads that run the host-side tile copies of the staged path.  A
+// stream callback hands a list to the pool and waits for it: the copies happen
+// in stream order, on the pool's threads, without blocking the caller.
+class CopyPool {
+ public:
+  explicit CopyPool(size_t n) {
+    for (size_t i = 0; i < n; ++i) th_.emplace_back([this, i] { loop(i); });
+  }
+  ~CopyPool() {
+    {
+      std::lock_guard<std::mutex> g(mu_);
+      stop_ = true;
+      ++gen_;
+    }
+    cv_.notify_all();
+    for (auto& t : th_) t.join();
+  }
+  size_t size() const { return th_.size(); }
+  // Copy list[0, n) (tile_bytes each) with every thread of the pool; returns
+  // when all copies are done.  Called from one callback at a time.
+  void run(const TileCopy* list, size_t n, size_t tile_bytes) {
+    {
+      std::lock_guard<std::mutex> g(mu_);
+      list_ = list;
+      n_ = n;
+      tb_ = tile_bytes;
+      next_.store(0);
+      pending_ = th_.size();
+      ++gen_;
+    }
+    cv_.notify_all();
+    std::unique_lock<std::mutex> g(mu_);
+    done_cv_.wait(g, [this] { return pending_ == 0; });
+  }
+
+ private:
+  void loop(size_t) {
+    uint64_t seen = 0;
+    while (true) {
+      {
+        std::unique_lock<std::mutex> g(mu_);
+        cv_.wait(g, [&] { return gen_ != seen; });
+        seen = gen_;
+        if (stop_) return;
+      }
+      while (true) {                       // tiles handed out 8 at a time
+        const size_t i0 = next_.fetch_add(8);
+        if (i0 >= n_) break;
+        const size_t i1 = std::min(n_, i0 + 8);
+        for (size_t i = i0; i < i1; ++i)
+          std::memcpy(reinterpret_cast<void*>(list_[i].dst),
+                      reinterpret_cast<const void*>(list_[i].src), tb_);
+      }
+      {
+        std::lock_guard<std::mutex> g(mu_);
+        if (--pending_ == 0) done_cv_.notify_one();
+      }
+    }
+  }
+  std::vector<std::thread> th_;
+  std::mutex mu_;
+  std::condition_variable cv_, done_cv_;
+  const TileCopy* list_ = nullptr;
+  size_t n_ = 0, tb_ = 0, pending_ = 0;
+  std::atomic<size_t> next_{0};
+  uint64_t gen_ = 0;
+  bool stop_ = false;
+};
+
+// A list of host-side tile copies for the pool, run by a stream callback.
+struct HostMove {
+  CopyPool* pool;
+  const TileCopy* list;
+  size_t n;
+  size_t tile_bytes;
+};
+
+void CUDART_CB host_copy_cb(void* arg) {
+  const HostMove* m = static_cast<const HostMove*>(arg);
+  if (m->n) m->pool->run(m->list, m->n, m->tile_bytes);
+}
+
+// Pinned staging for one acquire, flush or write-back: its task lists and page
+// table mirror, and the event recorded after the moves that read them.
 struct Staging {
-  TileCopy* tasks = nullptr;
-  TileCopy* tasks_dev = nullptr;
+  TileCopy* tasks = nullptr;       // planned moves: [0, n_wb) write-backs, then fetches
+  TileCopy* tasks_dev = nullptr;   // device view of `tasks`
+  TileCopy* dev_tasks = nullptr;   // through the device staging buffer: device-side copies
+  TileCopy* dev_tasks_dev = nullptr;
+  std::vector<TileCopy> host_tasks;  // through the host staging buffer: host-side copies
+  std::vector<HostMove> moves;
   int32_t* pt = nullptr;
   cudaEvent_t done = nullptr;
   bool used = false;
@@ -100,6 +190,13 @@ struct oomb_offload {
   std::vector<uint32_t> need;            // per page: KV heads the current acquire needs
   uint64_t epoch = 0;
   size_t cap_tasks = 0;
+  // copy-engine path: tiles move through a device staging buffer (caller's)
+  // and a pinned host staging buffer (the library's) of the same size
+  char* dev_staging = nullptr;
+  char* host_staging = nullptr;
+  size_t stage_tiles = 0;                // tiles per round; 0: zero-copy kernels
+  CopyPool* pool = nullptr;              // host copy threads of the staged path
+  cudaEvent_t last_done = nullptr;       // moves of the previous call (any stream)
   Staging stage[4];
   int next_stage = 0;
   int64_t stats[6] = {0, 0, 0, 0, 0, 0};
@@ -124,9 +221,8 @@ oomb_status take_stage(oomb_offload* h, Staging** out) {
   return OOMB_OK;
 }
 
-// Launch the copies tasks[first, first + n) of a staging buffer.
-cudaError_t launch_copies(const oomb_offload* h, const Staging& st, size_t first, size_t n,
-                          cudaStream_t s) {
+// Launch the copies list[0, n) (device-readable list) with the copy kernel.
+cudaError_t launch_list(const oomb_offload* h, const TileCopy* list, size_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   // Same shared-memory carveout as the attention kernels, so that a copy CTA
   // can share an SM with one of theirs instead of waiting for the SM to drain.
@@ -139,8 +235,63 @@ cudaError_t launch_copies(const oomb_offload* h, const Staging& st, size_t first
     carveout_set = true;
   }
   tile_copy_kernel<<<static_cast<unsigned>(n), kCopyThreads, 0, s>>>(
-      st.tasks_dev + first, static_cast<int>(h->tile_bytes / 16));
+      list, static_cast<int>(h->tile_bytes / 16));
   return cudaGetLastError();
+}
+
+// Enqueue the planned moves st.tasks[0, n): write-backs [0, n_wb) (cache ->
+// host) before fetches [n_wb, n) (host -> cache, which may reuse a slot just
+// written back).  Zero-copy: the copy kernel reads or writes the host pools
+// directly.  Staged: per round of at most stage_tiles tiles, write-backs go
+// cache -> device staging (kernel) -> host staging (copy engine) -> host pools
+// (host callback), fetches the reverse way, so the bulk of the bytes crosses
+// the CPU-GPU link on a copy engine instead of occupying SMs.
+cudaError_t enqueue_moves(oomb_offload* h, Staging& st, size_t n_wb, size_t n, cudaStream_t s) {
+  if (h->stage_tiles == 0) {
+    cudaError_t e = launch_list(h, st.tasks_dev, n_wb, s);
+    if (e == cudaSuccess) e = launch_list(h, st.tasks_dev + n_wb, n - n_wb, s);
+    return e;
+  }
+  if (n == 0) return cudaSuccess;
+  if (h->last_done) {
+    cudaError_t e = cudaStreamWaitEvent(s, h->last_done, 0);   // one set of staging buffers
+    if (e != cudaSuccess) return e;
+  }
+  const size_t cap = h->stage_tiles, tb = h->tile_bytes;
+  st.host_tasks.resize(n);
+  st.moves.clear();
+  st.moves.reserve((n_wb + cap - 1) / cap + (n - n_wb + cap - 1) / cap);
+  for (size_t r0 = 0; r0 < n_wb; r0 += cap) {
+    const size_t k = std::min(cap, n_wb - r0);
+    for (size_t i = 0; i < k; ++i) {
+      st.dev_tasks[r0 + i] = {st.tasks[r0 + i].src,
+                              reinterpret_cast<uint4*>(h->dev_staging + i * tb)};
+      st.host_tasks[r0 + i] = {reinterpret_cast<const uint4*>(h->host_staging + i * tb),
+                               st.tasks[r0 + i].dst};
+    }
+    cudaError_t e = launch_list(h, st.dev_tasks_dev + r0, k, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h->host_staging, h->dev_staging, k * tb, cudaMemcpyDeviceToHost, s);
+    st.moves.push_back({h->pool, st.host_tasks.data() + r0, k, tb});
+    if (e == cudaSuccess) e = cudaLaunchHostFunc(s, host_copy_cb, &st.moves.back());
+    if (e != cudaSuccess) return e;
+  }
+  for (size_t r0 = n_wb; r0 < n; r0 += cap) {
+    const size_t k = std::min(cap, n - r0);
+    for (size_t i = 0; i < k; ++i) {
+      st.host_tasks[r0 + i] = {st.tasks[r0 + i].src,
+                               reinterpret_cast<uint4*>(h->host_staging + i * tb)};
+      st.dev_tasks[r0 + i] = {reinterpret_cast<const uint4*>(h->dev_staging + i * tb),
+                              st.tasks[r0 + i].dst};
+    }
+    st.moves.push_back({h->pool, st.host_tasks.data() + r0, k, tb});
+    cudaError_t e = cudaLaunchHostFunc(s, host_copy_cb, &st.moves.back());
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h->dev_staging, h->host_staging, k * tb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = launch_list(h, st.dev_tasks_dev + r0, k, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 void add_writeback(oomb_offload* h, Staging& st, size_t& n, int slot) {
@@ -194,6 +345,11 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
       return oomb::report(OOMB_ERR_INVALID_ARG,
                           "cache pool %d must be device memory, 16-byte aligned", i);
   }
+  if (d->dev_staging && (!is_device(d->dev_staging) ||
+                         reinterpret_cast<uintptr_t>(d->dev_staging) % 16 ||
+                         d->dev_staging_bytes < static_cast<int64_t>(tile)))
+    return oomb::report(OOMB_ERR_INVALID_ARG,
+                        "dev_staging must be device memory, 16-byte aligned, >= one tile");
   oomb_offload* h = new (std::nothrow) oomb_offload();
   if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "out of host memory");
   h->d = *d;
@@ -222,10 +378,28 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
   // per slot and KV head: an acquire writes back at most 2 tiles (dK, dV) and
   // fetches at most 4 (K, V, dK, dV); a flush writes back at most 2
   h->cap_tasks = static_cast<size_t>(d->cache_slots) * d->num_kv_heads * 6 + 16;
+  if (d->dev_staging) {
+    h->stage_tiles = static_cast<size_t>(d->dev_staging_bytes) / tile;
+    h->dev_staging = static_cast<char*>(d->dev_staging);
+    const unsigned hw = std::thread::hardware_concurrency();
+    h->pool = new (std::nothrow) CopyPool(std::max(1u, std::min(8u, hw ? hw / 2 : 1u)));
+    cudaError_t e = h->pool ? cudaHostAlloc(&h->host_staging, h->stage_tiles * tile,
+                                            cudaHostAllocDefault)
+                            : cudaErrorMemoryAllocation;
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->last_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      oomb_offload_destroy(h);
+      return oomb::report(OOMB_ERR_CUDA, "offload host staging: %s", cudaGetErrorString(e));
+    }
+  }
   for (auto& st : h->stage) {
     cudaError_t e = cudaHostAlloc(&st.tasks, h->cap_tasks * sizeof(TileCopy), cudaHostAllocMapped);
     if (e == cudaSuccess)
       e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&st.tasks_dev), st.tasks, 0);
+    if (e == cudaSuccess)
+      e = cudaHostAlloc(&st.dev_tasks, h->cap_tasks * sizeof(TileCopy), cudaHostAllocMapped);
+    if (e == cudaSuccess)
+      e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&st.dev_tasks_dev), st.dev_tasks, 0);
     if (e == cudaSuccess)
       e = cudaHostAlloc(&st.pt, static_cast<size_t>(d->num_pages) * sizeof(int32_t),
                         cudaHostAllocDefault);
@@ -358,12 +532,12 @@ oomb_status oomb_offload_acquire(oomb_offload* h, const int32_t* sel_host, int32
   // 4. page table of this chunk: cache slot of every resident page
   std::memcpy(st->pt, h->slot_of_page.data(), static_cast<size_t>(d.num_pages) * sizeof(int32_t));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_copies(h, *st, 0, n_wb, s);       // write-backs before the fetches
-  if (e == cudaSuccess) e = launch_copies(h, *st, n_wb, n - n_wb, s);
+  cudaError_t e = enqueue_moves(h, *st, n_wb, n, s);        // write-backs before the fetches
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(page_table_dev, st->pt, static_cast<size_t>(d.num_pages) * sizeof(int32_t),
                         cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaEventRecord(st->done, s);
+  if (e == cudaSuccess && h->last_done) e = cudaEventRecord(h->last_done, s);
   st->used = true;
   if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload acquire: %s", cudaGetErrorString(e));
   return OOMB_OK;
@@ -378,8 +552,9 @@ oomb_status oomb_offload_flush(oomb_offload* h, int32_t drop, void* stream) {
   for (int s = 0; s < h->d.cache_slots; ++s)
     if (h->page_of_slot[s] >= 0 && h->dirty[s]) add_writeback(h, *st, n, s);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_copies(h, *st, 0, n, s);
+  cudaError_t e = enqueue_moves(h, *st, n, n, s);
   if (e == cudaSuccess) e = cudaEventRecord(st->done, s);
+  if (e == cudaSuccess && h->last_done) e = cudaEventRecord(h->last_done, s);
   st->used = true;
   if (drop) {
     for (int sl = 0; sl < h->d.cache_slots; ++sl) {
@@ -408,8 +583,9 @@ oomb_status oomb_offload_writeback(oomb_offload* h, int32_t first_page, int32_t 
     if (s >= 0 && h->dirty[s]) add_writeback(h, *st, n, s);
   }
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_copies(h, *st, 0, n, cs);
+  cudaError_t e = enqueue_moves(h, *st, n, n, cs);
   if (e == cudaSuccess) e = cudaEventRecord(st->done, cs);
+  if (e == cudaSuccess && h->last_done) e = cudaEventRecord(h->last_done, cs);
   st->used = true;
   if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload writeback: %s", cudaGetErrorString(e));
   return OOMB_OK;
@@ -427,8 +603,12 @@ void oomb_offload_destroy(oomb_offload* h) {
     if (st.used && st.done) cudaEventSynchronize(st.done);
     if (st.done) cudaEventDestroy(st.done);
     if (st.tasks) cudaFreeHost(st.tasks);
+    if (st.dev_tasks) cudaFreeHost(st.dev_tasks);
     if (st.pt) cudaFreeHost(st.pt);
   }
+  if (h->last_done) cudaEventDestroy(h->last_done);
+  if (h->host_staging) cudaFreeHost(h->host_staging);
+  delete h->pool;
   delete h;
 }
 

@@ -52,7 +52,8 @@ class OombOffloadDesc(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("cache_k", ctypes.c_void_p), ("cache_v", ctypes.c_void_p),
                 ("cache_dk", ctypes.c_void_p), ("cache_dv", ctypes.c_void_p),
-                ("cache_slots", ctypes.c_int32)]
+                ("cache_slots", ctypes.c_int32), ("dev_staging", ctypes.c_void_p),
+                ("dev_staging_bytes", ctypes.c_int64)]
 
 
 class OombPagedKV(ctypes.Structure):
@@ -443,11 +444,12 @@ class OffloadCache:
 
     host: a PagedKV whose k, v (and dk, dv) are pinned CPU tensors
     ``[num_host_slots, Hkv, P, D]`` and whose page_table is a CPU int32 tensor
-    (logical page -> host slot).  The cache pools are allocated here on
+    (logical page -> host slot).  The cache pools (and, with staging_bytes > 0,
+    the device staging buffer the moves go through) are allocated here on
     ``device`` (torch); the library's handle holds only host state.
     """
 
-    def __init__(self, host: PagedKV, cache_slots: int, device="cuda"):
+    def __init__(self, host: PagedKV, cache_slots: int, device="cuda", staging_bytes=0):
         ns, hkv, p, d = host.k.shape
         self.host = host
         self.num_pages = host.page_table.numel()
@@ -460,12 +462,16 @@ class OffloadCache:
         self.cdk = torch.empty(shape, dtype=host.k.dtype, device=device) if grads else None
         self.cdv = torch.empty(shape, dtype=host.k.dtype, device=device) if grads else None
         self._pt_host = host.page_table.to(torch.int32).contiguous()
+        # staging_bytes > 0: moves through a device staging buffer and the copy
+        # engines; 0: zero-copy copy kernel
+        self.staging = (torch.empty(staging_bytes, dtype=torch.uint8, device=device)
+                        if staging_bytes else None)
         dt = OOMB_BF16 if host.k.dtype == torch.bfloat16 else OOMB_FP32
         ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
         desc = OombOffloadDesc(ptr(host.k), ptr(host.v), ptr(host.dk), ptr(host.dv),
                                self._pt_host.data_ptr(), self.num_pages, ns, p, hkv, d, dt,
                                ptr(self.ck), ptr(self.cv), ptr(self.cdk), ptr(self.cdv),
-                               cache_slots)
+                               cache_slots, ptr(self.staging), staging_bytes)
         h = ctypes.c_void_p()
         _check(load().oomb_offload_create(ctypes.byref(desc), ctypes.byref(h)))
         self._h = h

@@ -226,8 +226,10 @@ def _bits(t):
     return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
 
 
-@pytest.mark.parametrize("prefetch", [False, True])
-def test_offload_chunk_pass_matches_resident(prefetch):
+@pytest.mark.parametrize("prefetch,staging", [(False, 256 << 20), (True, 256 << 20),
+                                              (True, 0), (True, 5 * 64 * 128 * 2)],
+                         ids=["serial", "prefetch", "zero_copy", "staging_5_tiles"])
+def test_offload_chunk_pass_matches_resident(prefetch, staging):
     """Pools in pinned host memory behind a device cache that must reuse slots
     (28 slots for 64 pages): the chunk-recurrent pass gives bit-identical O,
     selections and host dK/dV to the same pass on resident pools, starting
@@ -238,7 +240,7 @@ def test_offload_chunk_pass_matches_resident(prefetch):
     o_r, dq_r, sels_r = oomb.chunk_recurrent_pass(q_full, do_full, kv, 512, 3)
     host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
                         x.page_table.cpu(), dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
-    cache = oomb.OffloadCache(host, 28, DEV)
+    cache = oomb.OffloadCache(host, 28, DEV, staging_bytes=staging)
     o_o, dq_o, sels_o = oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 512, 3,
                                                             prefetch=prefetch)
     torch.cuda.synchronize()
