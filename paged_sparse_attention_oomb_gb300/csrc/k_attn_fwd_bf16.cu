@@ -10,14 +10,18 @@
 // scores of three consecutive key tiles live in three TMEM buffers, so the
 // MMA S(j+2) = Q K_{j+2}^T only waits for O += P(j-1) V_{j-1} -- an MMA issued
 // one tile earlier -- and the softmax of tile j+1 can follow the softmax of
-// tile j without waiting for the O update of tile j.  Roles (320 threads):
+// tile j without waiting for the O update of tile j.  Roles (352 threads):
 //   warp 0      TMA producer: Q once; then K_j, V_j page by page through the
 //               page table (one 2-D box per page and 64-column half) into a
 //               6-slot shared ring; also allocates TMEM.
-//   warp 1      MMA issuer (a whole warp in lockstep, one elected lane issues):
-//                 S(j) = Q K_j^T into buffer j % 3      (SS)
-//                 O += P(j) V_j, P(j) in buffer j % 3   (P from TMEM)
-//               in the order S(0), S(1), then per j: O += P(j) V_j, S(j+2).
+//   warp 10     issues S(j) = Q K_j^T into buffer j % 3 (SS), j = 0, 1, ...,
+//               each once the O update that last read the buffer is done;
+//   warp 1      issues O += P(j) V_j, P(j) in buffer j % 3 (P from TMEM), each
+//               once P(j) is ready.  (Each a whole warp in lockstep, one
+//               elected lane issues.)  tcgen05.mma blocks its issuing thread
+//               while the tensor pipe's queue is full; with two issuing warps
+//               an O update waiting on the softmax never holds back the next
+//               score MMA, and the reverse.
 //   warps 2..9  softmax, two threads per query row (warps w and w + 4 share a
 //               TMEM lane quarter and split the 128 key columns): the half row
 //               of S is read from TMEM into registers once, the row maximum is
@@ -40,7 +44,8 @@
 namespace oomb {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kSWarp = 10;                      // issues S(j) = Q K_j^T
 constexpr int kSoftmaxThreads = 256;
 constexpr int kSlots = 6;                         // K/V ring (3 key tiles)
 constexpr int kSBufs = 3;                         // score buffers in TMEM
@@ -61,7 +66,7 @@ struct Bars {
   // test two phases ahead reads as complete).
   uint64_t s_full[kSBufs], p_ready[kSBufs], pv_done[kSBufs];
   uint64_t pair[4];           // the two softmax warps of a TMEM lane quarter
-  uint64_t drain;
+  uint64_t drain, drain_s;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -123,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 4; ++i) mbar_init(BAR(pair[i]), 64);
     mbar_init(BAR(drain), 1);
+    mbar_init(BAR(drain_s), 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -241,16 +247,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last >= 0) mbar_drain_wait(BAR(slot_full[sl]), (last / kSlots) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop in lockstep (its decisions are warp-uniform);
-    // one elected lane issues the MMAs and their commits.
+  } else if (warp == 1 || warp == kSWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Each issuing warp runs its loop in lockstep (its decisions are
+    // warp-uniform); one elected lane issues the MMAs and their commits.  A
+    // commit tracks the MMAs of its own thread, so s_full is committed by the
+    // S warp and pv_done by the O-update warp.
     constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
     const uint64_t d0 = desc_kmajor0(sbase);
     const uint64_t dQ = d0 + desc_off(kQOff);
     const uint64_t dRing_k = d0 + desc_off(kRingOff), dRing_mn = d0 + kDescMn + desc_off(kRingOff);
-    bool ok = mbar_wait_spin(BAR(q_full), 0, wc, kWhereFwdMma);
+    const bool s_role = warp == kSWarp;
+    bool ok = !s_role || mbar_wait_spin(BAR(q_full), 0, wc, kWhereFwdMma);
     // S(j) = Q K_j^T into buffer j % 3.  The buffer last held P(j-3), read by
     // the O update of tile j-3, which must be complete.
     auto issue_s = [&](int j) -> bool {
@@ -292,19 +301,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    // O += P(j) V_j goes first: S(j+2) waits for the O update of tile j-1, which
-    // is done by then, while the O update of tile j is what the pipe needs next
-    for (int j = 0; ok && j < n_tiles && j < 2; ++j) ok = issue_s(j);
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      if (!(ok = issue_pv(j))) break;
-      if (j + 2 < n_tiles && !(ok = issue_s(j + 2))) break;
+    if (s_role) {
+      for (int j = 0; ok && j < n_tiles; ++j) ok = issue_s(j);
+    } else {
+      for (int j = 0; ok && j < n_tiles; ++j) ok = issue_pv(j);
     }
     if (!ok) {
-      if (elect_one()) umma_commit(BAR(drain));
+      if (elect_one()) umma_commit(s_role ? BAR(drain_s) : BAR(drain));
       __syncwarp();
-      mbar_drain_wait(BAR(drain), 0);
+      mbar_drain_wait(s_role ? BAR(drain_s) : BAR(drain), 0);
     }
-  } else {
+  } else if (warp < kSWarp) {
     // ------------------------------------------------------------ softmax
     // Two warps per TMEM lane quarter (the same 32 query rows): warp half
     // ch = 0 takes key columns [0, 64), ch = 1 columns [64, 128).  Their
