@@ -29,6 +29,7 @@
 
 #include "oomb.h"
 #include "oomb_internal.h"
+#include "page_cache_directory.h"
 
 namespace {
 
@@ -179,16 +180,9 @@ bool is_device(const void* p) {
 struct oomb_offload {
   oomb_offload_desc d;
   size_t tile_bytes = 0;                 // P * D * element size
-  uint32_t all_heads = 0;
   std::vector<int32_t> host_pt;          // logical page -> host slot
-  std::vector<int32_t> slot_of_page;     // logical page -> cache slot, -1: not resident
-  std::vector<int32_t> page_of_slot;     // cache slot -> logical page, -1: free
-  std::vector<uint32_t> kv_valid;        // per slot: KV heads whose K and V tiles are loaded
-  std::vector<uint32_t> g_valid;         // per slot: KV heads whose dK and dV tiles are loaded
-  std::vector<uint32_t> dirty;           // per slot: KV heads whose dK/dV tiles are modified
-  std::vector<uint64_t> last_use;        // per slot: acquire number of its last use
-  std::vector<uint32_t> need;            // per page: KV heads the current acquire needs
-  uint64_t epoch = 0;
+  oomb::PageCacheDirectory* dir = nullptr;
+  std::vector<oomb::TileMove> moves;     // the current call's plan
   size_t cap_tasks = 0;
   // copy-engine path: tiles move through a device staging buffer (caller's)
   // and a pinned host staging buffer (the library's) of the same size
@@ -294,19 +288,58 @@ cudaError_t enqueue_moves(oomb_offload* h, Staging& st, size_t n_wb, size_t n, c
   return cudaSuccess;
 }
 
-void add_writeback(oomb_offload* h, Staging& st, size_t& n, int slot) {
-  const int page = h->page_of_slot[slot];
-  const int hs = h->host_pt[page];
-  for (int g = 0; g < h->d.num_kv_heads; ++g) {
-    if (!(h->dirty[slot] >> g & 1u)) continue;
-    st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(h->d.cache_dk, h, slot, g)),
-                     reinterpret_cast<uint4*>(tile_ptr(h->d.dk, h, hs, g))};
-    st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(h->d.cache_dv, h, slot, g)),
-                     reinterpret_cast<uint4*>(tile_ptr(h->d.dv, h, hs, g))};
-    h->stats[1] += 2;
-    h->stats[3] += 2 * static_cast<int64_t>(h->tile_bytes);
+// The copies of a plan's tile moves: two per move (K and V, or dK and dV).
+size_t plan_to_tasks(oomb_offload* h, Staging& st) {
+  const oomb_offload_desc& d = h->d;
+  size_t n = 0;
+  for (const oomb::TileMove& m : h->moves) {
+    const int hs = h->host_pt[m.page];
+    switch (m.kind) {
+      case oomb::TileMove::kWriteGrad:
+        st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.cache_dk, h, m.slot, m.head)),
+                         reinterpret_cast<uint4*>(tile_ptr(d.dk, h, hs, m.head))};
+        st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.cache_dv, h, m.slot, m.head)),
+                         reinterpret_cast<uint4*>(tile_ptr(d.dv, h, hs, m.head))};
+        h->stats[1] += 2;
+        h->stats[3] += 2 * static_cast<int64_t>(h->tile_bytes);
+        break;
+      case oomb::TileMove::kFetchKV:
+        st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.k, h, hs, m.head)),
+                         reinterpret_cast<uint4*>(tile_ptr(d.cache_k, h, m.slot, m.head))};
+        st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.v, h, hs, m.head)),
+                         reinterpret_cast<uint4*>(tile_ptr(d.cache_v, h, m.slot, m.head))};
+        h->stats[0] += 2;
+        h->stats[2] += 2 * static_cast<int64_t>(h->tile_bytes);
+        break;
+      case oomb::TileMove::kFetchGrad:
+        st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.dk, h, hs, m.head)),
+                         reinterpret_cast<uint4*>(tile_ptr(d.cache_dk, h, m.slot, m.head))};
+        st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.dv, h, hs, m.head)),
+                         reinterpret_cast<uint4*>(tile_ptr(d.cache_dv, h, m.slot, m.head))};
+        h->stats[0] += 2;
+        h->stats[2] += 2 * static_cast<int64_t>(h->tile_bytes);
+        break;
+    }
   }
-  h->dirty[slot] = 0;
+  return n;
+}
+
+// Enqueue st.tasks (write-backs [0, n_wb) first) and record the call's event.
+oomb_status finish_call(oomb_offload* h, Staging& st, size_t n_wb, size_t n, cudaStream_t s,
+                        int32_t* page_table_dev, const char* what) {
+  cudaError_t e = enqueue_moves(h, st, n_wb, n, s);
+  if (e == cudaSuccess && page_table_dev) {
+    std::memcpy(st.pt, h->dir->slot_of_page().data(),
+                static_cast<size_t>(h->d.num_pages) * sizeof(int32_t));
+    e = cudaMemcpyAsync(page_table_dev, st.pt,
+                        static_cast<size_t>(h->d.num_pages) * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(st.done, s);
+  if (e == cudaSuccess && h->last_done) e = cudaEventRecord(h->last_done, s);
+  st.used = true;
+  if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return OOMB_OK;
 }
 
 }  // namespace
@@ -354,7 +387,6 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
   if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "out of host memory");
   h->d = *d;
   h->tile_bytes = tile;
-  h->all_heads = d->num_kv_heads == 32 ? 0xFFFFFFFFu : ((1u << d->num_kv_heads) - 1u);
   h->host_pt.assign(d->host_page_table, d->host_page_table + d->num_pages);
   {
     std::vector<char> seen(d->num_host_slots, 0);
@@ -368,13 +400,12 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
       seen[s] = 1;
     }
   }
-  h->slot_of_page.assign(d->num_pages, -1);
-  h->page_of_slot.assign(d->cache_slots, -1);
-  h->kv_valid.assign(d->cache_slots, 0);
-  h->g_valid.assign(d->cache_slots, 0);
-  h->dirty.assign(d->cache_slots, 0);
-  h->last_use.assign(d->cache_slots, 0);
-  h->need.assign(d->num_pages, 0);
+  h->dir = new (std::nothrow) oomb::PageCacheDirectory(d->num_pages, d->cache_slots,
+                                                       d->num_kv_heads);
+  if (!h->dir) {
+    delete h;
+    return oomb::report(OOMB_ERR_INVALID_ARG, "out of host memory");
+  }
   // per slot and KV head: an acquire writes back at most 2 tiles (dK, dV) and
   // fetches at most 4 (K, V, dK, dV); a flush writes back at most 2
   h->cap_tasks = static_cast<size_t>(d->cache_slots) * d->num_kv_heads * 6 + 16;
@@ -418,7 +449,7 @@ oomb_status oomb_offload_acquire(oomb_offload* h, const int32_t* sel_host, int32
                                  int32_t* page_table_dev, void* stream) {
   if (!h || !page_table_dev) return oomb::report(OOMB_ERR_INVALID_ARG, "handle and page_table_dev");
   const oomb_offload_desc& d = h->d;
-  const int P = d.page_size, hkv = d.num_kv_heads;
+  const int P = d.page_size;
   if (chunk_start < 0 || chunk_len <= 0 || chunk_start % P || chunk_len % P ||
       chunk_start + chunk_len > d.num_pages * P)
     return oomb::report(OOMB_ERR_INVALID_ARG, "chunk [%d, %d) is not whole pages inside the cache",
@@ -427,120 +458,20 @@ oomb_status oomb_offload_acquire(oomb_offload* h, const int32_t* sel_host, int32
     return oomb::report(OOMB_ERR_INVALID_ARG, "n_sel %d / sel_host", n_sel);
   if (with_grads && !d.dk)
     return oomb::report(OOMB_ERR_INVALID_ARG, "with_grads needs the dK/dV pools");
-  // 1. the tiles this chunk reads: (sel[g][i], g) and every head of its own pages
-  std::vector<int32_t> pages;
-  pages.reserve(static_cast<size_t>(n_sel) * hkv + chunk_len / P);
-  auto want = [&](int l, uint32_t mask) {
-    if (h->need[l] == 0) pages.push_back(l);
-    h->need[l] |= mask;
-  };
-  const int own0 = chunk_start / P, own1 = (chunk_start + chunk_len) / P;
-  for (int g = 0; g < hkv; ++g)
-    for (int i = 0; i < n_sel; ++i) {
-      const int l = sel_host[static_cast<size_t>(g) * n_sel + i];
-      if (l < 0 || l >= own0) {
-        for (int x : pages) h->need[x] = 0;
-        return oomb::report(OOMB_ERR_INVALID_ARG, "sel[%d][%d] = %d is not a page before the chunk",
-                            g, i, l);
-      }
-      want(l, 1u << g);
-    }
-  for (int l = own0; l < own1; ++l) want(l, h->all_heads);
-  if (static_cast<int>(pages.size()) > d.cache_slots) {
-    for (int x : pages) h->need[x] = 0;
-    return oomb::report(OOMB_ERR_INVALID_ARG, "the chunk needs %zu cache slots, the cache has %d",
-                        pages.size(), d.cache_slots);
-  }
-  // 2. slots: resident pages keep theirs; the others take free slots, then the
-  //    least recently used slots not used by this acquire or the one before it
-  const uint64_t ep = ++h->epoch;
-  int missing = 0;
-  for (int l : pages) {
-    const int s = h->slot_of_page[l];
-    if (s >= 0) h->last_use[s] = ep;
-    else ++missing;
-  }
-  std::vector<std::pair<uint64_t, int>> cand;
-  if (missing > 0) {
-    for (int s = 0; s < d.cache_slots; ++s)
-      if (h->page_of_slot[s] < 0) cand.push_back({0, s});
-      else if (h->last_use[s] + 1 < ep) cand.push_back({h->last_use[s], s});
-    if (static_cast<int>(cand.size()) < missing) {
-      for (int x : pages) h->need[x] = 0;
-      return oomb::report(OOMB_ERR_INVALID_ARG,
-                          "cache of %d slots: %d pages to bring in, %zu slots free or reusable "
-                          "(slots of this chunk and the previous one are kept)",
-                          d.cache_slots, missing, cand.size());
-    }
-    std::partial_sort(cand.begin(), cand.begin() + missing, cand.end());
-  }
+  // the staging buffer is taken first: a failed wait leaves the directory as it was
   Staging* st = nullptr;
   oomb_status rs = take_stage(h, &st);
-  if (rs != OOMB_OK) {
-    for (int x : pages) h->need[x] = 0;
-    return rs;
-  }
-  size_t n = 0;
-  int c = 0;
-  for (int l : pages) {
-    if (h->slot_of_page[l] >= 0) continue;
-    const int s = cand[c++].second;
-    const int old = h->page_of_slot[s];
-    if (old >= 0) {                              // reuse: modified gradients go home first
-      add_writeback(h, *st, n, s);
-      h->slot_of_page[old] = -1;
-      ++h->stats[5];
-    }
-    h->page_of_slot[s] = l;
-    h->slot_of_page[l] = s;
-    h->kv_valid[s] = h->g_valid[s] = h->dirty[s] = 0;
-    h->last_use[s] = ep;
-  }
-  const size_t n_wb = n;
-  // 3. fetch the missing tiles
-  for (int l : pages) {
-    const int s = h->slot_of_page[l];
-    const int hs = h->host_pt[l];
-    const uint32_t m = h->need[l];
-    h->need[l] = 0;
-    const uint32_t kv_miss = m & ~h->kv_valid[s];
-    const uint32_t g_miss = with_grads ? (m & ~h->g_valid[s]) : 0u;
-    for (int g = 0; g < hkv; ++g) {
-      if (kv_miss >> g & 1u) {
-        st->tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.k, h, hs, g)),
-                          reinterpret_cast<uint4*>(tile_ptr(d.cache_k, h, s, g))};
-        st->tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.v, h, hs, g)),
-                          reinterpret_cast<uint4*>(tile_ptr(d.cache_v, h, s, g))};
-      }
-      if (g_miss >> g & 1u) {
-        st->tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.dk, h, hs, g)),
-                          reinterpret_cast<uint4*>(tile_ptr(d.cache_dk, h, s, g))};
-        st->tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.dv, h, hs, g)),
-                          reinterpret_cast<uint4*>(tile_ptr(d.cache_dv, h, s, g))};
-      }
-    }
-    h->kv_valid[s] |= m;
-    if (with_grads) {
-      h->g_valid[s] |= m;
-      h->dirty[s] |= m;                          // the backward adds into them in place
-    }
-  }
-  const int64_t n_fetch = static_cast<int64_t>(n - n_wb);
-  h->stats[0] += n_fetch;
-  h->stats[2] += n_fetch * static_cast<int64_t>(h->tile_bytes);
+  if (rs != OOMB_OK) return rs;
+  h->moves.clear();
+  size_t n_wb_moves = 0;
+  const std::string err = h->dir->plan(sel_host, n_sel, chunk_start / P,
+                                       (chunk_start + chunk_len) / P, with_grads != 0, &h->moves,
+                                       &n_wb_moves, &h->stats[5]);
+  if (!err.empty()) return oomb::report(OOMB_ERR_INVALID_ARG, "%s", err.c_str());
+  const size_t n = plan_to_tasks(h, *st);
   ++h->stats[4];
-  // 4. page table of this chunk: cache slot of every resident page
-  std::memcpy(st->pt, h->slot_of_page.data(), static_cast<size_t>(d.num_pages) * sizeof(int32_t));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = enqueue_moves(h, *st, n_wb, n, s);        // write-backs before the fetches
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(page_table_dev, st->pt, static_cast<size_t>(d.num_pages) * sizeof(int32_t),
-                        cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaEventRecord(st->done, s);
-  if (e == cudaSuccess && h->last_done) e = cudaEventRecord(h->last_done, s);
-  st->used = true;
-  if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload acquire: %s", cudaGetErrorString(e));
-  return OOMB_OK;
+  return finish_call(h, *st, 2 * n_wb_moves, n, static_cast<cudaStream_t>(stream),
+                     page_table_dev, "offload acquire");
 }
 
 oomb_status oomb_offload_flush(oomb_offload* h, int32_t drop, void* stream) {
@@ -548,24 +479,11 @@ oomb_status oomb_offload_flush(oomb_offload* h, int32_t drop, void* stream) {
   Staging* st = nullptr;
   oomb_status rs = take_stage(h, &st);
   if (rs != OOMB_OK) return rs;
-  size_t n = 0;
-  for (int s = 0; s < h->d.cache_slots; ++s)
-    if (h->page_of_slot[s] >= 0 && h->dirty[s]) add_writeback(h, *st, n, s);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = enqueue_moves(h, *st, n, n, s);
-  if (e == cudaSuccess) e = cudaEventRecord(st->done, s);
-  if (e == cudaSuccess && h->last_done) e = cudaEventRecord(h->last_done, s);
-  st->used = true;
-  if (drop) {
-    for (int sl = 0; sl < h->d.cache_slots; ++sl) {
-      if (h->page_of_slot[sl] >= 0) h->slot_of_page[h->page_of_slot[sl]] = -1;
-      h->page_of_slot[sl] = -1;
-      h->kv_valid[sl] = h->g_valid[sl] = h->dirty[sl] = 0;
-      h->last_use[sl] = 0;
-    }
-  }
-  if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload flush: %s", cudaGetErrorString(e));
-  return OOMB_OK;
+  h->moves.clear();
+  h->dir->collect_writebacks(0, -1, &h->moves);
+  if (drop) h->dir->drop();
+  const size_t n = plan_to_tasks(h, *st);
+  return finish_call(h, *st, n, n, static_cast<cudaStream_t>(stream), nullptr, "offload flush");
 }
 
 oomb_status oomb_offload_writeback(oomb_offload* h, int32_t first_page, int32_t n_pages,
@@ -577,18 +495,11 @@ oomb_status oomb_offload_writeback(oomb_offload* h, int32_t first_page, int32_t 
   Staging* st = nullptr;
   oomb_status rs = take_stage(h, &st);
   if (rs != OOMB_OK) return rs;
-  size_t n = 0;
-  for (int l = first_page; l < first_page + n_pages; ++l) {
-    const int s = h->slot_of_page[l];
-    if (s >= 0 && h->dirty[s]) add_writeback(h, *st, n, s);
-  }
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = enqueue_moves(h, *st, n, n, cs);
-  if (e == cudaSuccess) e = cudaEventRecord(st->done, cs);
-  if (e == cudaSuccess && h->last_done) e = cudaEventRecord(h->last_done, cs);
-  st->used = true;
-  if (e != cudaSuccess) return oomb::report(OOMB_ERR_CUDA, "offload writeback: %s", cudaGetErrorString(e));
-  return OOMB_OK;
+  h->moves.clear();
+  h->dir->collect_writebacks(first_page, n_pages, &h->moves);
+  const size_t n = plan_to_tasks(h, *st);
+  return finish_call(h, *st, n, n, static_cast<cudaStream_t>(stream), nullptr,
+                     "offload writeback");
 }
 
 oomb_status oomb_offload_stats(const oomb_offload* h, int64_t* out) {
@@ -609,6 +520,7 @@ void oomb_offload_destroy(oomb_offload* h) {
   if (h->last_done) cudaEventDestroy(h->last_done);
   if (h->host_staging) cudaFreeHost(h->host_staging);
   delete h->pool;
+  delete h->dir;
   delete h;
 }
 
