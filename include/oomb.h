@@ -242,9 +242,12 @@ oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *dout,
  * acquires must have completed (the caller orders the streams with events),
  * and each in-flight chunk needs its own page_table_dev.  The call blocks the
  * host only until the moves enqueued four calls earlier (acquire, flush or
- * writeback) have completed (four pinned staging buffers).  Errors: OOMB_ERR_INVALID_ARG if a page index is
- * out of range, a host slot is out of range, or the chunk's pages do not fit
- * in the cache next to those of the previous acquire.
+ * writeback) have completed (four pinned staging buffers).  Errors:
+ * OOMB_ERR_INVALID_ARG if a page index is out of range or the chunk's pages
+ * do not fit in the cache next to those of the previous acquire (the
+ * directory is then unchanged); OOMB_ERR_CUDA if a launch or copy fails.
+ * oomb_offload_create rejects a host page table that is out of range or not
+ * injective.
  * ------------------------------------------------------------------------- */
 typedef struct {
   void *k, *v, *dk, *dv;          /* host tier: pinned host pools; dk/dv may be NULL (forward only) */
