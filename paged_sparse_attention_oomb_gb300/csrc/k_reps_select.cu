@@ -299,12 +299,18 @@ __global__ void __launch_bounds__(256) page_scores_kernel(const float* __restric
 // ---------------------------------------------------------------------------
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkSmemKeys = 48 * 1024;          // keys cached in shared memory
+constexpr int kTopkCand = 2048;                   // keys of one value bin resolved exactly
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   if (f != f) return 0u;                          // NaN never outranks a number
   if (f == 0.f) f = 0.f;                          // -0 == +0
   const uint32_t b = __float_as_uint(f);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The float a key stands for (inverse of order_key on numbers).
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
@@ -389,15 +395,81 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   __syncthreads();
   auto key_at = [&](int i) -> uint32_t { return cached ? keys_sm[i] : order_key(__ldcg(sc + i)); };
 
-  // Every key shares the bits above the highest bit where min and max differ:
-  // the radix digits start just below that common prefix, so the first
-  // histogram spreads even when all scores have similar magnitude.
-  const uint32_t diff = sh_min ^ sh_max;
-  int lo_bit = diff ? 32 - __clz(diff) : 0;       // bits [0, lo_bit) still vary
-  const uint32_t low = (lo_bit >= 32) ? 0xFFFFFFFFu : ((1u << lo_bit) - 1u);
-  uint32_t prefix = sh_max & ~low;                // the common high bits
-  uint32_t mask = ~low;
+  // Fast path: a histogram of the score values in 2048 equal-width bins
+  // between the smallest and the largest score.  The scores of a head sit in
+  // a narrow range of either sign, where the bits of their encodings put
+  // most keys in a few radix bins; equal-width value bins spread them.  The
+  // bin is monotone in the score, so every key of a higher bin ranks above
+  // every key of a lower one, and the k-th largest key is found exactly among
+  // the keys of its own bin (ranked by counting).  Degenerate ranges, or a bin
+  // with more than kTopkCand keys, take the radix passes below.
+  __shared__ uint32_t cand[kTopkCand];
+  __shared__ int sh_nc, sh_bin;
+  uint32_t prefix = 0;
   int need = k;                                   // still to take at or below `prefix`
+  bool fast = false;
+  {
+    const float fmin = key_value(sh_min), fmax = key_value(sh_max);
+    const float inv_w = 2048.f / (fmax - fmin);
+    if (fmax > fmin && isfinite(fmin) && isfinite(fmax) && isfinite(inv_w)) {
+      auto vbin = [&](uint32_t key) -> int {
+        const int b = static_cast<int>((key_value(key) - fmin) * inv_w);
+        return b < 2047 ? b : 2047;
+      };
+      for (int i = threadIdx.x; i < 2048; i += blockDim.x) hist[i] = 0;
+      if (threadIdx.x == 0) sh_nc = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < n_cand; i += blockDim.x) atomicAdd(&hist[vbin(key_at(i))], 1);
+      __syncthreads();
+      // bin counts from the top: thread t owns bins 2047 - 2t and 2046 - 2t
+      const int b_hi = 2047 - 2 * static_cast<int>(threadIdx.x);
+      const int c0 = hist[b_hi], c1 = hist[b_hi - 1];
+      const int before = block_excl_scan(c0 + c1, warp_tot, &total);
+      if (before < k && before + c0 >= k) {
+        sh_bin = b_hi;
+        sh_need = k - before;
+      } else if (before + c0 < k && before + c0 + c1 >= k) {
+        sh_bin = b_hi - 1;
+        sh_need = k - before - c0;
+      }
+      __syncthreads();
+      const int bin = sh_bin, need_b = sh_need, c_b = hist[bin];
+      if (c_b <= kTopkCand) {
+        for (int i = threadIdx.x; i < n_cand; i += blockDim.x) {
+          const uint32_t key = key_at(i);
+          if (vbin(key) == bin) cand[atomicAdd(&sh_nc, 1)] = key;
+        }
+        __syncthreads();
+        // the need_b-th largest key of the bin: gt keys above it, eq equal to it
+        for (int c = threadIdx.x; c < c_b; c += blockDim.x) {
+          const uint32_t x = cand[c];
+          int gt = 0, eq = 0;
+          for (int u = 0; u < c_b; ++u) {
+            gt += cand[u] > x;
+            eq += cand[u] == x;
+          }
+          if (gt < need_b && need_b <= gt + eq) {  // every writer writes the same values
+            sh_prefix = x;
+            sh_nc = need_b - gt;
+          }
+        }
+        __syncthreads();
+        prefix = sh_prefix;
+        need = sh_nc;
+        fast = true;
+      }
+      __syncthreads();
+    }
+  }
+  // Radix passes: every key shares the bits above the highest bit where min
+  // and max differ, so the digits start just below that common prefix.
+  const uint32_t diff = sh_min ^ sh_max;
+  int lo_bit = (fast || !diff) ? 0 : 32 - __clz(diff);   // bits [0, lo_bit) still vary
+  if (!fast) {
+    const uint32_t low = (lo_bit >= 32) ? 0xFFFFFFFFu : ((1u << lo_bit) - 1u);
+    prefix = sh_max & ~low;                       // the common high bits
+  }
+  uint32_t mask = (lo_bit >= 32) ? 0u : ~((1u << lo_bit) - 1u);
   while (lo_bit > 0) {
     const int width = lo_bit < 11 ? lo_bit : 11;
     const int sh = lo_bit - width, nbins = 1 << width;
