@@ -347,9 +347,18 @@ def run_ours(args, rank, world, dev):
 
     flops = attn_flops(wl)
     pk, pk_src = peaks()
-    chunk_pass = (measure_chunk_pass(dev, pk["bf16_tflops_sustained"])
+    def optional(fn):
+        # the side measurements must not cost the step's line: a failure (for
+        # example pinned host memory refused) is reported in place of the figures
+        try:
+            return fn()
+        except Exception as e:  # noqa: BLE001
+            torch.cuda.synchronize()
+            return {"error": f"{type(e).__name__}: {e}"[:300]}
+
+    chunk_pass = (optional(lambda: measure_chunk_pass(dev, pk["bf16_tflops_sustained"]))
                   if args.chunk_pass and wl.dtype == "bf16" else None)
-    offload = (measure_offload(wl, x, kv, reps, dev)
+    offload = (optional(lambda: measure_offload(wl, x, kv, reps, dev))
                if args.offload and wl.dtype == "bf16" and wl.n_sel > 0 else None)
     pairs_total = pairs_per_head(wl) * hq
     bwd_flops = 10.0 * d * pairs_total
