@@ -57,7 +57,7 @@ __all__ = [
 # ---------------------------------------------------------------------------
 # Step 1: representative vector of each page
 # ---------------------------------------------------------------------------
-def page_reps(k_pool, page_table, first_page=0, n_pages=None, block=1024):
+def page_reps(k_pool, page_table, first_page=0, n_pages=None, block=1024, n_tokens=None):
     """Mean of each page's keys, per KV head.
 
     Page-level Sparse Attention item: pages are ranked by a representative
@@ -67,16 +67,28 @@ def page_reps(k_pool, page_table, first_page=0, n_pages=None, block=1024):
     fp32 where the stored representative is fp32).  Pages are processed in
     groups of ``block`` only to bound host memory; each page's mean is
     independent of every other page.
+
+    ``n_tokens`` (optional) is the length of the sequence when its last page
+    is only partly written.  Reading: a page holds only the tokens written to
+    it, so the page that ``n_tokens`` cuts is represented by the mean of its
+    keys at positions below ``n_tokens``; the rows after them hold no token.
+    A page wholly at or after ``n_tokens`` has no representative (ValueError).
     """
     pt = np.asarray(page_table)
     if n_pages is None:
         n_pages = pt.shape[0] - first_page
     num_slots, hkv, p, d = k_pool.shape
     out = np.empty((n_pages, hkv, d), np.float64)
+    if n_tokens is not None and n_pages > 0 and (first_page + n_pages - 1) * p >= n_tokens:
+        raise ValueError("a page with no token before n_tokens has no representative")
     for b0 in range(0, n_pages, block):
         b1 = min(n_pages, b0 + block)
         slots = pt[first_page + b0:first_page + b1]
         out[b0:b1] = k_pool[slots].astype(np.float64).mean(axis=2)
+    cut = None if n_tokens is None or n_tokens % p == 0 else n_tokens // p
+    if cut is not None and first_page <= cut < first_page + n_pages:
+        # the partial page: only its first n_tokens % P rows hold tokens
+        out[cut - first_page] = k_pool[pt[cut], :, :n_tokens % p].astype(np.float64).mean(axis=1)
     return out
 
 
@@ -375,12 +387,18 @@ def chunk_recurrent_grads(q_full, k_pool, v_pool, page_table, do_full, chunk_len
     c scores its past pages, keeps ``top_k`` of them, and attends them plus
     its own causal pages; chunks are then differentiated from last to first,
     every call adding its dK/dV into the same logical-page accumulators.
+    ``chunk_len`` is a multiple of P, so every chunk starts on a page; when T
+    is not a multiple of ``chunk_len`` the last chunk is shorter, and when T
+    is not a multiple of P its last page is partial (its rows past T are
+    neither attended nor given gradient).
     Returns ``(o_full, dq_full, dk_acc, dv_acc, sels)``.
     """
     t, hq, d = q_full.shape
     hkv = k_pool.shape[1]
-    n_chunks = t // chunk_len
-    reps = page_reps(k_pool, page_table)
+    if chunk_len % page_size:
+        raise ValueError("chunks must start on a page boundary")
+    n_chunks = -(-t // chunk_len)
+    reps = page_reps(k_pool, page_table, 0, -(-t // page_size), n_tokens=t)
     outs, sels = [], []
     for c in range(n_chunks):
         t0 = c * chunk_len

@@ -188,6 +188,41 @@ def test_cross_chunk_accumulation_equals_single_pass():
     np.testing.assert_allclose(_flat(dv_acc), dvd, atol=1e-12)
 
 
+def _ragged_case(t, hq=4, hkv=2, d=8, p=8, seed=3, tail=1e3):
+    """A sequence of T tokens in ceil(T/P) shuffled pages; the rows of the last
+    page past T hold large values that must never be read."""
+    rng = np.random.default_rng(seed)
+    n = -(-t // p)
+    k_log = rng.normal(size=(n, hkv, p, d)) + 0.5 * rng.normal(size=(n, hkv, 1, d))
+    v_log = rng.normal(size=(n, hkv, p, d))
+    if t % p:
+        k_log[-1, :, t % p:] = tail * rng.normal(size=(hkv, p - t % p, d))
+        v_log[-1, :, t % p:] = tail * rng.normal(size=(hkv, p - t % p, d))
+    pt = rng.permutation(n)
+    k_pool = np.empty_like(k_log); v_pool = np.empty_like(v_log)
+    k_pool[pt] = k_log; v_pool[pt] = v_log
+    return dict(q=rng.normal(size=(t, hq, d)), do=rng.normal(size=(t, hq, d)), k_log=k_log,
+                v_log=v_log, k_pool=k_pool, v_pool=v_pool, pt=pt, n=n, p=p, t=t)
+
+
+@pytest.mark.parametrize("t,chunk_len", [(123, 32), (120, 32), (101, 48), (5, 16)])
+def test_cross_chunk_ragged_sequence_equals_single_pass(t, chunk_len):
+    # a sequence that is not whole chunks (and, but for t = 120, not whole
+    # pages): the shorter last chunk and its partial page give the dense causal
+    # gradient over the T tokens; the rows past T get no gradient
+    c = _ragged_case(t)
+    o, dq, dk_acc, dv_acc, _ = oracle.chunk_recurrent_grads(
+        c["q"], c["k_pool"], c["v_pool"], c["pt"], c["do"], chunk_len=chunk_len, page_size=8,
+        top_k=10 ** 6)
+    kf, vf = _flat(c["k_log"])[:t], _flat(c["v_log"])[:t]
+    od, _, dqd, dkd, dvd = oracle.dense_causal_reference(c["q"], kf, vf, c["do"])
+    np.testing.assert_allclose(o, od, atol=1e-12)
+    np.testing.assert_allclose(dq, dqd, atol=1e-12)
+    np.testing.assert_allclose(_flat(dk_acc)[:t], dkd, atol=1e-12)
+    np.testing.assert_allclose(_flat(dv_acc)[:t], dvd, atol=1e-12)
+    assert np.all(_flat(dk_acc)[t:] == 0) and np.all(_flat(dv_acc)[t:] == 0)
+
+
 def test_no_selected_pages_is_chunk_local_causal():
     c = _rng_case(t=96, hq=4, hkv=2, d=8, p=8, seed=9)
     t0 = 56
@@ -237,6 +272,31 @@ def test_page_reps_closed_forms():
     np.testing.assert_array_equal(oracle.page_reps(one, np.arange(n)), one[:, :, 0])
     part = oracle.page_reps(pool, pt, first_page=2, n_pages=2)
     np.testing.assert_array_equal(part, reps[2:4])
+
+
+def test_page_reps_partial_last_page():
+    # the page cut by n_tokens: the mean of its written rows only; whatever the
+    # rows after them hold does not matter
+    hkv, p, d, n = 2, 8, 3, 4
+    rng = np.random.default_rng(4)
+    pool = rng.normal(size=(n, hkv, p, d)) * 1e3
+    pt = np.array([2, 0, 3, 1])
+    for l in range(n):
+        pool[pt[l]] = l + 10 * np.arange(hkv)[:, None, None]
+    pool[pt[3], :, 5:] = rng.normal(size=(hkv, p - 5, d)) * 1e3
+    full = oracle.page_reps(pool, pt, 0, 3)
+    reps = oracle.page_reps(pool, pt, 0, 4, n_tokens=3 * p + 5)
+    np.testing.assert_array_equal(reps[:3], full)
+    for g in range(hkv):
+        np.testing.assert_array_equal(reps[3, g], 3 + 10 * g)
+    # one written row: the representative is that key
+    one = oracle.page_reps(pool, pt, 3, 1, n_tokens=3 * p + 1)
+    np.testing.assert_array_equal(one[0], pool[pt[3], :, 0])
+    # whole pages: n_tokens changes nothing; a page with no token is refused
+    np.testing.assert_array_equal(oracle.page_reps(pool, pt, n_tokens=4 * p),
+                                  oracle.page_reps(pool, pt))
+    with pytest.raises(ValueError):
+        oracle.page_reps(pool, pt, 0, 4, n_tokens=3 * p)
 
 
 def test_score_is_mean_pair_logit_brute_force():
