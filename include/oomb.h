@@ -44,11 +44,17 @@
  *       reps                       float [num_pages][Hkv][D], logical order
  *       sel                        int32 [Hkv][n_sel], ascending, unique
  *   - GQA: query head h uses KV head h / (Hq / Hkv).
- *   - Own pages of a chunk: logical pages [chunk_start/P, (chunk_start +
- *     chunk_len)/P).  Candidates: logical pages [0, chunk_start/P).
+ *   - Own pages of a chunk: logical pages [chunk_start/P, ceil((chunk_start +
+ *     chunk_len)/P)).  Candidates: logical pages [0, chunk_start/P).
  *   - Supported: bf16 with D = 128 and P in {16, 32, 64, 128}; fp32 with
- *     D = 64 and P in {16, 32, 64, 128}.  chunk_start and chunk_len are
- *     multiples of P, chunk_len >= P.
+ *     D = 64 and P in {16, 32, 64, 128}.  chunk_start is a multiple of P and
+ *     chunk_len >= 1, chunk_start + chunk_len <= num_pages * P.
+ *   - Partial last page (a sequence whose length is not a multiple of P; only
+ *     its last chunk can end inside a page, since every chunk starts on one):
+ *     the rows of that page past chunk_start + chunk_len hold no token.  They
+ *     are never attended and their dK/dV rows are left as they are, but the
+ *     tensor-core kernels load them with the page and weight them by zero, so
+ *     their K and V values must be finite (a zero-initialised pool is).
  */
 #ifndef OOMB_H
 #define OOMB_H
@@ -116,7 +122,9 @@ oomb_status oomb_validate_page_table(const oomb_paged_kv *kv, void *ws, size_t w
  *   reps[l][g][d] = (1/P) sum_t K[page_table[l]][g][t][d]     (fp32 accumulate)
  * reps points at the row of logical page 0 ([num_pages][Hkv][D]); only the
  * requested rows are written.  ws: oomb_workspace_bytes(PAGE_REPS) (status
- * word only). */
+ * word only).  Every page is taken as P keys: the representative of a
+ * partial last page comes from oomb_sparse_attn_fwd_own_reps, which knows
+ * where the chunk ends. */
 oomb_status oomb_page_reps(const oomb_paged_kv *kv, int32_t first_page, int32_t n_pages,
                            float *reps, void *ws, size_t ws_bytes, void *stream);
 
@@ -177,10 +185,12 @@ oomb_status oomb_sparse_attn_fwd(const void *q, const oomb_paged_kv *kv, const i
  * chunks after it, so their representatives are needed as soon as the
  * chunk's forward is done).  Computes exactly what oomb_sparse_attn_fwd
  * computes and, in addition, reps[l][g][*] for the chunk's own pages
- * l in [chunk_start/P, (chunk_start+chunk_len)/P) and every KV head g --
+ * l in [chunk_start/P, ceil((chunk_start+chunk_len)/P)) and every KV head g --
  * the same values oomb_page_reps writes for those pages (bf16: bit-identical;
  * the forward kernel sums the K tiles it has already loaded into shared
  * memory in oomb_page_reps's order, so the chunk's keys are not read again).
+ * A partial last own page is represented by the mean of its rows that hold
+ * the chunk's keys (oomb_page_reps always takes whole pages).
  * reps: float [num_pages][Hkv][D], 16-byte aligned; other rows are not
  * touched.  fp32 pools: the representatives come from the representatives
  * kernel launched after the forward on the same stream (not fused).

@@ -133,7 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_iter = grp * nq;
   const int ppt = 128 / p.page_size;
   const int own_page0 = p.chunk_start / p.page_size;
-  const int n_own_pages = p.chunk_len / p.page_size;
+  // the last own page may be partial: its rows past the chunk are masked as keys
+  // (key_valid) and their gradient rows are left as they are
+  const int n_own_pages = (p.chunk_len + p.page_size - 1) / p.page_size;
   const int padded = p.n_qtiles * 128;
   const int32_t* sel_g = p.sel + static_cast<long>(g) * p.n_sel;
 

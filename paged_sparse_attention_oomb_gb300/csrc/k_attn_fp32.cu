@@ -318,7 +318,7 @@ KeyMap make_keymap(const KvDesc& kv, const int32_t* sel, int n_sel, int chunk_le
   km.g = 0;
   km.own_page0 = chunk_start / kv.page_size;
   km.n_cand = chunk_start / kv.page_size;
-  km.n_own_pages = chunk_len / kv.page_size;
+  km.n_own_pages = (chunk_len + kv.page_size - 1) / kv.page_size;   // the last may be partial
   return km;
 }
 

@@ -113,7 +113,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = p.t_sel + qt + 1;            // key tiles of this query tile
   const int ppt = 128 / p.page_size;               // pages per key tile
   const int own_page0 = p.chunk_start / p.page_size;
-  const int n_own_pages = p.chunk_len / p.page_size;
+  // the chunk's own pages; the last one may be partial (rows past the chunk's
+  // end hold no token: the causal mask never reaches them)
+  const int n_own_pages = (p.chunk_len + p.page_size - 1) / p.page_size;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(q_full), 1);
@@ -212,14 +214,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this lane's 4 columns [4 lane, 4 lane + 4): half, 16-byte chunk, offset in chunk
         const uint32_t col_off = (lane >> 4) * kHalfBytes + (lane & 1) * 8;
         const int chunk = (lane & 15) >> 1;
-        const float inv_p = 1.0f / static_cast<float>(p.page_size);
         for (int u = 0; u < ppt; ++u) {
           const int op = qt * ppt + u;                 // own page index in the chunk
           if (op >= n_own_pages) break;
+          // rows of the page that hold the chunk's keys (fewer on a partial page)
+          const int n_rows = min(p.page_size, p.chunk_len - op * p.page_size);
+          const float inv = 1.0f / static_cast<float>(n_rows);
           float s4[4] = {0.f, 0.f, 0.f, 0.f};
           for (int rg = 0; rg < 16; ++rg) {
             float a4[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int rr = rg; rr < p.page_size; rr += 16) {
+            for (int rr = rg; rr < n_rows; rr += 16) {
               const int row = u * p.page_size + rr;
               const uint32_t addr = tile + col_off + row * 128 + ((chunk ^ (row & 7)) << 4);
               uint32_t w0, w1;
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float4* dst = reinterpret_cast<float4*>(
               p.reps + (static_cast<long>(own_page0 + op) * p.hkv + g) * 128) + lane;
-          *dst = make_float4(s4[0] * inv_p, s4[1] * inv_p, s4[2] * inv_p, s4[3] * inv_p);
+          *dst = make_float4(s4[0] * inv, s4[1] * inv, s4[2] * inv, s4[3] * inv);
         }
       }
     }

@@ -53,11 +53,14 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 // One CTA of 256 threads per (page, KV head): 16 threads cover one 256-byte
 // key row with 16-byte loads, 16 row groups stride over the page's rows.
 // Rows are 256 bytes for both supported shapes (bf16 D=128, fp32 D=64).
+// The last page of the range may hold keys in its first last_rows rows only
+// (the partial last page of a sequence): its mean is over those rows.
 // ---------------------------------------------------------------------------
 template <typename T, int P>
 __global__ void __launch_bounds__(256) page_reps_kernel(const T* __restrict__ k,
                                                         const int32_t* __restrict__ pt,
-                                                        int first_page, int num_slots, int hkv,
+                                                        int first_page, int last_page,
+                                                        int last_rows, int num_slots, int hkv,
                                                         float* __restrict__ reps, int* status) {
   constexpr int E = Vec<T>::kElems;
   constexpr int D = 16 * E;
@@ -72,13 +75,14 @@ __global__ void __launch_bounds__(256) page_reps_kernel(const T* __restrict__ k,
     if (threadIdx.x == 0) raise_status(status, kStatusBounds, kWhereReps);
     return;
   }
+  const int rows = l == last_page ? last_rows : P;
   const int col = threadIdx.x & 15, rg = threadIdx.x >> 4;
   const T* base = k + (static_cast<size_t>(slot) * hkv + g) * P * D + col * E;
   uint4 v[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
     const int r = rg + RG * i;
-    v[i] = (r < P) ? ldg_stream(base + static_cast<size_t>(r) * D) : make_uint4(0, 0, 0, 0);
+    v[i] = (r < rows) ? ldg_stream(base + static_cast<size_t>(r) * D) : make_uint4(0, 0, 0, 0);
   }
   float acc[E];
 #pragma unroll
@@ -97,35 +101,32 @@ __global__ void __launch_bounds__(256) page_reps_kernel(const T* __restrict__ k,
     float s = 0.f;
 #pragma unroll
     for (int r = 0; r < RG; ++r) s += part[r][threadIdx.x];
-    reps[(static_cast<size_t>(l) * hkv + g) * D + threadIdx.x] = s * (1.0f / P);
+    const float inv = rows == P ? 1.0f / P : 1.0f / static_cast<float>(rows);
+    reps[(static_cast<size_t>(l) * hkv + g) * D + threadIdx.x] = s * inv;
   }
 }
 
 template <typename T>
-cudaError_t reps_dispatch(const KvDesc& kv, int first_page, int n_pages, float* reps, int* status,
-                          cudaStream_t st) {
+cudaError_t reps_dispatch(const KvDesc& kv, int first_page, int n_pages, int last_rows,
+                          float* reps, int* status, cudaStream_t st) {
   const dim3 grid(n_pages * kv.hkv);
   const T* k = static_cast<const T*>(kv.k);
+  const int last_page = first_page + n_pages - 1;
+#define OOMB_REPS_CASE(PS)                                                                  \
+  case PS:                                                                                  \
+    page_reps_kernel<T, PS><<<grid, 256, 0, st>>>(k, kv.page_table, first_page, last_page, \
+                                                  last_rows, kv.num_slots, kv.hkv, reps,    \
+                                                  status);                                  \
+    break;
   switch (kv.page_size) {
-    case 16:
-      page_reps_kernel<T, 16><<<grid, 256, 0, st>>>(k, kv.page_table, first_page, kv.num_slots,
-                                                    kv.hkv, reps, status);
-      break;
-    case 32:
-      page_reps_kernel<T, 32><<<grid, 256, 0, st>>>(k, kv.page_table, first_page, kv.num_slots,
-                                                    kv.hkv, reps, status);
-      break;
-    case 64:
-      page_reps_kernel<T, 64><<<grid, 256, 0, st>>>(k, kv.page_table, first_page, kv.num_slots,
-                                                    kv.hkv, reps, status);
-      break;
-    case 128:
-      page_reps_kernel<T, 128><<<grid, 256, 0, st>>>(k, kv.page_table, first_page, kv.num_slots,
-                                                     kv.hkv, reps, status);
-      break;
+    OOMB_REPS_CASE(16)
+    OOMB_REPS_CASE(32)
+    OOMB_REPS_CASE(64)
+    OOMB_REPS_CASE(128)
     default:
       return cudaErrorInvalidValue;
   }
+#undef OOMB_REPS_CASE
   return cudaGetLastError();
 }
 
@@ -584,10 +585,11 @@ __global__ void debug_wait_kernel(int* status, uint64_t limit_ns) {
 }  // namespace
 
 cudaError_t launch_page_reps(const KvDesc& kv, bool bf16, int first_page, int n_pages,
-                             float* reps, int* status, cudaStream_t st) {
+                             int last_rows, float* reps, int* status, cudaStream_t st) {
   if (n_pages == 0) return cudaSuccess;
-  return bf16 ? reps_dispatch<__nv_bfloat16>(kv, first_page, n_pages, reps, status, st)
-              : reps_dispatch<float>(kv, first_page, n_pages, reps, status, st);
+  if (last_rows < 1 || last_rows > kv.page_size) return cudaErrorInvalidValue;
+  return bf16 ? reps_dispatch<__nv_bfloat16>(kv, first_page, n_pages, last_rows, reps, status, st)
+              : reps_dispatch<float>(kv, first_page, n_pages, last_rows, reps, status, st);
 }
 
 size_t select_ws_bytes(int num_pages, int hkv, int head_dim) {

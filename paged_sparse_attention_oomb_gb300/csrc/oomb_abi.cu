@@ -74,9 +74,9 @@ oomb_status check_chunk(const oomb_paged_kv* kv, int hq, int chunk_len, int chun
   if (hq <= 0 || hq % kv->num_kv_heads != 0)
     return fail(OOMB_ERR_INVALID_ARG, "num_q_heads %d must be a positive multiple of Hkv %d", hq,
                 kv->num_kv_heads);
-  if (chunk_len < P || chunk_len % P != 0)
-    return fail(OOMB_ERR_INVALID_ARG, "chunk_len %d must be a positive multiple of P=%d",
-                chunk_len, P);
+  // the chunk may end inside a page (the last page of a sequence that is not
+  // whole pages); it always starts on one
+  if (chunk_len <= 0) return fail(OOMB_ERR_INVALID_ARG, "chunk_len %d must be positive", chunk_len);
   if (chunk_start < 0 || chunk_start % P != 0)
     return fail(OOMB_ERR_INVALID_ARG, "chunk_start %d must be a non-negative multiple of P=%d",
                 chunk_start, P);
@@ -227,7 +227,7 @@ oomb_status oomb_page_reps(const oomb_paged_kv* kv, int32_t first_page, int32_t 
   s = check_ws(ws, ws_bytes, oomb::kStatusBytes);
   if (s != OOMB_OK) return s;
   cudaError_t e = oomb::launch_page_reps(desc(kv), kv->dtype == OOMB_BF16, first_page, n_pages,
-                                         reps, static_cast<int*>(ws),
+                                         kv->page_size, reps, static_cast<int*>(ws),
                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OOMB_OK : cuda_fail(e, "oomb_page_reps launch");
 }
@@ -322,7 +322,9 @@ static oomb_status attn_fwd(const char* name, const void* q, const oomb_paged_kv
                                    static_cast<float*>(o), lse, static_cast<int*>(ws), st);
     if (e == cudaSuccess && own_reps != nullptr)
       e = oomb::launch_page_reps(desc(kv), false, chunk_start / kv->page_size,
-                                 chunk_len / kv->page_size, own_reps, static_cast<int*>(ws), st);
+                                 (chunk_len + kv->page_size - 1) / kv->page_size,
+                                 (chunk_len - 1) % kv->page_size + 1, own_reps,
+                                 static_cast<int*>(ws), st);
   }
   return e == cudaSuccess ? OOMB_OK : cuda_fail(e, name);
 }

@@ -49,8 +49,9 @@ struct KvDesc {
 };
 
 // --- k_reps_select.cu
+// last_rows: rows of the last page of the range that hold keys (P: whole pages)
 cudaError_t launch_page_reps(const KvDesc& kv, bool bf16, int first_page, int n_pages,
-                             float* reps, int* status, cudaStream_t st);
+                             int last_rows, float* reps, int* status, cudaStream_t st);
 constexpr int kQbarBlocks = 152;
 size_t select_ws_bytes(int num_pages, int hkv, int head_dim);
 cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, int n_cand,

@@ -450,10 +450,12 @@ oomb_status oomb_offload_acquire(oomb_offload* h, const int32_t* sel_host, int32
   if (!h || !page_table_dev) return oomb::report(OOMB_ERR_INVALID_ARG, "handle and page_table_dev");
   const oomb_offload_desc& d = h->d;
   const int P = d.page_size;
-  if (chunk_start < 0 || chunk_len <= 0 || chunk_start % P || chunk_len % P ||
-      chunk_start + chunk_len > d.num_pages * P)
-    return oomb::report(OOMB_ERR_INVALID_ARG, "chunk [%d, %d) is not whole pages inside the cache",
-                        chunk_start, chunk_start + chunk_len);
+  // the chunk starts on a page; its last page may be partial
+  if (chunk_start < 0 || chunk_len <= 0 || chunk_start % P ||
+      static_cast<long long>(chunk_start) + chunk_len > static_cast<long long>(d.num_pages) * P)
+    return oomb::report(OOMB_ERR_INVALID_ARG,
+                        "chunk [%d, %d) does not start on a page or runs past the %d pages",
+                        chunk_start, chunk_start + chunk_len, d.num_pages);
   if (n_sel < 0 || (n_sel > 0 && !sel_host))
     return oomb::report(OOMB_ERR_INVALID_ARG, "n_sel %d / sel_host", n_sel);
   if (with_grads && !d.dk)
@@ -465,7 +467,8 @@ oomb_status oomb_offload_acquire(oomb_offload* h, const int32_t* sel_host, int32
   h->moves.clear();
   size_t n_wb_moves = 0;
   const std::string err = h->dir->plan(sel_host, n_sel, chunk_start / P,
-                                       (chunk_start + chunk_len) / P, with_grads != 0, &h->moves,
+                                       (chunk_start + chunk_len + P - 1) / P, with_grads != 0,
+                                       &h->moves,
                                        &n_wb_moves, &h->stats[5]);
   if (!err.empty()) return oomb::report(OOMB_ERR_INVALID_ARG, "%s", err.c_str());
   const size_t n = plan_to_tasks(h, *st);

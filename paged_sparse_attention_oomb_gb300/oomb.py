@@ -387,7 +387,9 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
     backward).
 
     q_full, dout_full: ``[T, Hq, D]``, the tokens at positions [start, start + T)
-    (T a multiple of chunk_len, start a multiple of P).  reps: float
+    (start and chunk_len multiples of P, so that every chunk starts on a page;
+    when T is not a multiple of chunk_len the last chunk is shorter, and when
+    start + T is not a multiple of P it ends in a partial page).  reps: float
     ``[num_pages, Hkv, D]`` holding the representatives of the pages before
     ``start`` (computed here from the pool if None).  Returns
     ``(o_full, dq_full, sels)``; sels[c] is ``[Hkv, n_sel_c]``.
@@ -395,8 +397,8 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
     t, hq, d = q_full.shape
     ns, hkv, p, _ = kv.k.shape
     n_pages = kv.page_table.numel()
-    if t % chunk_len or chunk_len % p or start % p or start + t > n_pages * p:
-        raise OombError(OOMB_ERR_INVALID_ARG, "sequence must be whole chunks of whole pages")
+    if t < 1 or chunk_len < 1 or chunk_len % p or start % p or start + t > n_pages * p:
+        raise OombError(OOMB_ERR_INVALID_ARG, "chunks must start on pages inside the cache")
     dev = q_full.device
     if reps is None:
         reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
@@ -409,7 +411,7 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
     o_full = torch.empty_like(q_full)
     dq_full = torch.empty_like(q_full)
     lses, sels = [], []
-    n_chunks = t // chunk_len
+    n_chunks = -(-t // chunk_len)                 # the last chunk may be shorter
     for c in range(n_chunks):
         r0 = c * chunk_len
         t0 = start + r0
@@ -418,7 +420,7 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
         sel = torch.zeros((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
         if n_sel:
             oomb_select_topk(q, t0, reps, kv, n_sel, sel, ws_s, stream=stream)
-        lse = torch.empty((hq, chunk_len), dtype=torch.float32, device=dev)
+        lse = torch.empty((hq, q.shape[0]), dtype=torch.float32, device=dev)
         oomb_sparse_attn_fwd_own_reps(q, kv, sel, n_sel, t0, o_full[r0:r0 + chunk_len], lse, reps,
                                       ws_f, scale, stream)
         lses.append(lse)
@@ -540,8 +542,8 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     """
     t, hq, d = q_full.shape
     p, hkv, n_pages = cache.page_size, cache.hkv, cache.num_pages
-    if t % chunk_len or chunk_len % p or start % p or start + t > n_pages * p:
-        raise OombError(OOMB_ERR_INVALID_ARG, "sequence must be whole chunks of whole pages")
+    if t < 1 or chunk_len < 1 or chunk_len % p or start % p or start + t > n_pages * p:
+        raise OombError(OOMB_ERR_INVALID_ARG, "chunks must start on pages inside the cache")
     if start and reps is None:
         raise OombError(OOMB_ERR_INVALID_ARG, "reps of the pages before start are required")
     dev = q_full.device
@@ -562,9 +564,12 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     ws_b = workspace(OOMB_OP_ATTN_BWD, kv0, hq, chunk_len)
     o_full = torch.empty_like(q_full)
     dq_full = torch.empty_like(q_full)
-    n_chunks = t // chunk_len
+    n_chunks = -(-t // chunk_len)                 # the last chunk may be shorter
     last = n_chunks - 1
     sels, lses = [None] * n_chunks, [None] * n_chunks
+
+    def length(c):
+        return min(chunk_len, t - c * chunk_len)
     ready, done = [None] * n_chunks, [None] * n_chunks
     ready_last = [None]
 
@@ -588,7 +593,7 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
 
     def acquire(c, grads, pt):
         _, sel_h, n_sel = sels[c]
-        cache.acquire(sel_h, n_sel, start + c * chunk_len, chunk_len, grads, pt, cur())
+        cache.acquire(sel_h, n_sel, start + c * chunk_len, length(c), grads, pt, cur())
 
     def acquire_fwd(c):
         acquire(c, False, pts[c % 2])
@@ -607,7 +612,7 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
         r0 = c * chunk_len
         comp.wait_event(ready[c])
         sel, _, n_sel = sels[c]
-        lses[c] = torch.empty((hq, chunk_len), dtype=torch.float32, device=dev)
+        lses[c] = torch.empty((hq, length(c)), dtype=torch.float32, device=dev)
         oomb_sparse_attn_fwd(q_full[r0:r0 + chunk_len], cache.device_kv(pts[c % 2]), sel, n_sel,
                              start + r0, o_full[r0:r0 + chunk_len], lses[c], ws_f, scale, comp)
         done[c] = torch.cuda.Event()
@@ -643,7 +648,7 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
                 ready[c - 1] = mark()
             # chunk c's own pages are final: no earlier chunk reads them
             copy.wait_event(done[c])
-            cache.writeback((start + r0) // p, chunk_len // p, copy)
+            cache.writeback((start + r0) // p, -(-length(c) // p), copy)
     comp.wait_stream(copy)
     cache.flush(stream=comp)
     for w in (ws_r, ws_f, ws_b):

@@ -85,7 +85,9 @@ def test_bad_cache_rejected(lib, kw, code, msg):
 
 @pytest.mark.parametrize("args,msg", [
     (dict(hq=30), "multiple of Hkv"),
-    (dict(clen=100), "chunk_len"),
+    (dict(clen=0), "chunk_len"),
+    (dict(clen=-3), "chunk_len"),
+    (dict(cstart=3968, clen=129), "runs past"),   # a partial page past the last one
     (dict(cstart=100), "chunk_start"),
     (dict(cstart=4032), "runs past"),
     (dict(n_sel=61), "n_sel"),

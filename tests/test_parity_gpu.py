@@ -210,6 +210,122 @@ def test_fwd_own_reps(wl):
     compare(fused[p0:p1].cpu().numpy(), reps64[p0:p1], "fp32", f"{wl.name} own reps")
 
 
+# Chunks that end inside a page (the last chunk of a sequence that is not whole
+# pages): ragged query tiles, a partial last own page, ragged selection tiles.
+PARTIAL = [
+    W("bf16_p64_c453_k13", "bf16", 4, 2, 4096, 64, 453, 13, start=3584),     # last page: 5 rows
+    W("bf16_p128_g8_c300_k5", "bf16", 8, 1, 2048, 128, 300, 5, start=1024),  # 44 rows
+    W("bf16_p16_g1_c77_k37", "bf16", 2, 2, 1024, 16, 77, 37, start=512),     # 13 rows
+    W("bf16_single_query", "bf16", 4, 2, 2048, 64, 1, 4, start=1024),
+    W("bf16_first_chunk_c45", "bf16", 4, 2, 1024, 32, 45, 8, start=0),
+    W("fp32_p16_c99_k7", "fp32", 4, 2, 512, 16, 99, 7, start=256),          # 3 rows
+    W("fp32_p32_c45_k0", "fp32", 2, 1, 1024, 32, 45, 0, start=0),
+]
+
+
+def _spoil_tail(x, tokens, scale=30.0):
+    """Fill the rows of the partial page past ``tokens`` with large values: a
+    kernel that reads them as keys or values would show it."""
+    wl = x.wl
+    p = wl.page_size
+    if tokens % p == 0:
+        return
+    slot = int(x.page_table[tokens // p])
+    g = torch.Generator(device=DEV)
+    g.manual_seed(99)
+    for pool in (x.k_pool, x.v_pool):
+        tail = pool[slot, :, tokens % p:]
+        tail.copy_((scale * torch.randn(tail.shape, generator=g, device=DEV)).to(pool.dtype))
+
+
+@pytest.mark.parametrize("wl", PARTIAL, ids=[w.name for w in PARTIAL])
+def test_partial_last_page(wl):
+    """Forward and backward of a chunk whose last own page is partial, against
+    the oracle element by element, starting from nonzero gradients: the rows
+    past the chunk are never attended and keep their dK/dV bit for bit; the
+    fused forward represents the partial page by the mean of its written keys."""
+    x = make_inputs(wl, seed=6, device=DEV)
+    end = wl.start + wl.chunk_len
+    _spoil_tail(x, end)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(12)
+    init = [torch.randn(x.k_pool.shape, generator=g, device=DEV).to(x.k_pool.dtype)
+            for _ in range(2)]
+    kv = gpu_kv(x, grad_init=init)
+    q, kp, vp, do, pt = (to_numpy64(x.q), to_numpy64(x.k_pool), to_numpy64(x.v_pool),
+                         to_numpy64(x.do), to_numpy64(x.page_table))
+    p = wl.page_size
+    p0, p1 = wl.start // p, -(-end // p)
+    reps = gpu_reps(kv)
+    reps64 = oracle.page_reps(kp, pt, 0, p1, n_tokens=end)
+    sel_g, _ = gpu_select(x, kv, reps, wl.top_k)
+    sel_o, scores_o = oracle_selection(x, reps64, wl.top_k)
+    check_selection(sel_g.cpu().numpy(), sel_o, scores_o)
+    n_sel = sel_o.shape[1]
+    st = sel_tensor(sel_o, DEV)
+    # forward with the own representatives fused in
+    o_g = torch.empty_like(x.q)
+    lse_g = torch.empty((wl.num_q_heads, wl.chunk_len), dtype=torch.float32, device=DEV)
+    fused = torch.full_like(reps, float("nan"))
+    ws = oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv, wl.num_q_heads, wl.chunk_len)
+    oomb.oomb_sparse_attn_fwd_own_reps(x.q, kv, st, n_sel, wl.start, o_g, lse_g, fused, ws)
+    code, where, blk = oomb.oomb_device_status(ws)
+    assert code == oomb.OOMB_OK, (code, where, blk)
+    full_end = p1 if end % p == 0 else p1 - 1
+    assert torch.equal(fused[p0:full_end], reps[p0:full_end])
+    compare(fused[p0:p1].cpu().numpy(), reps64[p0:p1], "fp32", f"{wl.name} own reps")
+    assert torch.isnan(fused[:p0]).all() and torch.isnan(fused[p1:]).all()
+    dq_g = gpu_bwd(x, kv, st, n_sel, o_g, lse_g)
+    o_o, lse_o = oracle.attn_fwd(q, kp, vp, pt, sel_o, wl.start, p)
+    dk_o, dv_o = to_numpy64(init[0])[pt], to_numpy64(init[1])[pt]
+    dq_o, dk_o, dv_o = oracle.attn_bwd(q, kp, vp, pt, sel_o, wl.start, p, o_o, lse_o, do,
+                                       dk_acc=dk_o, dv_acc=dv_o)
+    dt = wl.dtype
+    compare(o_g.float().cpu().numpy(), o_o, dt, f"{wl.name} O")
+    np.testing.assert_allclose(lse_g.cpu().numpy(), lse_o, atol=2e-3 if dt == "bf16" else 1e-4)
+    compare(dq_g.float().cpu().numpy(), dq_o, dt, f"{wl.name} dQ")
+    dk_g, dv_g = to_numpy64(kv.dk)[pt], to_numpy64(kv.dv)[pt]
+    compare(dk_g, dk_o, dt, f"{wl.name} dK")
+    compare(dv_g, dv_o, dt, f"{wl.name} dV")
+    # the rows past the chunk and the pages after it: exactly the initial values
+    k0, v0 = to_numpy64(init[0])[pt], to_numpy64(init[1])[pt]
+    if end % p:
+        assert np.array_equal(dk_g[end // p, :, end % p:], k0[end // p, :, end % p:])
+        assert np.array_equal(dv_g[end // p, :, end % p:], v0[end // p, :, end % p:])
+    assert np.array_equal(dk_g[p1:], k0[p1:]) and np.array_equal(dv_g[p1:], v0[p1:])
+
+
+@pytest.mark.parametrize("top_k", [3, 1 << 20])
+def test_chunk_recurrent_pass_ragged_sequence(top_k):
+    """The sequence of test_chunk_recurrent_pass cut 19 tokens before its end:
+    2029 tokens in chunks of 512, the last chunk has 493 rows and ends 45 rows
+    into its last page, whose unwritten rows hold large values.  Selections,
+    O, dQ and the paged dK/dV against the oracle's chunk-recurrent pass; the
+    rows past the sequence keep zero gradient."""
+    t = 2029
+    wl = W("crp_ragged", "bf16", 4, 2, 2048, 64, 512, top_k)
+    x = make_inputs(wl, seed=8, device=DEV)
+    _spoil_tail(x, t)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(3)
+    q_full = torch.randn((2048, 4, 128), generator=g, device=DEV).to(torch.bfloat16)[:t].contiguous()
+    do_full = torch.randn((2048, 4, 128), generator=g, device=DEV).to(torch.bfloat16)[:t].contiguous()
+    kv = gpu_kv(x)
+    o_g, dq_g, sels = oomb.chunk_recurrent_pass(q_full, do_full, kv, 512, top_k)
+    kp, vp, pt = to_numpy64(x.k_pool), to_numpy64(x.v_pool), to_numpy64(x.page_table)
+    o_o, dq_o, dk_o, dv_o, sels_o = oracle.chunk_recurrent_grads(
+        to_numpy64(q_full), kp, vp, pt, to_numpy64(do_full), 512, 64, top_k)
+    assert len(sels) == len(sels_o) == 4
+    for sg, so in zip(sels, sels_o):
+        assert sg.cpu().numpy().tolist() == so.tolist()
+    compare(o_g.float().cpu().numpy(), o_o, "bf16", "ragged chunk-recurrent O")
+    compare(dq_g.float().cpu().numpy(), dq_o, "bf16", "ragged chunk-recurrent dQ")
+    dk_g, dv_g = to_numpy64(kv.dk)[pt], to_numpy64(kv.dv)[pt]
+    compare(dk_g, dk_o, "bf16", "ragged chunk-recurrent dK")
+    compare(dv_g, dv_o, "bf16", "ragged chunk-recurrent dV")
+    assert np.all(dk_g[31, :, 45:] == 0) and np.all(dv_g[31, :, 45:] == 0)
+
+
 def _offload_case(seed):
     wl = W("offl", "bf16", 4, 2, 4096, 64, 512, 3)     # 64 pages; a chunk needs <= 3 * 2 + 8 pages
     x = make_inputs(wl, seed=seed, device=DEV)
@@ -283,6 +399,32 @@ def test_offload_chunk_pass_fp32():
     assert torch.equal(o_r, o_o) and torch.equal(dq_r, dq_o)
     assert torch.equal(kv.dk.cpu(), host.dk) and torch.equal(kv.dv.cpu(), host.dv)
     assert cache.stats()["slots_reused"] > 0
+    cache.close()
+
+
+def test_offload_ragged_sequence_matches_resident():
+    """The offloaded pass over a sequence that ends inside a page (4001 tokens,
+    chunks of 512, the last one 417 rows ending 33 rows into its last page):
+    bit-identical O, selections and host dK/dV to the resident pass."""
+    wl, x, q_full, do_full, dk0, dv0 = _offload_case(25)
+    t = 4001
+    _spoil_tail(x, t)
+    q_full, do_full = q_full[:t].contiguous(), do_full[:t].contiguous()
+    kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, dk0.clone(), dv0.clone())
+    o_r, dq_r, sels_r = oomb.chunk_recurrent_pass(q_full, do_full, kv, 512, 3)
+    host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
+                        x.page_table.cpu(), dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
+    cache = oomb.OffloadCache(host, 28, DEV)
+    o_o, dq_o, sels_o = oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 512, 3)
+    torch.cuda.synchronize()
+    assert len(sels_o) == 8
+    for a, b in zip(sels_r, sels_o):
+        assert torch.equal(a, b)
+    assert torch.equal(_bits(o_r), _bits(o_o))
+    a, b = dq_r.float(), dq_o.float()
+    assert float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(a)) < 1e-3
+    assert torch.equal(_bits(kv.dk.cpu()), _bits(host.dk))
+    assert torch.equal(_bits(kv.dv.cpu()), _bits(host.dv))
     cache.close()
 
 
