@@ -51,6 +51,7 @@ __all__ = [
     "attn_dq_rows",
     "dense_causal_reference",
     "chunk_recurrent_grads",
+    "fp8_e4m3_decode",
 ]
 
 
@@ -419,3 +420,26 @@ def chunk_recurrent_grads(q_full, k_pool, v_pool, page_table, do_full, chunk_len
         dq_full[t0:t0 + chunk_len] = dq
     o_full = np.concatenate([o for o, _ in outs], axis=0)
     return o_full, dq_full, dk_acc, dv_acc, sels
+
+
+# ---------------------------------------------------------------------------
+# Storage variant: K/V pools held as 8-bit E4M3 codes
+# ---------------------------------------------------------------------------
+def fp8_e4m3_decode(codes):
+    """Value of each 8-bit E4M3 code (OCP 8-bit floating point specification,
+    E4M3 format): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits.
+    Exponent field 0 encodes the subnormals m * 2^-9; the fields (15, 7) encode
+    NaN; there are no infinities, so 0x7E = 448 is the largest finite value.
+
+    Reading for an fp8 KV cache: a stored code stands for exactly this value
+    (no scale factor), and the path computes on these values as it does on the
+    values of a bf16 pool.  Returns float64 with the shape of ``codes``.
+    """
+    b = np.asarray(codes).astype(np.int64) & 0xFF
+    sign = np.where(b >> 7 == 1, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    sub = m * 2.0 ** -9
+    val = sign * np.where(e == 0, sub, normal)
+    return np.where((e == 15) & (m == 7), np.nan, val)

@@ -386,3 +386,30 @@ def test_golden_worked_example():
     np.testing.assert_allclose(dq[0, 0], [_ev(x) for x in exp["dq"]], atol=1e-14)
     np.testing.assert_allclose(dk[:, 0, 0], [[_ev(x) for x in r] for r in exp["dk"]], atol=1e-14)
     np.testing.assert_allclose(dv[:, 0, 0], [[_ev(x) for x in r] for r in exp["dv"]], atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# fp8 (E4M3) storage of the K/V pools
+# ---------------------------------------------------------------------------
+def test_fp8_e4m3_decode_worked_values():
+    # values worked out by hand from the format (bias 7, 3 mantissa bits)
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x38: 1.0, 0x3C: 1.5, 0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0, 0x30: 0.5,
+             0xB8: -1.0, 0xFE: -448.0, 0x81: -(2.0 ** -9)}
+    got = oracle.fp8_e4m3_decode(np.array(list(cases), np.uint8))
+    np.testing.assert_array_equal(got, np.array(list(cases.values())))
+    assert np.isnan(oracle.fp8_e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+    neg0 = oracle.fp8_e4m3_decode(np.array([0x80], np.uint8))
+    assert neg0[0] == 0.0 and np.signbit(neg0[0])
+
+
+def test_fp8_e4m3_decode_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.fp8_e4m3_decode(codes.numpy())
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got)) and nan.sum() == 2
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    # the 254 finite values are distinct up to the sign of zero, and monotone
+    pos = got[:127]
+    assert np.all(np.diff(pos) > 0)
