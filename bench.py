@@ -146,7 +146,9 @@ def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=3):
     device page cache (oomb_offload_*), the next chunk's tiles brought in on a
     second stream while the current chunk computes.  The cache starts empty
     in every offloaded pass.  Both passes are timed with CUDA events; the
-    difference is the offload overhead."""
+    difference is the offload overhead.  Then the same offloaded pass with the
+    host K/V pools stored as E4M3 codes (an fp8 KV cache, expanded to bf16 as
+    tiles are fetched), against the same resident time."""
     from paged_sparse_attention_oomb_gb300 import oomb
     c, p, hkv = wl.chunk_len, wl.page_size, wl.num_kv_heads
     start = wl.context - n_chunks * c
@@ -201,6 +203,32 @@ def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=3):
            "what": "fwd in order + bwd in reverse, cold cache per pass; next chunk's tiles "
                    "fetched on a second stream"}
     cache.close()
+    # fp8 KV: E4M3 host K/V pools (half the bytes over the link), same gradients
+    del host.k, host.v                  # the bf16 host K/V pools are not needed any more
+    t_host0 = time.time()
+    k8 = torch.empty(x.k_pool.shape, dtype=torch.float8_e4m3fn, pin_memory=True)
+    v8 = torch.empty(x.v_pool.shape, dtype=torch.float8_e4m3fn, pin_memory=True)
+    for dst, src in ((k8, x.k_pool), (v8, x.v_pool)):
+        for b0 in range(0, src.shape[0], 4096):
+            dst[b0:b0 + 4096].copy_(src[b0:b0 + 4096].to(torch.float8_e4m3fn))
+    setup8 = time.time() - t_host0
+    cache8 = oomb.OffloadCache(oomb.PagedKV(k8, v8, x.page_table.cpu(), host.dk, host.dv),
+                               2 * per_chunk + 64, dev)
+    before = cache8.stats()
+
+    def offloaded8():
+        cache8.flush(drop=True)
+        oomb.chunk_recurrent_pass_offloaded(q, do, cache8, c, wl.top_k, start=start, reps=reps)
+    ms8 = timed(offloaded8)
+    after = cache8.stats()
+    res["fp8_kv"] = {"ms_per_pass_offloaded": ms8, "overhead": ms8 / ms_res - 1.0,
+                     "host_pool_bytes": 2 * k8.numel() + 4 * k8.numel(),
+                     "bytes_in_per_pass": (after["bytes_in"] - before["bytes_in"]) / n_pass,
+                     "bytes_out_per_pass": (after["bytes_out"] - before["bytes_out"]) / n_pass,
+                     "host_setup_s": setup8,
+                     "what": "host K/V as E4M3 codes expanded to bf16 on fetch; overhead "
+                             "against the resident bf16 pass above"}
+    cache8.close()
     return res
 
 

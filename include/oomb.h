@@ -75,7 +75,10 @@ typedef enum {
   OOMB_ERR_DEVICE_BOUNDS = 5  /* a device-side index check failed        */
 } oomb_status;
 
-typedef enum { OOMB_BF16 = 0, OOMB_FP32 = 1 } oomb_dtype;
+/* OOMB_FP8_E4M3: 8-bit E4M3 codes (OCP 8-bit floating point specification),
+ * a storage format only: the K/V pools of an offload cache's backing tier
+ * (oomb_offload_desc.backing_kv_dtype).  Every kernel computes on bf16. */
+typedef enum { OOMB_BF16 = 0, OOMB_FP32 = 1, OOMB_FP8_E4M3 = 2 } oomb_dtype;
 
 /* The paged KV cache and its paged gradient buffers (Paged Memory Management
  * item).  dk/dv may be NULL for forward-only use. */
@@ -226,6 +229,15 @@ oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *dout,
  * The K, V, dK and dV pools of every page live in pinned host memory
  * ([num_host_slots][Hkv][P][D], caller-owned, allocated with cudaHostAlloc or
  * registered; the GPU reads and writes them directly over the CPU-GPU link).
+ * With the zero-copy moves (dev_staging NULL) this backing tier may instead be
+ * device memory: a compact tier in HBM in front of which the cache holds the
+ * working pages.
+ *
+ * fp8 KV (backing_kv_dtype = OOMB_FP8_E4M3, dtype = OOMB_BF16): the backing K
+ * and V pools hold E4M3 codes (one byte per element, P x D bytes per tile) and
+ * each fetch expands a tile to bf16 in the cache.  Every E4M3 value is a bf16
+ * value, so the expansion is exact and the kernels compute on exactly the
+ * stored values; dK/dV stay bf16 in both tiers.  Zero-copy moves only.
  * A cache of cache_slots page slots ([cache_slots][Hkv][P][D] for each of
  * K, V, dK, dV) lives in caller-owned device memory.  The unit moved is one
  * (page, KV head) tile of P x D elements; a cache slot holds one logical page
@@ -260,7 +272,7 @@ oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *dout,
  * injective.
  * ------------------------------------------------------------------------- */
 typedef struct {
-  void *k, *v, *dk, *dv;          /* host tier: pinned host pools; dk/dv may be NULL (forward only) */
+  void *k, *v, *dk, *dv;          /* backing tier (pinned host or device); dk/dv may be NULL (forward only) */
   const int32_t *host_page_table; /* HOST int32 [num_pages]: logical page -> host slot, injective */
   int32_t num_pages, num_host_slots, page_size, num_kv_heads, head_dim;
   oomb_dtype dtype;
@@ -276,13 +288,18 @@ typedef struct {
    * directly (zero-copy), which needs SMs. */
   void *dev_staging;
   int64_t dev_staging_bytes;
+  /* Element type of the backing K/V pools: dtype, or OOMB_FP8_E4M3 with
+   * dtype OOMB_BF16 (see fp8 KV above). */
+  oomb_dtype backing_kv_dtype;
 } oomb_offload_desc;
 
 typedef struct oomb_offload oomb_offload;   /* opaque; host memory of the library */
 
-/* Checks the description (the host pools must be pinned host memory and the
- * cache pools device memory), copies the host page table and allocates the
- * handle's host state and pinned staging buffers.  No device memory. */
+/* Checks the description (the backing pools must be pinned host memory, or
+ * device memory with zero-copy moves; the cache pools device memory), copies
+ * the host page table and allocates the handle's host state and pinned
+ * staging buffers.  No device memory.  OOMB_ERR_UNSUPPORTED for fp8 K/V with
+ * a staging buffer. */
 oomb_status oomb_offload_create(const oomb_offload_desc *desc, oomb_offload **out);
 oomb_status oomb_offload_acquire(oomb_offload *h, const int32_t *sel_host, int32_t n_sel,
                                  int32_t chunk_start, int32_t chunk_len, int32_t with_grads,

@@ -47,6 +47,10 @@ oomb_status check_kv(const oomb_paged_kv* kv) {
   if (!kv) return fail(OOMB_ERR_INVALID_ARG, "kv is NULL");
   if (!kv->k || !kv->v || !kv->page_table)
     return fail(OOMB_ERR_INVALID_ARG, "kv->k, kv->v and kv->page_table must be set");
+  if (kv->dtype == OOMB_FP8_E4M3)
+    return fail(OOMB_ERR_UNSUPPORTED,
+                "kv->dtype OOMB_FP8_E4M3 is a storage format of the offload backing tier; "
+                "the kernels read bf16 pools");
   if (kv->dtype != OOMB_BF16 && kv->dtype != OOMB_FP32)
     return fail(OOMB_ERR_INVALID_ARG, "kv->dtype %d is not OOMB_BF16 or OOMB_FP32", kv->dtype);
   if (kv->num_pages <= 0 || kv->num_slots <= 0)

@@ -15,6 +15,10 @@
 // and when the slot was last used.  Slots used by the current and the
 // previous acquire are never reused, so the next chunk's tiles can be brought
 // in on another stream while the current chunk computes.
+// The backing pools may also be device memory (a compact tier in HBM), and
+// the backing K/V pools may hold 8-bit E4M3 codes that each fetch expands to
+// bf16 in the cache (an fp8 KV cache; E4M3 values are bf16 values, so the
+// kernels see exactly the stored values).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -36,16 +40,58 @@ namespace {
 struct TileCopy {
   const uint4* src;
   uint4* dst;
+  int32_t expand;   // 1: src holds E4M3 codes, dst receives their bf16 values
+  int32_t pad;
 };
 
-// One CTA per tile of n16 16-byte words: 8 loads in flight per thread, then
-// the 8 stores.  Either side may be pinned host memory (zero-copy) or device
-// memory.  128 threads: small enough (in threads and registers) to share an SM
-// with a forward-attention CTA.
+// bf16 pair of the two E4M3 codes in the 16 bits `c2` (low code -> low half):
+// the hardware conversion to an f16 pair is exact (every E4M3 value is an f16
+// value), and so is each f16 -> f32 step, whose low 16 bits are then zero.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t c2) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+  float lo, hi;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(static_cast<uint16_t>(h2 & 0xFFFFu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(static_cast<uint16_t>(h2 >> 16)));
+  return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ uint4 expand8(uint32_t w0, uint32_t w1) {   // 8 codes -> 8 bf16
+  return make_uint4(e4m3x2_to_bf16x2(static_cast<uint16_t>(w0)),
+                    e4m3x2_to_bf16x2(static_cast<uint16_t>(w0 >> 16)),
+                    e4m3x2_to_bf16x2(static_cast<uint16_t>(w1)),
+                    e4m3x2_to_bf16x2(static_cast<uint16_t>(w1 >> 16)));
+}
+
+// One CTA per tile of n16 16-byte words (of the destination): 8 loads in
+// flight per thread, then the stores.  Either side may be pinned host memory
+// (zero-copy) or device memory.  An expanding task reads n16 / 2 words of
+// codes and writes two words per word read.  128 threads: small enough (in
+// threads and registers) to share an SM with a forward-attention CTA.
 constexpr int kCopyThreads = 128;
 __global__ void __launch_bounds__(kCopyThreads) tile_copy_kernel(
     const TileCopy* __restrict__ tasks, int n16) {
   const TileCopy t = tasks[blockIdx.x];
+  if (t.expand) {
+    const int n_src = n16 / 2;
+    for (int base = threadIdx.x; base < n_src; base += kCopyThreads * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = base + i * kCopyThreads;
+        if (k < n_src) v[i] = t.src[k];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = base + i * kCopyThreads;
+        if (k < n_src) {
+          t.dst[2 * k] = expand8(v[i].x, v[i].y);
+          t.dst[2 * k + 1] = expand8(v[i].z, v[i].w);
+        }
+      }
+    }
+    return;
+  }
   for (int base = threadIdx.x; base < n16; base += kCopyThreads * 8) {
     uint4 v[8];
 #pragma unroll
@@ -179,7 +225,9 @@ bool is_device(const void* p) {
 
 struct oomb_offload {
   oomb_offload_desc d;
-  size_t tile_bytes = 0;                 // P * D * element size
+  size_t tile_bytes = 0;                 // P * D * element size (cache; backing dK/dV)
+  size_t kv_tile_bytes = 0;              // P * D * element size of the backing K/V pools
+  int32_t expand = 0;                    // 1: backing K/V hold E4M3 codes
   std::vector<int32_t> host_pt;          // logical page -> host slot
   oomb::PageCacheDirectory* dir = nullptr;
   std::vector<oomb::TileMove> moves;     // the current call's plan
@@ -201,6 +249,11 @@ namespace {
 char* tile_ptr(void* pool, const oomb_offload* h, int slot, int g) {
   return static_cast<char*>(pool) +
          (static_cast<size_t>(slot) * h->d.num_kv_heads + g) * h->tile_bytes;
+}
+
+char* backing_kv_ptr(void* pool, const oomb_offload* h, int slot, int g) {
+  return static_cast<char*>(pool) +
+         (static_cast<size_t>(slot) * h->d.num_kv_heads + g) * h->kv_tile_bytes;
 }
 
 oomb_status take_stage(oomb_offload* h, Staging** out) {
@@ -259,9 +312,9 @@ cudaError_t enqueue_moves(oomb_offload* h, Staging& st, size_t n_wb, size_t n, c
     const size_t k = std::min(cap, n_wb - r0);
     for (size_t i = 0; i < k; ++i) {
       st.dev_tasks[r0 + i] = {st.tasks[r0 + i].src,
-                              reinterpret_cast<uint4*>(h->dev_staging + i * tb)};
+                              reinterpret_cast<uint4*>(h->dev_staging + i * tb), 0, 0};
       st.host_tasks[r0 + i] = {reinterpret_cast<const uint4*>(h->host_staging + i * tb),
-                               st.tasks[r0 + i].dst};
+                               st.tasks[r0 + i].dst, 0, 0};
     }
     cudaError_t e = launch_list(h, st.dev_tasks_dev + r0, k, s);
     if (e == cudaSuccess)
@@ -274,9 +327,9 @@ cudaError_t enqueue_moves(oomb_offload* h, Staging& st, size_t n_wb, size_t n, c
     const size_t k = std::min(cap, n - r0);
     for (size_t i = 0; i < k; ++i) {
       st.host_tasks[r0 + i] = {st.tasks[r0 + i].src,
-                               reinterpret_cast<uint4*>(h->host_staging + i * tb)};
+                               reinterpret_cast<uint4*>(h->host_staging + i * tb), 0, 0};
       st.dev_tasks[r0 + i] = {reinterpret_cast<const uint4*>(h->dev_staging + i * tb),
-                              st.tasks[r0 + i].dst};
+                              st.tasks[r0 + i].dst, 0, 0};
     }
     st.moves.push_back({h->pool, st.host_tasks.data() + r0, k, tb});
     cudaError_t e = cudaLaunchHostFunc(s, host_copy_cb, &st.moves.back());
@@ -297,25 +350,27 @@ size_t plan_to_tasks(oomb_offload* h, Staging& st) {
     switch (m.kind) {
       case oomb::TileMove::kWriteGrad:
         st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.cache_dk, h, m.slot, m.head)),
-                         reinterpret_cast<uint4*>(tile_ptr(d.dk, h, hs, m.head))};
+                         reinterpret_cast<uint4*>(tile_ptr(d.dk, h, hs, m.head)), 0, 0};
         st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.cache_dv, h, m.slot, m.head)),
-                         reinterpret_cast<uint4*>(tile_ptr(d.dv, h, hs, m.head))};
+                         reinterpret_cast<uint4*>(tile_ptr(d.dv, h, hs, m.head)), 0, 0};
         h->stats[1] += 2;
         h->stats[3] += 2 * static_cast<int64_t>(h->tile_bytes);
         break;
       case oomb::TileMove::kFetchKV:
-        st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.k, h, hs, m.head)),
-                         reinterpret_cast<uint4*>(tile_ptr(d.cache_k, h, m.slot, m.head))};
-        st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.v, h, hs, m.head)),
-                         reinterpret_cast<uint4*>(tile_ptr(d.cache_v, h, m.slot, m.head))};
+        st.tasks[n++] = {reinterpret_cast<const uint4*>(backing_kv_ptr(d.k, h, hs, m.head)),
+                         reinterpret_cast<uint4*>(tile_ptr(d.cache_k, h, m.slot, m.head)),
+                         h->expand, 0};
+        st.tasks[n++] = {reinterpret_cast<const uint4*>(backing_kv_ptr(d.v, h, hs, m.head)),
+                         reinterpret_cast<uint4*>(tile_ptr(d.cache_v, h, m.slot, m.head)),
+                         h->expand, 0};
         h->stats[0] += 2;
-        h->stats[2] += 2 * static_cast<int64_t>(h->tile_bytes);
+        h->stats[2] += 2 * static_cast<int64_t>(h->kv_tile_bytes);
         break;
       case oomb::TileMove::kFetchGrad:
         st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.dk, h, hs, m.head)),
-                         reinterpret_cast<uint4*>(tile_ptr(d.cache_dk, h, m.slot, m.head))};
+                         reinterpret_cast<uint4*>(tile_ptr(d.cache_dk, h, m.slot, m.head)), 0, 0};
         st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.dv, h, hs, m.head)),
-                         reinterpret_cast<uint4*>(tile_ptr(d.cache_dv, h, m.slot, m.head))};
+                         reinterpret_cast<uint4*>(tile_ptr(d.cache_dv, h, m.slot, m.head)), 0, 0};
         h->stats[0] += 2;
         h->stats[2] += 2 * static_cast<int64_t>(h->tile_bytes);
         break;
@@ -358,9 +413,17 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
     return oomb::report(OOMB_ERR_UNSUPPORTED, "num_kv_heads must be in [1, 32]");
   if (d->page_size <= 0 || d->head_dim <= 0)
     return oomb::report(OOMB_ERR_INVALID_ARG, "page_size and head_dim must be positive");
+  const bool fp8_kv = d->backing_kv_dtype == OOMB_FP8_E4M3;
+  if (d->backing_kv_dtype != d->dtype && !(fp8_kv && d->dtype == OOMB_BF16))
+    return oomb::report(OOMB_ERR_INVALID_ARG,
+                        "backing_kv_dtype %d: must equal dtype, or be FP8_E4M3 with BF16",
+                        static_cast<int>(d->backing_kv_dtype));
+  if (fp8_kv && d->dev_staging)
+    return oomb::report(OOMB_ERR_UNSUPPORTED, "fp8 K/V pools move by the zero-copy kernel only");
   const size_t elem = d->dtype == OOMB_BF16 ? 2 : 4;
   const size_t tile = static_cast<size_t>(d->page_size) * d->head_dim * elem;
-  if (tile % 16) return oomb::report(OOMB_ERR_UNSUPPORTED, "tile bytes must be a multiple of 16");
+  const size_t kv_tile = fp8_kv ? tile / 2 : tile;
+  if (kv_tile % 16) return oomb::report(OOMB_ERR_UNSUPPORTED, "tile bytes must be a multiple of 16");
   if (!d->k || !d->v || !d->cache_k || !d->cache_v || !d->host_page_table)
     return oomb::report(OOMB_ERR_INVALID_ARG, "k, v, cache_k, cache_v, host_page_table must be set");
   if ((d->dk == nullptr) != (d->cache_dk == nullptr) || (d->dv == nullptr) != (d->cache_dv == nullptr) ||
@@ -369,10 +432,13 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
   const void* host_pools[4] = {d->k, d->v, d->dk, d->dv};
   const void* dev_pools[4] = {d->cache_k, d->cache_v, d->cache_dk, d->cache_dv};
   for (int i = 0; i < 4; ++i) {
-    if (host_pools[i] && (!is_host_pinned(host_pools[i]) ||
-                          reinterpret_cast<uintptr_t>(host_pools[i]) % 16))
+    // the staged path gathers on the host: its backing pools must be host memory
+    if (host_pools[i] &&
+        (!(is_host_pinned(host_pools[i]) || (!d->dev_staging && is_device(host_pools[i]))) ||
+         reinterpret_cast<uintptr_t>(host_pools[i]) % 16))
       return oomb::report(OOMB_ERR_INVALID_ARG,
-                          "host pool %d must be pinned host memory, 16-byte aligned", i);
+                          "backing pool %d must be pinned host memory (or device memory "
+                          "without dev_staging), 16-byte aligned", i);
     if (dev_pools[i] && (!is_device(dev_pools[i]) ||
                          reinterpret_cast<uintptr_t>(dev_pools[i]) % 16))
       return oomb::report(OOMB_ERR_INVALID_ARG,
@@ -387,6 +453,8 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
   if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "out of host memory");
   h->d = *d;
   h->tile_bytes = tile;
+  h->kv_tile_bytes = kv_tile;
+  h->expand = fp8_kv ? 1 : 0;
   h->host_pt.assign(d->host_page_table, d->host_page_table + d->num_pages);
   {
     std::vector<char> seen(d->num_host_slots, 0);

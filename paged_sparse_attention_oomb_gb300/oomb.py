@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "liboomb.so")
 
 OOMB_OK, OOMB_ERR_INVALID_ARG, OOMB_ERR_UNSUPPORTED = 0, 1, 2
 OOMB_ERR_CUDA, OOMB_ERR_TIMEOUT, OOMB_ERR_DEVICE_BOUNDS = 3, 4, 5
-OOMB_BF16, OOMB_FP32 = 0, 1
+OOMB_BF16, OOMB_FP32, OOMB_FP8_E4M3 = 0, 1, 2
 OOMB_OP_VALIDATE, OOMB_OP_PAGE_REPS, OOMB_OP_SELECT_TOPK = 0, 1, 2
 OOMB_OP_ATTN_FWD, OOMB_OP_ATTN_BWD = 3, 4
 
@@ -53,7 +53,7 @@ class OombOffloadDesc(ctypes.Structure):
                 ("cache_k", ctypes.c_void_p), ("cache_v", ctypes.c_void_p),
                 ("cache_dk", ctypes.c_void_p), ("cache_dv", ctypes.c_void_p),
                 ("cache_slots", ctypes.c_int32), ("dev_staging", ctypes.c_void_p),
-                ("dev_staging_bytes", ctypes.c_int64)]
+                ("dev_staging_bytes", ctypes.c_int64), ("backing_kv_dtype", ctypes.c_int32)]
 
 
 class OombPagedKV(ctypes.Structure):
@@ -141,7 +141,10 @@ class PagedKV:
 
     def struct(self) -> OombPagedKV:
         ns, hkv, p, d = self.k.shape
-        dt = OOMB_BF16 if self.k.dtype == torch.bfloat16 else OOMB_FP32
+        dt = {torch.bfloat16: OOMB_BF16, torch.float32: OOMB_FP32}.get(self.k.dtype)
+        if dt is None:
+            raise OombError(OOMB_ERR_UNSUPPORTED, f"pools of {self.k.dtype}: the kernels read bf16 "
+                            "or fp32 (fp8 K/V go behind an OffloadCache)")
         return OombPagedKV(self.k.data_ptr(), self.v.data_ptr(),
                            self.dk.data_ptr() if self.dk is not None else None,
                            self.dv.data_ptr() if self.dv is not None else None,
@@ -445,10 +448,13 @@ class OffloadCache:
     """A device cache of ``cache_slots`` page slots in front of host pools.
 
     host: a PagedKV whose k, v (and dk, dv) are pinned CPU tensors
-    ``[num_host_slots, Hkv, P, D]`` and whose page_table is a CPU int32 tensor
-    (logical page -> host slot).  The cache pools (and, with staging_bytes > 0,
-    the device staging buffer the moves go through) are allocated here on
-    ``device`` (torch); the library's handle holds only host state.
+    ``[num_host_slots, Hkv, P, D]`` -- or, without staging, device tensors (a
+    compact tier in HBM) -- and whose page_table is a CPU int32 tensor (logical
+    page -> host slot).  k and v may be ``torch.float8_e4m3fn`` (an fp8 KV
+    cache, expanded to bf16 tile by tile as it is fetched; dk/dv bf16).  The
+    cache pools (and, with staging_bytes > 0, the device staging buffer the
+    moves go through) are allocated here on ``device`` (torch); the library's
+    handle holds only host state.
     """
 
     def __init__(self, host: PagedKV, cache_slots: int, device="cuda", staging_bytes=0):
@@ -457,23 +463,26 @@ class OffloadCache:
         self.num_pages = host.page_table.numel()
         self.page_size, self.hkv, self.head_dim = p, hkv, d
         self.cache_slots = cache_slots
+        fp8 = host.k.dtype == torch.float8_e4m3fn
+        cdt = torch.bfloat16 if fp8 else host.k.dtype   # what the kernels compute on
         shape = (cache_slots, hkv, p, d)
-        self.ck = torch.empty(shape, dtype=host.k.dtype, device=device)
-        self.cv = torch.empty(shape, dtype=host.k.dtype, device=device)
+        self.ck = torch.empty(shape, dtype=cdt, device=device)
+        self.cv = torch.empty(shape, dtype=cdt, device=device)
         grads = host.dk is not None
-        self.cdk = torch.empty(shape, dtype=host.k.dtype, device=device) if grads else None
-        self.cdv = torch.empty(shape, dtype=host.k.dtype, device=device) if grads else None
+        self.cdk = torch.empty(shape, dtype=cdt, device=device) if grads else None
+        self.cdv = torch.empty(shape, dtype=cdt, device=device) if grads else None
         self._pt_host = host.page_table.to(torch.int32).contiguous()
         # staging_bytes > 0: moves through a device staging buffer and the copy
         # engines; 0: zero-copy copy kernel
         self.staging = (torch.empty(staging_bytes, dtype=torch.uint8, device=device)
                         if staging_bytes else None)
-        dt = OOMB_BF16 if host.k.dtype == torch.bfloat16 else OOMB_FP32
+        dt = OOMB_BF16 if cdt == torch.bfloat16 else OOMB_FP32
         ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
         desc = OombOffloadDesc(ptr(host.k), ptr(host.v), ptr(host.dk), ptr(host.dv),
                                self._pt_host.data_ptr(), self.num_pages, ns, p, hkv, d, dt,
                                ptr(self.ck), ptr(self.cv), ptr(self.cdk), ptr(self.cdv),
-                               cache_slots, ptr(self.staging), staging_bytes)
+                               cache_slots, ptr(self.staging), staging_bytes,
+                               OOMB_FP8_E4M3 if fp8 else dt)
         h = ctypes.c_void_p()
         _check(load().oomb_offload_create(ctypes.byref(desc), ctypes.byref(h)))
         self._h = h

@@ -72,6 +72,7 @@ def _fwd(lib, kv, q=FAKE, n_sel=0, hq=28, clen=256, cstart=3840, ws=FAKE, ws_byt
     (dict(page_size=48), 2, "page_size"),
     (dict(head_dim=64), 2, "head_dim"),
     (dict(dtype=7), 1, "dtype"),
+    (dict(dtype=oomb.OOMB_FP8_E4M3), 2, "storage format"),
     (dict(num_slots=0), 1, "num_slots"),
     (dict(num_kv_heads=0), 2, "num_kv_heads"),
     (dict(k=FAKE + 8), 1, "aligned"),
@@ -130,6 +131,15 @@ def test_offload_create_checks_memory_kinds(lib):
     d.cache_slots, d.dk = 2, a                     # dk without dv / cache grads
     rc = lib.oomb_offload_create(ctypes.byref(d), ctypes.byref(h))
     assert rc == oomb.OOMB_ERR_INVALID_ARG and "all set or all NULL" in oomb.oomb_last_error()
+    d.dk = None
+    # fp8 K/V pools: only in front of a bf16 cache, and only with zero-copy moves
+    d.backing_kv_dtype, d.dtype = oomb.OOMB_FP8_E4M3, oomb.OOMB_FP32
+    rc = lib.oomb_offload_create(ctypes.byref(d), ctypes.byref(h))
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "backing_kv_dtype" in oomb.oomb_last_error()
+    d.dtype, d.dev_staging, d.dev_staging_bytes = oomb.OOMB_BF16, a, 1 << 16
+    rc = lib.oomb_offload_create(ctypes.byref(d), ctypes.byref(h))
+    assert rc == oomb.OOMB_ERR_UNSUPPORTED and "zero-copy" in oomb.oomb_last_error()
+    assert not h.value
 
 
 def test_bwd_requires_grad_buffers(lib):

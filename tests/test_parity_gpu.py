@@ -428,6 +428,72 @@ def test_offload_ragged_sequence_matches_resident():
     cache.close()
 
 
+def _fp8_pools(x):
+    """E4M3 copies of the workload's K/V pools and their exact bf16 values."""
+    k8, v8 = x.k_pool.to(torch.float8_e4m3fn), x.v_pool.to(torch.float8_e4m3fn)
+    return k8, v8, k8.to(torch.bfloat16), v8.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("tier", ["host", "device"])
+def test_fp8_kv_offload_matches_widened_resident(tier):
+    """An fp8 KV cache: E4M3 K/V pools behind a bf16 device cache (pinned host
+    memory, or device memory as a compact tier), expanded tile by tile on each
+    fetch.  The chunk-recurrent pass gives bit-identical O, selections and
+    dK/dV to the resident pass on bf16 pools holding the same values, and the
+    same dQ up to the order of its fp32 atomic sums; K/V fetches move one byte
+    per element."""
+    wl, x, q_full, do_full, dk0, dv0 = _offload_case(26)
+    k8, v8, kw, vw = _fp8_pools(x)
+    kv = oomb.PagedKV(kw, vw, x.page_table, dk0.clone(), dv0.clone())
+    o_r, dq_r, sels_r = oomb.chunk_recurrent_pass(q_full, do_full, kv, 512, 3)
+    if tier == "host":
+        back = oomb.PagedKV(k8.cpu().pin_memory(), v8.cpu().pin_memory(), x.page_table.cpu(),
+                            dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
+    else:
+        back = oomb.PagedKV(k8.clone(), v8.clone(), x.page_table.cpu(), dk0.clone(), dv0.clone())
+    cache = oomb.OffloadCache(back, 28, DEV)
+    o_o, dq_o, sels_o = oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 512, 3)
+    torch.cuda.synchronize()
+    for a, b in zip(sels_r, sels_o):
+        assert torch.equal(a, b)
+    assert torch.equal(_bits(o_r), _bits(o_o))
+    a, b = dq_r.float(), dq_o.float()
+    assert float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(a)) < 1e-3
+    assert torch.equal(_bits(kv.dk.cpu()), _bits(back.dk.cpu()))
+    assert torch.equal(_bits(kv.dv.cpu()), _bits(back.dv.cpu()))
+    st = cache.stats()
+    tile = 64 * 128
+    assert st["slots_reused"] > 0
+    assert tile * st["tiles_in"] < st["bytes_in"] < 2 * tile * st["tiles_in"]   # 1 B (K/V), 2 B (grads)
+    cache.close()
+
+
+def test_fp8_kv_offload_vs_oracle():
+    """The fp8 KV cache against the oracle reading the E4M3 codes itself: the
+    chunk-recurrent pass (8 chunks, Top-3, a cache that reuses slots) gives the
+    oracle's selections, and O, dQ and dK/dV within the bf16 bounds."""
+    wl, x, q_full, do_full, _, _ = _offload_case(27)
+    k8, v8, _, _ = _fp8_pools(x)
+    back = oomb.PagedKV(k8.cpu().pin_memory(), v8.cpu().pin_memory(), x.page_table.cpu(),
+                        torch.zeros(x.k_pool.shape, dtype=torch.bfloat16).pin_memory(),
+                        torch.zeros(x.k_pool.shape, dtype=torch.bfloat16).pin_memory())
+    cache = oomb.OffloadCache(back, 28, DEV)
+    o_g, dq_g, sels = oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 512, 3)
+    torch.cuda.synchronize()
+    kp = oracle.fp8_e4m3_decode(k8.view(torch.uint8).cpu().numpy())
+    vp = oracle.fp8_e4m3_decode(v8.view(torch.uint8).cpu().numpy())
+    pt = to_numpy64(x.page_table)
+    o_o, dq_o, dk_o, dv_o, sels_o = oracle.chunk_recurrent_grads(
+        to_numpy64(q_full), kp, vp, pt, to_numpy64(do_full), 512, 64, 3)
+    for sg, so in zip(sels, sels_o):
+        assert sg.cpu().numpy().tolist() == so.tolist()
+    compare(o_g.float().cpu().numpy(), o_o, "bf16", "fp8 KV O")
+    compare(dq_g.float().cpu().numpy(), dq_o, "bf16", "fp8 KV dQ")
+    compare(to_numpy64(back.dk)[pt], dk_o, "bf16", "fp8 KV dK")
+    compare(to_numpy64(back.dv)[pt], dv_o, "bf16", "fp8 KV dV")
+    cache.close()
+
+
 def test_step_pipeline_matches_sequential_steps():
     """Three steps with host-resident inputs and outputs through StepPipeline
     (copies overlapped with the neighbouring steps' compute) give the same O,
