@@ -335,8 +335,9 @@ def run_ours(args, rank, world, dev):
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
-    per = {n: statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps))
-           for k, n in enumerate(names)}
+    samples = {n: [evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps)]
+               for k, n in enumerate(names)}
+    per = {n: statistics.mean(v) for n, v in samples.items()}
     ms = max_over_ranks(total_ms / args.steps, world, dev)
 
     # end to end through the public API with host buffers: per step the chunk's
@@ -405,6 +406,9 @@ def run_ours(args, rank, world, dev):
         "attn_bwd": {"ms": per["attn_bwd"], "TFLOP/s": bwd_flops / per["attn_bwd"] / 1e9,
                      "frac_bf16": bwd_flops / per["attn_bwd"] / 1e9 / peak_t},
     }
+    for n, v in samples.items():          # spread of the per-call times over the timed steps
+        kern[n]["ms_median"] = statistics.median(v)
+        kern[n]["ms_min"] = min(v)
     achieved = bwd_flops / per["attn_bwd"] / 1e9
     res = {
         "metric": METRIC,
