@@ -316,9 +316,20 @@ oomb_status oomb_offload_flush(oomb_offload *h, int32_t drop, void *stream);
  * final flush has less to move. */
 oomb_status oomb_offload_writeback(oomb_offload *h, int32_t first_page, int32_t n_pages,
                                    void *stream);
+/* Declares that the caller has set every tile of the host dK/dV pools to zero
+ * (the start of a new pass over the sequence).  The cache's gradient tiles are
+ * forgotten without being written back (their sums belonged to the previous
+ * pass); the K/V tiles stay cached.  From then on, until a gradient tile is
+ * written back again, an acquire that needs it fills the cache tile with zeros
+ * on the device instead of copying it over the link.  Host-only bookkeeping:
+ * nothing is enqueued, so the caller orders it after the kernels and moves of
+ * the previous pass (and after its own zeroing of the host pools).
+ * OOMB_ERR_INVALID_ARG without gradient pools. */
+oomb_status oomb_offload_zero_grads(oomb_offload *h);
 /* Counters since create: out[0] tiles copied host -> cache, out[1] tiles
  * written back, out[2] bytes host -> cache, out[3] bytes cache -> host,
- * out[4] acquires, out[5] slots reused. */
+ * out[4] acquires, out[5] slots reused, out[6] gradient tiles zero-filled on
+ * the device instead of copied.  out: int64_t[7]. */
 oomb_status oomb_offload_stats(const oomb_offload *h, int64_t *out);
 /* Frees the handle (waits for its staging buffers' last moves). */
 void oomb_offload_destroy(oomb_offload *h);

@@ -37,10 +37,16 @@
 
 namespace {
 
+enum CopyMode : int32_t {
+  kCopy = 0,        // dst = src
+  kExpand = 1,      // src holds E4M3 codes, dst receives their bf16 values
+  kZeroFill = 2,    // dst = 0 (src unused)
+};
+
 struct TileCopy {
   const uint4* src;
   uint4* dst;
-  int32_t expand;   // 1: src holds E4M3 codes, dst receives their bf16 values
+  int32_t mode;
   int32_t pad;
 };
 
@@ -66,13 +72,18 @@ __device__ __forceinline__ uint4 expand8(uint32_t w0, uint32_t w1) {   // 8 code
 // One CTA per tile of n16 16-byte words (of the destination): 8 loads in
 // flight per thread, then the stores.  Either side may be pinned host memory
 // (zero-copy) or device memory.  An expanding task reads n16 / 2 words of
-// codes and writes two words per word read.  128 threads: small enough (in
-// threads and registers) to share an SM with a forward-attention CTA.
+// codes and writes two words per word read; a zero fill only writes.  128
+// threads: small enough (in threads and registers) to share an SM with a
+// forward-attention CTA.
 constexpr int kCopyThreads = 128;
 __global__ void __launch_bounds__(kCopyThreads) tile_copy_kernel(
     const TileCopy* __restrict__ tasks, int n16) {
   const TileCopy t = tasks[blockIdx.x];
-  if (t.expand) {
+  if (t.mode == kZeroFill) {
+    for (int k = threadIdx.x; k < n16; k += kCopyThreads) t.dst[k] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  if (t.mode == kExpand) {
     const int n_src = n16 / 2;
     for (int base = threadIdx.x; base < n_src; base += kCopyThreads * 8) {
       uint4 v[8];
@@ -200,6 +211,7 @@ struct Staging {
   std::vector<HostMove> moves;
   int32_t* pt = nullptr;
   cudaEvent_t done = nullptr;
+  size_t n_zero = 0;                 // zero fills at the end of `tasks`
   bool used = false;
 };
 
@@ -227,7 +239,7 @@ struct oomb_offload {
   oomb_offload_desc d;
   size_t tile_bytes = 0;                 // P * D * element size (cache; backing dK/dV)
   size_t kv_tile_bytes = 0;              // P * D * element size of the backing K/V pools
-  int32_t expand = 0;                    // 1: backing K/V hold E4M3 codes
+  int32_t kv_mode = 0;                   // kExpand: backing K/V hold E4M3 codes
   std::vector<int32_t> host_pt;          // logical page -> host slot
   oomb::PageCacheDirectory* dir = nullptr;
   std::vector<oomb::TileMove> moves;     // the current call's plan
@@ -241,7 +253,7 @@ struct oomb_offload {
   cudaEvent_t last_done = nullptr;       // moves of the previous call (any stream)
   Staging stage[4];
   int next_stage = 0;
-  int64_t stats[6] = {0, 0, 0, 0, 0, 0};
+  int64_t stats[7] = {0, 0, 0, 0, 0, 0, 0};
 };
 
 namespace {
@@ -288,11 +300,13 @@ cudaError_t launch_list(const oomb_offload* h, const TileCopy* list, size_t n, c
 
 // Enqueue the planned moves st.tasks[0, n): write-backs [0, n_wb) (cache ->
 // host) before fetches [n_wb, n) (host -> cache, which may reuse a slot just
-// written back).  Zero-copy: the copy kernel reads or writes the host pools
-// directly.  Staged: per round of at most stage_tiles tiles, write-backs go
-// cache -> device staging (kernel) -> host staging (copy engine) -> host pools
-// (host callback), fetches the reverse way, so the bulk of the bytes crosses
-// the CPU-GPU link on a copy engine instead of occupying SMs.
+// written back), the last st.n_zero of which are zero fills of cache tiles.
+// Zero-copy: the copy kernel reads or writes the host pools directly.
+// Staged: per round of at most stage_tiles tiles, write-backs go cache ->
+// device staging (kernel) -> host staging (copy engine) -> host pools (host
+// callback), fetches the reverse way, so the bulk of the bytes crosses the
+// CPU-GPU link on a copy engine instead of occupying SMs; the zero fills,
+// which touch only the cache, follow as one kernel launch.
 cudaError_t enqueue_moves(oomb_offload* h, Staging& st, size_t n_wb, size_t n, cudaStream_t s) {
   if (h->stage_tiles == 0) {
     cudaError_t e = launch_list(h, st.tasks_dev, n_wb, s);
@@ -300,6 +314,8 @@ cudaError_t enqueue_moves(oomb_offload* h, Staging& st, size_t n_wb, size_t n, c
     return e;
   }
   if (n == 0) return cudaSuccess;
+  const size_t n_zero = st.n_zero;
+  n -= n_zero;
   if (h->last_done) {
     cudaError_t e = cudaStreamWaitEvent(s, h->last_done, 0);   // one set of staging buffers
     if (e != cudaSuccess) return e;
@@ -338,16 +354,19 @@ cudaError_t enqueue_moves(oomb_offload* h, Staging& st, size_t n_wb, size_t n, c
     if (e == cudaSuccess) e = launch_list(h, st.dev_tasks_dev + r0, k, s);
     if (e != cudaSuccess) return e;
   }
-  return cudaSuccess;
+  return launch_list(h, st.tasks_dev + n, n_zero, s);
 }
 
-// The copies of a plan's tile moves: two per move (K and V, or dK and dV).
+// The copies of a plan's tile moves: two per move (K and V, or dK and dV), in
+// the plan's order, then the zero fills (st.n_zero of them).
 size_t plan_to_tasks(oomb_offload* h, Staging& st) {
   const oomb_offload_desc& d = h->d;
   size_t n = 0;
   for (const oomb::TileMove& m : h->moves) {
     const int hs = h->host_pt[m.page];
     switch (m.kind) {
+      case oomb::TileMove::kZeroGrad:
+        break;                                     // below, after every copy
       case oomb::TileMove::kWriteGrad:
         st.tasks[n++] = {reinterpret_cast<const uint4*>(tile_ptr(d.cache_dk, h, m.slot, m.head)),
                          reinterpret_cast<uint4*>(tile_ptr(d.dk, h, hs, m.head)), 0, 0};
@@ -359,10 +378,10 @@ size_t plan_to_tasks(oomb_offload* h, Staging& st) {
       case oomb::TileMove::kFetchKV:
         st.tasks[n++] = {reinterpret_cast<const uint4*>(backing_kv_ptr(d.k, h, hs, m.head)),
                          reinterpret_cast<uint4*>(tile_ptr(d.cache_k, h, m.slot, m.head)),
-                         h->expand, 0};
+                         h->kv_mode, 0};
         st.tasks[n++] = {reinterpret_cast<const uint4*>(backing_kv_ptr(d.v, h, hs, m.head)),
                          reinterpret_cast<uint4*>(tile_ptr(d.cache_v, h, m.slot, m.head)),
-                         h->expand, 0};
+                         h->kv_mode, 0};
         h->stats[0] += 2;
         h->stats[2] += 2 * static_cast<int64_t>(h->kv_tile_bytes);
         break;
@@ -375,6 +394,16 @@ size_t plan_to_tasks(oomb_offload* h, Staging& st) {
         h->stats[2] += 2 * static_cast<int64_t>(h->tile_bytes);
         break;
     }
+  }
+  st.n_zero = 0;
+  for (const oomb::TileMove& m : h->moves) {
+    if (m.kind != oomb::TileMove::kZeroGrad) continue;
+    st.tasks[n++] = {nullptr, reinterpret_cast<uint4*>(tile_ptr(d.cache_dk, h, m.slot, m.head)),
+                     kZeroFill, 0};
+    st.tasks[n++] = {nullptr, reinterpret_cast<uint4*>(tile_ptr(d.cache_dv, h, m.slot, m.head)),
+                     kZeroFill, 0};
+    st.n_zero += 2;
+    h->stats[6] += 2;
   }
   return n;
 }
@@ -454,7 +483,7 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
   h->d = *d;
   h->tile_bytes = tile;
   h->kv_tile_bytes = kv_tile;
-  h->expand = fp8_kv ? 1 : 0;
+  h->kv_mode = fp8_kv ? kExpand : kCopy;
   h->host_pt.assign(d->host_page_table, d->host_page_table + d->num_pages);
   {
     std::vector<char> seen(d->num_host_slots, 0);
@@ -573,9 +602,16 @@ oomb_status oomb_offload_writeback(oomb_offload* h, int32_t first_page, int32_t 
                      "offload writeback");
 }
 
+oomb_status oomb_offload_zero_grads(oomb_offload* h) {
+  if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "handle");
+  if (!h->d.dk) return oomb::report(OOMB_ERR_INVALID_ARG, "the cache has no gradient pools");
+  h->dir->declare_host_grads_zero();
+  return OOMB_OK;
+}
+
 oomb_status oomb_offload_stats(const oomb_offload* h, int64_t* out) {
   if (!h || !out) return oomb::report(OOMB_ERR_INVALID_ARG, "handle and out");
-  for (int i = 0; i < 6; ++i) out[i] = h->stats[i];
+  for (int i = 0; i < 7; ++i) out[i] = h->stats[i];
   return OOMB_OK;
 }
 

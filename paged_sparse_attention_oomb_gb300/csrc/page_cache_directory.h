@@ -1,9 +1,11 @@
 // Directory of the device page cache that sits in front of host-tier page
 // pools (the calls oomb_offload_* in include/oomb.h): which logical page each
 // cache slot holds, which KV heads of it have their K/V tiles and their
-// gradient tiles loaded, which gradient tiles are modified, and when each slot
-// was last used.  Pure host logic without CUDA, shared by the offload calls
-// and compiled on its own by the tests.
+// gradient tiles loaded, which gradient tiles are modified, when each slot
+// was last used, and which gradient tiles of the host pools are known to be
+// zero (so that bringing one in is a fill on the device, not a copy).  Pure
+// host logic without CUDA, shared by the offload calls and compiled on its
+// own by the tests.
 // Method: "Out of the Memory Barrier" technical summary, section 2, the fourth
 // optimisation ("Async CPU offloading"): only the pages a chunk attends need
 // to be on the GPU.
@@ -20,8 +22,10 @@ namespace oomb {
 
 // One tile move of a plan: (page, KV head) between the host pools and cache
 // slot `slot`.  A write-back carries the page the slot held before.
+// kZeroGrad: the host gradient tiles are zero; the cache tiles are filled
+// with zeros instead of being copied.
 struct TileMove {
-  enum Kind : uint8_t { kFetchKV = 0, kFetchGrad = 1, kWriteGrad = 2 };
+  enum Kind : uint8_t { kFetchKV = 0, kFetchGrad = 1, kWriteGrad = 2, kZeroGrad = 3 };
   int32_t page;
   int32_t slot;
   int32_t head;
@@ -34,7 +38,8 @@ class PageCacheDirectory {
       : num_pages_(num_pages), slots_(slots), heads_(heads),
         all_heads_(heads >= 32 ? 0xFFFFFFFFu : ((1u << heads) - 1u)),
         slot_of_page_(num_pages, -1), page_of_slot_(slots, -1), kv_valid_(slots, 0),
-        g_valid_(slots, 0), dirty_(slots, 0), last_use_(slots, 0), need_(num_pages, 0) {}
+        g_valid_(slots, 0), dirty_(slots, 0), last_use_(slots, 0), need_(num_pages, 0),
+        host_zero_(num_pages, 0) {}
 
   // Plans one acquire: the tiles the chunk's kernels read are (sel[g][i], g)
   // for every KV head g and i < n_sel (sel is [heads][n_sel]) and every head of
@@ -42,9 +47,10 @@ class PageCacheDirectory {
   // take free slots, then the least recently used slots not used by this
   // acquire or the previous one.  Appends to `moves` the gradient write-backs
   // of the reused slots (*n_writeback of them, first), then the fetches of the
-  // missing K/V tiles and, with `with_grads`, of the missing gradient tiles,
-  // which are then marked modified.  Returns "" on success, else a message
-  // and leaves the directory unchanged.
+  // missing K/V tiles and, with `with_grads`, of the missing gradient tiles
+  // (zero fills for those whose host tiles are known to be zero), which are
+  // then marked modified.  Returns "" on success, else a message and leaves
+  // the directory unchanged.
   std::string plan(const int32_t* sel, int n_sel, int own0, int own1, bool with_grads,
                    std::vector<TileMove>* moves, size_t* n_writeback, int64_t* reused) {
     std::vector<int32_t> pages;
@@ -121,7 +127,9 @@ class PageCacheDirectory {
       const uint32_t g_miss = with_grads ? (m & ~g_valid_[s]) : 0u;
       for (int g = 0; g < heads_; ++g) {
         if (kv_miss >> g & 1u) moves->push_back({l, s, g, TileMove::kFetchKV});
-        if (g_miss >> g & 1u) moves->push_back({l, s, g, TileMove::kFetchGrad});
+        if (g_miss >> g & 1u)
+          moves->push_back({l, s, g, (host_zero_[l] >> g & 1u) ? TileMove::kZeroGrad
+                                                                : TileMove::kFetchGrad});
       }
       kv_valid_[s] |= m;
       if (with_grads) {
@@ -146,6 +154,15 @@ class PageCacheDirectory {
     }
   }
 
+  // The caller has set every gradient tile of the host pools to zero (a new
+  // pass): the cached gradient tiles are forgotten without being written
+  // back, and until a tile is written back again, bringing it in is a zero
+  // fill.  The K/V tiles stay cached.
+  void declare_host_grads_zero() {
+    for (int l = 0; l < num_pages_; ++l) host_zero_[l] = all_heads_;
+    for (int s = 0; s < slots_; ++s) g_valid_[s] = dirty_[s] = 0;
+  }
+
   // Forgets every cached tile (after their write-backs have been collected).
   void drop() {
     for (int s = 0; s < slots_; ++s) {
@@ -163,11 +180,13 @@ class PageCacheDirectory {
   const std::vector<int32_t>& slot_of_page() const { return slot_of_page_; }
   int page_of_slot(int s) const { return page_of_slot_[s]; }
   uint32_t dirty(int s) const { return dirty_[s]; }
+  uint32_t host_zero(int l) const { return host_zero_[l]; }
 
  private:
   void add_writebacks(int s, std::vector<TileMove>* moves) {
     for (int g = 0; g < heads_; ++g)
       if (dirty_[s] >> g & 1u) moves->push_back({page_of_slot_[s], s, g, TileMove::kWriteGrad});
+    host_zero_[page_of_slot_[s]] &= ~dirty_[s];   // the host tiles now hold sums
     dirty_[s] = 0;
   }
   template <typename... A>
@@ -183,6 +202,7 @@ class PageCacheDirectory {
   std::vector<uint32_t> kv_valid_, g_valid_, dirty_;
   std::vector<uint64_t> last_use_;
   std::vector<uint32_t> need_;
+  std::vector<uint32_t> host_zero_;   // per page: heads whose host gradient tiles are zero
   uint64_t epoch_ = 0;
 };
 

@@ -28,7 +28,7 @@ EXPORTED = [
     "oomb_page_reps", "oomb_select_topk", "oomb_select_topk_noalloc", "oomb_sparse_attn_fwd",
     "oomb_sparse_attn_fwd_own_reps", "oomb_sparse_attn_bwd",
     "oomb_offload_create", "oomb_offload_acquire", "oomb_offload_flush", "oomb_offload_writeback",
-    "oomb_offload_stats", "oomb_offload_destroy",
+    "oomb_offload_stats", "oomb_offload_destroy", "oomb_offload_zero_grads",
     "oomb_device_status", "oomb_set_wait_limit_ns", "oomb_debug_wait_unset_flag",
     "oomb_status_string", "oomb_last_error",
 ]
@@ -96,6 +96,7 @@ def load():
         "oomb_offload_flush": (ctypes.c_int, [vp, i32, vp]),
         "oomb_offload_writeback": (ctypes.c_int, [vp, i32, i32, vp]),
         "oomb_offload_stats": (ctypes.c_int, [vp, vp]),
+        "oomb_offload_zero_grads": (ctypes.c_int, [vp]),
         "oomb_offload_destroy": (None, [vp]),
         "oomb_device_status": (ctypes.c_int, [vp, vp, vp]),
         "oomb_set_wait_limit_ns": (None, [ctypes.c_uint64]),
@@ -509,10 +510,17 @@ class OffloadCache:
         """Write the modified gradient tiles of these pages back now."""
         _check(load().oomb_offload_writeback(self._h, first_page, n_pages, _stream(stream)))
 
+    def zero_grads(self):
+        """Declare the host dK/dV pools zeroed (a new pass): the cached gradient
+        tiles are dropped, and tiles still zero on the host are brought in as
+        zero fills on the device instead of copies."""
+        _check(load().oomb_offload_zero_grads(self._h))
+
     def stats(self) -> dict:
-        out = (ctypes.c_int64 * 6)()
+        out = (ctypes.c_int64 * 7)()
         _check(load().oomb_offload_stats(self._h, out))
-        keys = ["tiles_in", "tiles_out", "bytes_in", "bytes_out", "acquires", "slots_reused"]
+        keys = ["tiles_in", "tiles_out", "bytes_in", "bytes_out", "acquires", "slots_reused",
+                "tiles_zero_filled"]
         return dict(zip(keys, list(out)))
 
     def close(self):

@@ -1,6 +1,7 @@
 // Host-logic checks of the device page cache's directory (no GPU): slot
 // assignment, reuse order, protection of the slots of the previous acquire,
-// write-back of modified gradient tiles, per-KV-head tile masks, refusals.
+// write-back of modified gradient tiles, per-KV-head tile masks, refusals,
+// zero fills of gradient tiles known to be zero on the host.
 // Built and run by tests/test_page_cache_directory.py.
 #include <cstdio>
 #include <cstdlib>
@@ -121,6 +122,46 @@ int main() {
     CHECK(d.plan(ok, 1, 6, 8, false, &m, &nwb, &reused).empty());
     // page 1 for both heads: one slot, both heads' tiles
     CHECK(m.size() == 6 && has(m, 1, 0, 0, TileMove::kFetchKV) && has(m, 1, 0, 1, TileMove::kFetchKV));
+  }
+  // 9. Host gradients declared zero: gradient tiles come in as zero fills
+  //    (K/V tiles stay cached and move nothing) until a write-back puts sums
+  //    into the host tile, after which bringing it in is a copy again.
+  {
+    PageCacheDirectory d(16, 8, 2);
+    std::vector<TileMove> m;
+    size_t nwb = 0;
+    int64_t reused = 0;
+    const int32_t sel[2] = {1, 2};               // A: pages 1, 2, 8, 9 -> slots 0..3
+    CHECK(d.plan(sel, 1, 8, 10, true, &m, &nwb, &reused).empty());
+    CHECK(count(m, TileMove::kFetchGrad) == 6 && count(m, TileMove::kZeroGrad) == 0);
+    d.declare_host_grads_zero();
+    CHECK(d.dirty(0) == 0u && d.dirty(2) == 0u && d.host_zero(1) == 3u);
+    m.clear();                                   // B: the same chunk again
+    CHECK(d.plan(sel, 1, 8, 10, true, &m, &nwb, &reused).empty());
+    CHECK(m.size() == 6 && count(m, TileMove::kZeroGrad) == 6);   // no K/V moves
+    CHECK(has(m, 1, 0, 0, TileMove::kZeroGrad) && has(m, 9, 3, 1, TileMove::kZeroGrad));
+    CHECK(d.dirty(0) == 1u && d.dirty(2) == 3u);
+    m.clear();                                   // the own pages go home: sums on the host
+    d.collect_writebacks(8, 2, &m);
+    CHECK(count(m, TileMove::kWriteGrad) == 4);
+    CHECK(d.host_zero(8) == 0u && d.host_zero(9) == 0u && d.host_zero(1) == 3u);
+    m.clear();                                   // C: pages 3, 4, 5 -> free slots 4, 5, 6
+    const int32_t sel_c[2] = {3, 3};
+    CHECK(d.plan(sel_c, 1, 4, 6, true, &m, &nwb, &reused).empty());
+    CHECK(count(m, TileMove::kZeroGrad) == 6 && count(m, TileMove::kFetchGrad) == 0);
+    m.clear();                                   // D: 12 -> free slot 7, 13 -> slot 0 (page 1 out)
+    const int32_t sel_d[2] = {3, 2};
+    CHECK(d.plan(sel_d, 1, 12, 14, true, &m, &nwb, &reused).empty());
+    CHECK(nwb == 1 && has(m, 1, 0, 0, TileMove::kWriteGrad));
+    CHECK(d.slot_of_page()[12] == 7 && d.slot_of_page()[13] == 0 && d.slot_of_page()[1] == -1);
+    CHECK(has(m, 13, 0, 0, TileMove::kZeroGrad) && has(m, 12, 7, 1, TileMove::kZeroGrad));
+    CHECK(d.host_zero(1) == 2u);                 // head 0 of page 1 now holds sums
+    m.clear();                                   // E: page 1 back: head 0 copied, head 1 filled
+    const int32_t sel_e[2] = {1, 1};
+    CHECK(d.plan(sel_e, 1, 14, 16, true, &m, &nwb, &reused).empty());
+    const int s1 = d.slot_of_page()[1];
+    CHECK(s1 >= 0 && has(m, 1, s1, 0, TileMove::kFetchGrad) && has(m, 1, s1, 1, TileMove::kZeroGrad));
+    CHECK(has(m, 8, d.slot_of_page()[8], 0, TileMove::kWriteGrad) == false);   // 8 was clean
   }
   if (g_fail == 0) std::printf("ok\n");
   return g_fail == 0 ? 0 : 1;

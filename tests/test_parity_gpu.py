@@ -428,6 +428,38 @@ def test_offload_ragged_sequence_matches_resident():
     cache.close()
 
 
+def test_offload_zero_grads_new_pass_matches_resident():
+    """Two offloaded passes over the same sequence: the first accumulates into
+    nonzero host gradients; then the host dK/dV are zeroed and declared zero
+    (a new pass), and the second pass -- whose first-touch gradient tiles are
+    zero fills on the device, not copies -- ends with host dK/dV bit-identical
+    to a resident pass from zero gradients, and the same O."""
+    wl, x, q_full, do_full, dk0, dv0 = _offload_case(28)
+    kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, torch.zeros_like(dk0),
+                      torch.zeros_like(dv0))
+    o_r, _, sels_r = oomb.chunk_recurrent_pass(q_full, do_full, kv, 512, 3)
+    host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
+                        x.page_table.cpu(), dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
+    cache = oomb.OffloadCache(host, 28, DEV)
+    oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 512, 3)
+    torch.cuda.synchronize()
+    assert not torch.equal(_bits(host.dk), _bits(dk0.cpu()))      # the first pass wrote sums
+    host.dk.zero_()
+    host.dv.zero_()
+    cache.zero_grads()
+    before = cache.stats()
+    o_o, _, sels_o = oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 512, 3)
+    torch.cuda.synchronize()
+    after = cache.stats()
+    for a, b in zip(sels_r, sels_o):
+        assert torch.equal(a, b)
+    assert torch.equal(_bits(o_r), _bits(o_o))
+    assert torch.equal(_bits(kv.dk.cpu()), _bits(host.dk))
+    assert torch.equal(_bits(kv.dv.cpu()), _bits(host.dv))
+    assert after["tiles_zero_filled"] - before["tiles_zero_filled"] > 0
+    cache.close()
+
+
 def _fp8_pools(x):
     """E4M3 copies of the workload's K/V pools and their exact bf16 values."""
     k8, v8 = x.k_pool.to(torch.float8_e4m3fn), x.v_pool.to(torch.float8_e4m3fn)
