@@ -202,35 +202,37 @@ def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=3):
            "host_setup_s": setup_s,
            "what": "fwd in order + bwd in reverse, cold cache per pass; next chunk's tiles "
                    "fetched on a second stream"}
-    # a new pass: host gradients zeroed (untimed) and declared zero, so the
-    # first touch of a gradient tile is a fill on the device, not a copy
-    def fresh_pass():
-        host.dk.zero_()
-        host.dv.zero_()
-        cache.zero_grads()
-        cache.flush(drop=True)
-        torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    tot, z0 = 0.0, None
-    for i in range(passes + 1):                  # the first pass is a warm-up
-        fresh_pass()
-        if i == 1:
-            z0 = cache.stats()
-        e0.record()
-        oomb.chunk_recurrent_pass_offloaded(q, do, cache, c, wl.top_k, start=start, reps=reps)
-        e1.record()
-        torch.cuda.synchronize()
-        if i > 0:
-            tot += e0.elapsed_time(e1)
-    z1 = cache.stats()
-    ms_z = tot / passes
-    res["zero_grads"] = {
-        "ms_per_pass_offloaded": ms_z, "overhead": ms_z / ms_res - 1.0,
-        "bytes_in_per_pass": (z1["bytes_in"] - z0["bytes_in"]) / passes,
-        "bytes_out_per_pass": (z1["bytes_out"] - z0["bytes_out"]) / passes,
-        "tiles_zero_filled_per_pass": (z1["tiles_zero_filled"] - z0["tiles_zero_filled"]) / passes,
-        "what": "each pass starts a new pass: host dK/dV zeroed (untimed) and declared with "
-                "zero_grads(); gradient tiles still zero on the host are zero-filled in the cache"}
+    def new_passes(cch):
+        # each pass a new pass: host gradients zeroed (untimed) and declared
+        # zero, so the first touch of a gradient tile is a fill on the device
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot, z0 = 0.0, None
+        for i in range(passes + 1):              # the first pass is a warm-up
+            host.dk.zero_()
+            host.dv.zero_()
+            cch.zero_grads()
+            cch.flush(drop=True)
+            torch.cuda.synchronize()
+            if i == 1:
+                z0 = cch.stats()
+            e0.record()
+            oomb.chunk_recurrent_pass_offloaded(q, do, cch, c, wl.top_k, start=start, reps=reps)
+            e1.record()
+            torch.cuda.synchronize()
+            if i > 0:
+                tot += e0.elapsed_time(e1)
+        z1 = cch.stats()
+        ms_z = tot / passes
+        return {"ms_per_pass_offloaded": ms_z, "overhead": ms_z / ms_res - 1.0,
+                "bytes_in_per_pass": (z1["bytes_in"] - z0["bytes_in"]) / passes,
+                "bytes_out_per_pass": (z1["bytes_out"] - z0["bytes_out"]) / passes,
+                "tiles_zero_filled_per_pass":
+                    (z1["tiles_zero_filled"] - z0["tiles_zero_filled"]) / passes}
+
+    res["zero_grads"] = new_passes(cache)
+    res["zero_grads"]["what"] = ("each pass starts a new pass: host dK/dV zeroed (untimed) and "
+                                 "declared with zero_grads(); gradient tiles still zero on the "
+                                 "host are zero-filled in the cache")
     cache.close()
     # fp8 KV: E4M3 host K/V pools (half the bytes over the link), same gradients
     del host.k, host.v                  # the bf16 host K/V pools are not needed any more
@@ -257,6 +259,7 @@ def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=3):
                      "host_setup_s": setup8,
                      "what": "host K/V as E4M3 codes expanded to bf16 on fetch; overhead "
                              "against the resident bf16 pass above"}
+    res["fp8_kv"]["new_pass"] = new_passes(cache8)
     cache8.close()
     return res
 
