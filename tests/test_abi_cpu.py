@@ -114,6 +114,14 @@ def test_fwd_own_reps_checks_reps(lib, reps, msg):
     assert rc == oomb.OOMB_ERR_INVALID_ARG and msg in oomb.oomb_last_error()
 
 
+def test_offload_calls_refuse_a_null_handle(lib):
+    assert lib.oomb_offload_zero_grads(None) == oomb.OOMB_ERR_INVALID_ARG
+    assert lib.oomb_offload_flush(None, 0, None) == oomb.OOMB_ERR_INVALID_ARG
+    assert lib.oomb_offload_writeback(None, 0, 1, None) == oomb.OOMB_ERR_INVALID_ARG
+    out = (ctypes.c_int64 * 7)()
+    assert lib.oomb_offload_stats(None, out) == oomb.OOMB_ERR_INVALID_ARG
+
+
 def test_offload_create_checks_memory_kinds(lib):
     """The host pools must be pinned host memory and the cache pools device
     memory; a plain host buffer is refused before anything is allocated."""
