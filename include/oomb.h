@@ -54,7 +54,8 @@
  *     the rows of that page past chunk_start + chunk_len hold no token.  They
  *     are never attended and their dK/dV rows are left as they are, but the
  *     tensor-core kernels load them with the page and weight them by zero, so
- *     their K and V values must be finite (a zero-initialised pool is).
+ *     their K and V values must be finite (a zero-initialised pool is; in fp8
+ *     backing pools of an offload cache, codes other than the NaN codes).
  */
 #ifndef OOMB_H
 #define OOMB_H
