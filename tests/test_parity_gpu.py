@@ -428,7 +428,8 @@ def test_offload_ragged_sequence_matches_resident():
     cache.close()
 
 
-def test_offload_zero_grads_new_pass_matches_resident():
+@pytest.mark.parametrize("staging", [0, 5 * 64 * 128 * 2], ids=["zero_copy", "staging_5_tiles"])
+def test_offload_zero_grads_new_pass_matches_resident(staging):
     """Two offloaded passes over the same sequence: the first accumulates into
     nonzero host gradients; then the host dK/dV are zeroed and declared zero
     (a new pass), and the second pass -- whose first-touch gradient tiles are
@@ -440,7 +441,7 @@ def test_offload_zero_grads_new_pass_matches_resident():
     o_r, _, sels_r = oomb.chunk_recurrent_pass(q_full, do_full, kv, 512, 3)
     host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
                         x.page_table.cpu(), dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
-    cache = oomb.OffloadCache(host, 28, DEV)
+    cache = oomb.OffloadCache(host, 28, DEV, staging_bytes=staging)
     oomb.chunk_recurrent_pass_offloaded(q_full, do_full, cache, 512, 3)
     torch.cuda.synchronize()
     assert not torch.equal(_bits(host.dk), _bits(dk0.cpu()))      # the first pass wrote sums
