@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from paged_sparse_attention_oomb_gb300 import oomb
 
@@ -185,3 +186,15 @@ def test_noalloc_selection_refuses_oversized_shapes_on_the_host(lib):
     rc = lib.oomb_select_topk_noalloc(ctypes.c_void_p(FAKE), 28, 256, 4096, ctypes.c_void_p(FAKE),
                                       ctypes.byref(kv), 64, ctypes.c_void_p(FAKE), None, None)
     assert rc == oomb.OOMB_ERR_INVALID_ARG and "fixed scratch" in oomb.oomb_last_error()
+
+
+@pytest.mark.parametrize("t,chunk_len,start", [(48, 24, 0), (48, 16, 8), (80, 16, 0), (0, 16, 0)])
+def test_chunk_recurrent_pass_checks_its_chunks_on_the_host(t, chunk_len, start):
+    """Chunks must start on pages inside the cache (chunk_len and start multiples
+    of P, the sequence within the pages); refused before anything runs."""
+    pool = torch.zeros((4, 1, 16, 64))
+    kv = oomb.PagedKV(pool, pool, torch.arange(4, dtype=torch.int32))
+    q = torch.zeros((t, 2, 64))
+    with pytest.raises(oomb.OombError) as e:
+        oomb.chunk_recurrent_pass(q, q, kv, chunk_len, 1, start=start)
+    assert e.value.code == oomb.OOMB_ERR_INVALID_ARG
