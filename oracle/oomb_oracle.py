@@ -32,8 +32,10 @@ Parity pins (tests/test_oracle.py): every function here is pinned against
 something other than itself -- torch's CPU scaled-dot-product attention with
 autograd (dense equality), closed-form worked examples (tests/golden/),
 brute-force pair means, order invariants of the Top-K, rows of the softmax
-summing to one, central finite differences, and cross-chunk accumulation
-equal to the single-pass dense gradient.
+summing to one, central finite differences, cross-chunk accumulation equal to
+the single-pass dense gradient (also over sequences that end inside a page),
+closed forms of a partial page's representative, and the E4M3 decoding against
+hand-worked codes and torch's float8_e4m3fn conversion.
 """
 from __future__ import annotations
 
