@@ -316,6 +316,7 @@ def run_ours(args, rank, world, dev):
     reps = torch.empty((wl.num_pages, hkv, d), dtype=torch.float32, device=dev)
     sel = torch.empty((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
     o = torch.empty_like(x.q)
+    o_lo = oomb.o_residual_like(o)
     lse = torch.empty((hq, c), dtype=torch.float32, device=dev)
     dq = torch.empty_like(x.q)
     ws_r = oomb.workspace(oomb.OOMB_OP_PAGE_REPS, kv)
@@ -334,11 +335,12 @@ def run_ours(args, rank, world, dev):
         oomb.oomb_select_topk(q, wl.start, reps, kv, wl.top_k, sel, ws_s, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        oomb.oomb_sparse_attn_fwd(q, kv, sel, n_sel, wl.start, o, lse, ws_f, stream=stream)
+        oomb.oomb_sparse_attn_fwd(q, kv, sel, n_sel, wl.start, o, lse, ws_f, stream=stream,
+                                  o_lo=o_lo)
         if ev is not None:
             ev[3].record(stream)
         oomb.oomb_sparse_attn_bwd(q, o, dout, lse, kv, sel, n_sel, wl.start, dq, ws_b,
-                                  stream=stream)
+                                  stream=stream, o_lo=o_lo)
         if ev is not None:
             ev[4].record(stream)
 

@@ -39,7 +39,7 @@
  *                                   absent pages -1).  An entry a kernel reads
  *                                   out of range is recorded as
  *                                   OOMB_ERR_DEVICE_BOUNDS, never followed.
- *       q, o, dout, dq             [chunk_len][Hq][D]
+ *       q, o, o_lo, dout, dq       [chunk_len][Hq][D]
  *       lse                        float [Hq][chunk_len], natural log
  *       reps                       float [num_pages][Hkv][D], logical order
  *       sel                        int32 [Hkv][n_sel], ascending, unique
@@ -177,12 +177,19 @@ oomb_status oomb_select_topk_noalloc(const void *q, int32_t num_q_heads, int32_t
  *   o[t][h] = softmax_k(scale * q[t][h] . k) v,  lse[h][t] = log sum_k exp(...)
  * scale <= 0 selects 1/sqrt(D).  bf16: tcgen05 tensor cores, fp32
  * accumulation, o rounded once to bf16.  fp32: CUDA-core FMA.
+ * o_lo (optional, bf16 pools only; NULL to skip): [chunk_len][Hq][D] bf16,
+ * the rounding residual of o -- o_lo = bf16(o32 - o) where o32 is the fp32
+ * value that o rounds -- so that o + o_lo carries o32 to about 16 bits.
+ * Pass it to the backward: its row sums Delta = dout . o are subtracted from
+ * dP = dout . v_k, and in a row whose attention concentrates on one key the
+ * two nearly cancel, so the bf16 rounding of o alone (2^-9 relative) would
+ * leave an error of up to 2^-9 |Delta| in dS and in dQ.
  * sel must be the same array later passed to the backward (the backward
  * reuses the forward's choice). */
 oomb_status oomb_sparse_attn_fwd(const void *q, const oomb_paged_kv *kv, const int32_t *sel,
                                  int32_t n_sel, int32_t num_q_heads, int32_t chunk_len,
-                                 int32_t chunk_start, float scale, void *o, float *lse, void *ws,
-                                 size_t ws_bytes, void *stream);
+                                 int32_t chunk_start, float scale, void *o, void *o_lo,
+                                 float *lse, void *ws, size_t ws_bytes, void *stream);
 
 /* Step 3 with step 1 of the chunk's own pages fused in (Chunk-Recurrent
  * Training Framework: the pages a chunk writes become candidates for the
@@ -202,8 +209,9 @@ oomb_status oomb_sparse_attn_fwd(const void *q, const oomb_paged_kv *kv, const i
 oomb_status oomb_sparse_attn_fwd_own_reps(const void *q, const oomb_paged_kv *kv,
                                           const int32_t *sel, int32_t n_sel,
                                           int32_t num_q_heads, int32_t chunk_len,
-                                          int32_t chunk_start, float scale, void *o, float *lse,
-                                          float *reps, void *ws, size_t ws_bytes, void *stream);
+                                          int32_t chunk_start, float scale, void *o, void *o_lo,
+                                          float *lse, float *reps, void *ws, size_t ws_bytes,
+                                          void *stream);
 
 /* Step 4 -- sparse attention backward with in-place paged gradient
  * accumulation (Paged Memory Management: gradients of the KV cache are
@@ -215,11 +223,16 @@ oomb_status oomb_sparse_attn_fwd_own_reps(const void *q, const oomb_paged_kv *kv
  *   dV[slot]  += sum_{t,h in group} P dout                    (read-add-write)
  * for the slots of the selected and own pages only; each of those slots is
  * rounded once per call.  kv->dk and kv->dv must be set.
+ * o_lo: the forward's rounding residual of o (bf16 pools; may be NULL): with
+ * it, Delta = dout . (o + o_lo), the forward's fp32 output, instead of
+ * dout . o -- see oomb_sparse_attn_fwd for why the rows whose attention
+ * concentrates on one key need it.  fp32 pools: must be NULL.
  * ws: oomb_workspace_bytes(ATTN_BWD) (holds Delta and an fp32 dq accumulator). */
-oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *dout, const float *lse,
-                                 const oomb_paged_kv *kv, const int32_t *sel, int32_t n_sel,
-                                 int32_t num_q_heads, int32_t chunk_len, int32_t chunk_start,
-                                 float scale, void *dq, void *ws, size_t ws_bytes, void *stream);
+oomb_status oomb_sparse_attn_bwd(const void *q, const void *o, const void *o_lo,
+                                 const void *dout, const float *lse, const oomb_paged_kv *kv,
+                                 const int32_t *sel, int32_t n_sel, int32_t num_q_heads,
+                                 int32_t chunk_len, int32_t chunk_start, float scale, void *dq,
+                                 void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Host-tier pools with a device page cache (the method's fourth optimisation,

@@ -561,8 +561,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Delta[h][t] = dout[t][h] . o[t][h], lse2[h][t] = lse[h][t] * log2(e); on the
 // padding rows of the last query tile Delta = 0 and lse2 = +inf (so P = 0
-// there).  Also zeroes the fp32 dq accumulator.  Half a warp per (t, h) row.
+// there).  With the forward's residual o_lo, o is taken as o + o_lo (exact in
+// fp32): Delta is subtracted from dP = dout . v, which it nearly equals in a
+// row whose attention sits on one key, so the bf16 rounding of o would
+// otherwise reach dS.  Also zeroes the fp32 dq accumulator.  Half a warp per
+// (t, h) row.
 __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                const __nv_bfloat16* __restrict__ o_lo,
                                 const __nv_bfloat16* __restrict__ dout,
                                 const float* __restrict__ lse, int hq, int chunk_len,
                                 int padded_len, float* __restrict__ delta,
@@ -576,11 +581,16 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
   if (t < chunk_len) {
     const uint4 a = reinterpret_cast<const uint4*>(o + row * 128)[l16];
     const uint4 b = reinterpret_cast<const uint4*>(dout + row * 128)[l16];
+    const uint4 c = o_lo ? reinterpret_cast<const uint4*>(o_lo + row * 128)[l16]
+                         : make_uint4(0, 0, 0, 0);
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+    const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      s = fmaf(__uint_as_float(wa[i] << 16), __uint_as_float(wb[i] << 16), s);
-      s = fmaf(__uint_as_float(wa[i] & 0xFFFF0000u), __uint_as_float(wb[i] & 0xFFFF0000u), s);
+      const float o0 = __uint_as_float(wa[i] << 16) + __uint_as_float(wc[i] << 16);
+      const float o1 = __uint_as_float(wa[i] & 0xFFFF0000u) + __uint_as_float(wc[i] & 0xFFFF0000u);
+      s = fmaf(o0, __uint_as_float(wb[i] << 16), s);
+      s = fmaf(o1, __uint_as_float(wb[i] & 0xFFFF0000u), s);
     }
     float4* z = reinterpret_cast<float4*>(dq_acc + row * 128) + 2 * l16;
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -618,10 +628,11 @@ size_t bf16_bwd_ws_bytes(int hq, int chunk_len, int head_dim) {
          align_up(static_cast<size_t>(chunk_len) * hq * head_dim * 4, 256);
 }
 
-cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* dout,
-                                 const float* lse, const KvDesc& kv, const int32_t* sel,
-                                 int n_sel, int hq, int chunk_len, int chunk_start, float scale,
-                                 void* dq, void* ws, uint64_t wait_ns, cudaStream_t st) {
+cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* o_lo,
+                                 const void* dout, const float* lse, const KvDesc& kv,
+                                 const int32_t* sel, int n_sel, int hq, int chunk_len,
+                                 int chunk_start, float scale, void* dq, void* ws,
+                                 uint64_t wait_ns, cudaStream_t st) {
   const int n_qtiles = (chunk_len + 127) / 128;
   const int padded = n_qtiles * 128;
   char* w = static_cast<char*>(ws);
@@ -649,8 +660,8 @@ cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* dout,
   {
     const long rows16 = static_cast<long>(padded) * hq * 16;
     bwd_prep_kernel<<<static_cast<unsigned>((rows16 + 255) / 256), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, hq,
-        chunk_len, padded, delta, lse2, dq_acc);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(o_lo),
+        static_cast<const __nv_bfloat16*>(dout), lse, hq, chunk_len, padded, delta, lse2, dq_acc);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -675,12 +686,13 @@ cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* dout,
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = wait_ns;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_attn_bwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static PerDeviceOnce attr;
+  {
+    cudaError_t e = once_per_device(attr, [] {
+      return cudaFuncSetAttribute(sparse_attn_bwd_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int n_key_tiles = p.t_sel + n_qtiles;
   sparse_attn_bwd_kernel<<<n_key_tiles * kv.hkv, kThreads, kSmemBytes, st>>>(tq, tdo, tk, tv, p);

@@ -76,6 +76,7 @@ struct FwdParams {
   const int32_t* sel;
   const int32_t* pt;
   __nv_bfloat16* o;
+  __nv_bfloat16* o_lo;                 // rounding residual of o, or null
   float* lse;
   float* reps;                         // own-page representatives, or null
   int* status;
@@ -452,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = l + *slot(n_tiles & 1, ch ^ 1);
       const float inv = 1.f / lt;
       const bool row_ok = t < p.chunk_len;
-      uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<long>(t) * p.hq + h) * 128 + 64 * ch);
+      const long row_off = (static_cast<long>(t) * p.hq + h) * 128 + 64 * ch;
+      uint4* orow = reinterpret_cast<uint4*>(p.o + row_off);
+      uint4* lrow = p.o_lo ? reinterpret_cast<uint4*>(p.o_lo + row_off) : nullptr;
 #pragma unroll 1
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t rr[32];
@@ -460,12 +463,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(rr[8 * i]) * inv, __uint_as_float(rr[8 * i + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(rr[8 * i + 2]) * inv, __uint_as_float(rr[8 * i + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(rr[8 * i + 4]) * inv, __uint_as_float(rr[8 * i + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(rr[8 * i + 6]) * inv, __uint_as_float(rr[8 * i + 7]) * inv);
-            orow[c2 * 4 + i] = v;
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float a = __uint_as_float(rr[8 * i + 2 * k]) * inv;
+              const float b = __uint_as_float(rr[8 * i + 2 * k + 1]) * inv;
+              hi[k] = pack_bf16(a, b);
+              // what the rounding dropped (exact in fp32), itself rounded to bf16
+              lo[k] = pack_bf16(a - __uint_as_float(hi[k] << 16),
+                                b - __uint_as_float(hi[k] & 0xFFFF0000u));
+            }
+            orow[c2 * 4 + i] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            if (lrow) lrow[c2 * 4 + i] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
         }
       }
@@ -486,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t* sel, int n_sel,
                                  int hq, int chunk_len, int chunk_start, float scale, void* o,
-                                 float* lse, float* own_reps, int* status, uint64_t wait_ns,
-                                 cudaStream_t st) {
+                                 void* o_lo, float* lse, float* own_reps, int* status,
+                                 uint64_t wait_ns, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {128, static_cast<uint64_t>(hq), static_cast<uint64_t>(chunk_len)};
@@ -507,6 +516,7 @@ cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t*
   p.sel = sel;
   p.pt = kv.page_table;
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_lo = static_cast<__nv_bfloat16*>(o_lo);
   p.lse = lse;
   p.reps = own_reps;
   p.status = status;
@@ -521,12 +531,13 @@ cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t*
   p.t_sel = (n_sel * kv.page_size + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = wait_ns;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_attn_fwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static PerDeviceOnce attr;
+  {
+    cudaError_t e = once_per_device(attr, [] {
+      return cudaFuncSetAttribute(sparse_attn_fwd_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   sparse_attn_fwd_kernel<<<p.n_qtiles * hq, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   return cudaGetLastError();

@@ -634,13 +634,12 @@ cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, 
   e = cudaGetLastError();
   if (e != cudaSuccess || top_k == 0 || n_cand == 0) return e;
   const size_t ksm = n_cand <= kTopkSmemKeys ? static_cast<size_t>(n_cand) * 4 : 0;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTopkSmemKeys * 4);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attr;
+  e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kTopkSmemKeys * 4);
+  });
+  if (e != cudaSuccess) return e;
   topk_kernel<<<hkv, kTopkThreads, ksm, st>>>(scores, num_pages, n_cand, top_k, sel);
   return cudaGetLastError();
 }

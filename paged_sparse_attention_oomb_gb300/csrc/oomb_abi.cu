@@ -176,6 +176,7 @@ oomb_status oomb_validate_page_table_host(const int32_t* pt, int32_t num_pages,
 }
 
 oomb_status oomb_device_status(void* ws, void* stream, int32_t* info) {
+  OOMB_NVTX_RANGE("oomb_device_status");
   if (!ws) return fail(OOMB_ERR_INVALID_ARG, "ws is NULL");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int h[3] = {0, 0, 0};
@@ -198,6 +199,7 @@ oomb_status oomb_device_status(void* ws, void* stream, int32_t* info) {
 
 oomb_status oomb_validate_page_table(const oomb_paged_kv* kv, void* ws, size_t ws_bytes,
                                      void* stream) {
+  OOMB_NVTX_RANGE("oomb_validate_page_table");
   oomb_status s = check_kv(kv);
   if (s != OOMB_OK) return s;
   s = check_ws(ws, ws_bytes, oomb_workspace_bytes(OOMB_OP_VALIDATE, kv, 0, 0, 0));
@@ -221,6 +223,7 @@ oomb_status oomb_validate_page_table(const oomb_paged_kv* kv, void* ws, size_t w
 
 oomb_status oomb_page_reps(const oomb_paged_kv* kv, int32_t first_page, int32_t n_pages,
                            float* reps, void* ws, size_t ws_bytes, void* stream) {
+  OOMB_NVTX_RANGE("oomb_page_reps");
   oomb_status s = check_kv(kv);
   if (s != OOMB_OK) return s;
   if (!reps) return fail(OOMB_ERR_INVALID_ARG, "reps is NULL");
@@ -240,6 +243,7 @@ oomb_status oomb_select_topk(const void* q, int32_t num_q_heads, int32_t chunk_l
                              int32_t chunk_start, const float* reps, const oomb_paged_kv* kv,
                              int32_t top_k, int32_t* sel, float* scores_opt, void* ws,
                              size_t ws_bytes, void* stream) {
+  OOMB_NVTX_RANGE("oomb_select_topk");
   oomb_status s = check_kv(kv);
   if (s != OOMB_OK) return s;
   s = check_chunk(kv, num_q_heads, chunk_len, chunk_start);
@@ -267,6 +271,7 @@ oomb_status oomb_select_topk_noalloc(const void* q, int32_t num_q_heads, int32_t
                                      int32_t chunk_start, const float* reps,
                                      const oomb_paged_kv* kv, int32_t top_k, int32_t* sel,
                                      float* scores_opt, void* stream) {
+  OOMB_NVTX_RANGE("oomb_select_topk_noalloc");
   oomb_status s = check_kv(kv);
   if (s != OOMB_OK) return s;
   s = check_chunk(kv, num_q_heads, chunk_len, chunk_start);
@@ -298,15 +303,17 @@ oomb_status oomb_select_topk_noalloc(const void* q, int32_t num_q_heads, int32_t
 static oomb_status attn_fwd(const char* name, const void* q, const oomb_paged_kv* kv,
                             const int32_t* sel, int32_t n_sel, int32_t num_q_heads,
                             int32_t chunk_len, int32_t chunk_start, float scale, void* o,
-                            float* lse, float* own_reps, void* ws, size_t ws_bytes,
+                            void* o_lo, float* lse, float* own_reps, void* ws, size_t ws_bytes,
                             void* stream) {
   oomb_status s = check_kv(kv);
   if (s != OOMB_OK) return s;
   s = check_chunk(kv, num_q_heads, chunk_len, chunk_start);
   if (s != OOMB_OK) return s;
   if (!q || !o || !lse) return fail(OOMB_ERR_INVALID_ARG, "q, o and lse must be set");
-  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 16))
-    return fail(OOMB_ERR_INVALID_ARG, "q, o and lse must be 16-byte aligned");
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 16) || !aligned(o_lo, 16))
+    return fail(OOMB_ERR_INVALID_ARG, "q, o, o_lo and lse must be 16-byte aligned");
+  if (o_lo && kv->dtype != OOMB_BF16)
+    return fail(OOMB_ERR_INVALID_ARG, "o_lo is for bf16 pools (an fp32 o needs no residual)");
   const int n_cand = chunk_start / kv->page_size;
   if (n_sel < 0 || n_sel > n_cand)
     return fail(OOMB_ERR_INVALID_ARG, "n_sel %d outside [0, %d] (pages before the chunk)", n_sel,
@@ -319,7 +326,8 @@ static oomb_status attn_fwd(const char* name, const void* q, const oomb_paged_kv
   cudaError_t e;
   if (kv->dtype == OOMB_BF16) {
     e = oomb::launch_attn_fwd_bf16(q, desc(kv), sel, n_sel, num_q_heads, chunk_len, chunk_start,
-                                   sc, o, lse, own_reps, static_cast<int*>(ws), g_wait_ns, st);
+                                   sc, o, o_lo, lse, own_reps, static_cast<int*>(ws), g_wait_ns,
+                                   st);
   } else {
     e = oomb::launch_attn_fwd_fp32(static_cast<const float*>(q), desc(kv), sel, n_sel,
                                    num_q_heads, chunk_len, chunk_start, sc,
@@ -335,27 +343,32 @@ static oomb_status attn_fwd(const char* name, const void* q, const oomb_paged_kv
 
 oomb_status oomb_sparse_attn_fwd(const void* q, const oomb_paged_kv* kv, const int32_t* sel,
                                  int32_t n_sel, int32_t num_q_heads, int32_t chunk_len,
-                                 int32_t chunk_start, float scale, void* o, float* lse, void* ws,
-                                 size_t ws_bytes, void* stream) {
+                                 int32_t chunk_start, float scale, void* o, void* o_lo,
+                                 float* lse, void* ws, size_t ws_bytes, void* stream) {
+  OOMB_NVTX_RANGE("oomb_sparse_attn_fwd");
   return attn_fwd("oomb_sparse_attn_fwd", q, kv, sel, n_sel, num_q_heads, chunk_len, chunk_start,
-                  scale, o, lse, nullptr, ws, ws_bytes, stream);
+                  scale, o, o_lo, lse, nullptr, ws, ws_bytes, stream);
 }
 
 oomb_status oomb_sparse_attn_fwd_own_reps(const void* q, const oomb_paged_kv* kv,
                                           const int32_t* sel, int32_t n_sel,
                                           int32_t num_q_heads, int32_t chunk_len,
-                                          int32_t chunk_start, float scale, void* o, float* lse,
-                                          float* reps, void* ws, size_t ws_bytes, void* stream) {
+                                          int32_t chunk_start, float scale, void* o, void* o_lo,
+                                          float* lse, float* reps, void* ws, size_t ws_bytes,
+                                          void* stream) {
+  OOMB_NVTX_RANGE("oomb_sparse_attn_fwd_own_reps");
   if (!reps) return fail(OOMB_ERR_INVALID_ARG, "reps must be set");
   if (!aligned(reps, 16)) return fail(OOMB_ERR_INVALID_ARG, "reps must be 16-byte aligned");
   return attn_fwd("oomb_sparse_attn_fwd_own_reps", q, kv, sel, n_sel, num_q_heads, chunk_len,
-                  chunk_start, scale, o, lse, reps, ws, ws_bytes, stream);
+                  chunk_start, scale, o, o_lo, lse, reps, ws, ws_bytes, stream);
 }
 
-oomb_status oomb_sparse_attn_bwd(const void* q, const void* o, const void* dout, const float* lse,
-                                 const oomb_paged_kv* kv, const int32_t* sel, int32_t n_sel,
-                                 int32_t num_q_heads, int32_t chunk_len, int32_t chunk_start,
-                                 float scale, void* dq, void* ws, size_t ws_bytes, void* stream) {
+oomb_status oomb_sparse_attn_bwd(const void* q, const void* o, const void* o_lo,
+                                 const void* dout, const float* lse, const oomb_paged_kv* kv,
+                                 const int32_t* sel, int32_t n_sel, int32_t num_q_heads,
+                                 int32_t chunk_len, int32_t chunk_start, float scale, void* dq,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  OOMB_NVTX_RANGE("oomb_sparse_attn_bwd");
   oomb_status s = check_kv(kv);
   if (s != OOMB_OK) return s;
   s = check_chunk(kv, num_q_heads, chunk_len, chunk_start);
@@ -364,8 +377,10 @@ oomb_status oomb_sparse_attn_bwd(const void* q, const void* o, const void* dout,
   if (!q || !o || !dout || !lse || !dq)
     return fail(OOMB_ERR_INVALID_ARG, "q, o, dout, lse and dq must be set");
   if (!aligned(q, 16) || !aligned(o, 16) || !aligned(dout, 16) || !aligned(lse, 16) ||
-      !aligned(dq, 16))
-    return fail(OOMB_ERR_INVALID_ARG, "q, o, dout, lse and dq must be 16-byte aligned");
+      !aligned(dq, 16) || !aligned(o_lo, 16))
+    return fail(OOMB_ERR_INVALID_ARG, "q, o, o_lo, dout, lse and dq must be 16-byte aligned");
+  if (o_lo && kv->dtype != OOMB_BF16)
+    return fail(OOMB_ERR_INVALID_ARG, "o_lo is for bf16 pools (an fp32 o needs no residual)");
   const int n_cand = chunk_start / kv->page_size;
   if (n_sel < 0 || n_sel > n_cand)
     return fail(OOMB_ERR_INVALID_ARG, "n_sel %d outside [0, %d] (pages before the chunk)", n_sel,
@@ -378,8 +393,8 @@ oomb_status oomb_sparse_attn_bwd(const void* q, const void* o, const void* dout,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (kv->dtype == OOMB_BF16)
-    e = oomb::launch_attn_bwd_bf16(q, o, dout, lse, desc(kv), sel, n_sel, num_q_heads, chunk_len,
-                                   chunk_start, sc, dq, ws, g_wait_ns, st);
+    e = oomb::launch_attn_bwd_bf16(q, o, o_lo, dout, lse, desc(kv), sel, n_sel, num_q_heads,
+                                   chunk_len, chunk_start, sc, dq, ws, g_wait_ns, st);
   else
     e = oomb::launch_attn_bwd_fp32(static_cast<const float*>(q), static_cast<const float*>(o),
                                    static_cast<const float*>(dout), lse, desc(kv), sel, n_sel,

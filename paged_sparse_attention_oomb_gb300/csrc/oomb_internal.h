@@ -3,8 +3,11 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "oomb.h"
 
@@ -13,6 +16,18 @@ namespace oomb {
 // Records a host-side error message for oomb_last_error() and returns `s`
 // (defined in oomb_abi.cu).
 oomb_status report(oomb_status s, const char* fmt, ...);
+
+// An NVTX range named after the ABI call, open for the call's host-side work
+// (checks and launches), so that a profiler's timeline and launch list group
+// the kernels by the call that issued them.  Costs nothing unless a tool is
+// attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define OOMB_NVTX_RANGE(name) ::oomb::NvtxRange oomb_nvtx_range_(name)
 
 // Workspace: a 256-byte status block first.
 //   int[0] status code (0 = ok), int[1] where, int[2] block
@@ -23,6 +38,27 @@ constexpr int kTicketIdx = 16;
 constexpr int kDebugFlagIdx = 17;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Runs `fn` (a cudaFuncSetAttribute call) once per device.  Kernel attributes
+// belong to a device, so a process-wide flag would leave a second device
+// without them; the mutex keeps concurrent first calls from racing.
+struct PerDeviceOnce {
+  std::mutex mu;
+  uint64_t done[2] = {0, 0};            // one bit per device ordinal < 128
+};
+template <class F>
+cudaError_t once_per_device(PerDeviceOnce& once, F&& fn) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return fn();
+  std::lock_guard<std::mutex> lock(once.mu);
+  const uint64_t bit = 1ull << (dev & 63);
+  if (once.done[dev >> 6] & bit) return cudaSuccess;
+  e = fn();
+  if (e == cudaSuccess) once.done[dev >> 6] |= bit;
+  return e;
+}
 
 // Where-codes recorded with a device error (status int[1]).
 enum Where : int {
@@ -80,16 +116,19 @@ cudaError_t launch_attn_bwd_fp32(const float* q, const float* o, const float* do
 // --- k_attn_fwd_bf16.cu
 // own_reps: if not null, the representatives of the chunk's own pages are
 // also written there (rows of the logical pages, [num_pages][hkv][128]).
+// o_lo: if not null, the rounding residual of o (bf16(o32 - bf16(o32))).
 cudaError_t launch_attn_fwd_bf16(const void* q, const KvDesc& kv, const int32_t* sel, int n_sel,
                                  int hq, int chunk_len, int chunk_start, float scale, void* o,
-                                 float* lse, float* own_reps, int* status, uint64_t wait_ns,
-                                 cudaStream_t st);
+                                 void* o_lo, float* lse, float* own_reps, int* status,
+                                 uint64_t wait_ns, cudaStream_t st);
 
 // --- k_attn_bwd_bf16.cu
 size_t bf16_bwd_ws_bytes(int hq, int chunk_len, int head_dim);
-cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* dout,
-                                 const float* lse, const KvDesc& kv, const int32_t* sel,
-                                 int n_sel, int hq, int chunk_len, int chunk_start, float scale,
-                                 void* dq, void* ws, uint64_t wait_ns, cudaStream_t st);
+// o_lo: the forward's residual of o (or null): Delta = dout . (o + o_lo).
+cudaError_t launch_attn_bwd_bf16(const void* q, const void* o, const void* o_lo,
+                                 const void* dout, const float* lse, const KvDesc& kv,
+                                 const int32_t* sel, int n_sel, int hq, int chunk_len,
+                                 int chunk_start, float scale, void* dq, void* ws,
+                                 uint64_t wait_ns, cudaStream_t st);
 
 }  // namespace oomb

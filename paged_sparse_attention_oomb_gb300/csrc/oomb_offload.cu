@@ -285,13 +285,13 @@ cudaError_t launch_list(const oomb_offload* h, const TileCopy* list, size_t n, c
   if (n == 0) return cudaSuccess;
   // Same shared-memory carveout as the attention kernels, so that a copy CTA
   // can share an SM with one of theirs instead of waiting for the SM to drain.
-  static bool carveout_set = false;
-  if (!carveout_set) {
-    cudaError_t e = cudaFuncSetAttribute(tile_copy_kernel,
-                                         cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared);
+  static oomb::PerDeviceOnce carveout;
+  {
+    cudaError_t e = oomb::once_per_device(carveout, [] {
+      return cudaFuncSetAttribute(tile_copy_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared);
+    });
     if (e != cudaSuccess) return e;
-    carveout_set = true;
   }
   tile_copy_kernel<<<static_cast<unsigned>(n), kCopyThreads, 0, s>>>(
       list, static_cast<int>(h->tile_bytes / 16));
@@ -431,6 +431,7 @@ oomb_status finish_call(oomb_offload* h, Staging& st, size_t n_wb, size_t n, cud
 extern "C" {
 
 oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) {
+  OOMB_NVTX_RANGE("oomb_offload_create");
   if (!d || !out) return oomb::report(OOMB_ERR_INVALID_ARG, "desc and out must be set");
   *out = nullptr;
   if (d->dtype != OOMB_BF16 && d->dtype != OOMB_FP32)
@@ -544,6 +545,7 @@ oomb_status oomb_offload_create(const oomb_offload_desc* d, oomb_offload** out) 
 oomb_status oomb_offload_acquire(oomb_offload* h, const int32_t* sel_host, int32_t n_sel,
                                  int32_t chunk_start, int32_t chunk_len, int32_t with_grads,
                                  int32_t* page_table_dev, void* stream) {
+  OOMB_NVTX_RANGE("oomb_offload_acquire");
   if (!h || !page_table_dev) return oomb::report(OOMB_ERR_INVALID_ARG, "handle and page_table_dev");
   const oomb_offload_desc& d = h->d;
   const int P = d.page_size;
@@ -575,6 +577,7 @@ oomb_status oomb_offload_acquire(oomb_offload* h, const int32_t* sel_host, int32
 }
 
 oomb_status oomb_offload_flush(oomb_offload* h, int32_t drop, void* stream) {
+  OOMB_NVTX_RANGE("oomb_offload_flush");
   if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "handle");
   Staging* st = nullptr;
   oomb_status rs = take_stage(h, &st);
@@ -588,6 +591,7 @@ oomb_status oomb_offload_flush(oomb_offload* h, int32_t drop, void* stream) {
 
 oomb_status oomb_offload_writeback(oomb_offload* h, int32_t first_page, int32_t n_pages,
                                    void* stream) {
+  OOMB_NVTX_RANGE("oomb_offload_writeback");
   if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "handle");
   if (first_page < 0 || n_pages < 0 || first_page + n_pages > h->d.num_pages)
     return oomb::report(OOMB_ERR_INVALID_ARG, "pages [%d, %d) outside [0, %d)", first_page,

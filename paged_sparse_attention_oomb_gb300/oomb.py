@@ -85,10 +85,11 @@ def load():
         "oomb_select_topk": (ctypes.c_int, [vp, i32, i32, i32, vp, kvp, i32, vp, vp, vp, sz, vp]),
         "oomb_select_topk_noalloc": (ctypes.c_int, [vp, i32, i32, i32, vp, kvp, i32, vp, vp, vp]),
         "oomb_sparse_attn_fwd": (ctypes.c_int, [vp, kvp, vp, i32, i32, i32, i32, ctypes.c_float,
-                                                vp, vp, vp, sz, vp]),
+                                                vp, vp, vp, vp, sz, vp]),
         "oomb_sparse_attn_fwd_own_reps": (ctypes.c_int, [vp, kvp, vp, i32, i32, i32, i32,
-                                                         ctypes.c_float, vp, vp, vp, vp, sz, vp]),
-        "oomb_sparse_attn_bwd": (ctypes.c_int, [vp, vp, vp, vp, kvp, vp, i32, i32, i32, i32,
+                                                         ctypes.c_float, vp, vp, vp, vp, vp, sz,
+                                                         vp]),
+        "oomb_sparse_attn_bwd": (ctypes.c_int, [vp, vp, vp, vp, vp, kvp, vp, i32, i32, i32, i32,
                                                 ctypes.c_float, vp, vp, sz, vp]),
         "oomb_offload_create": (ctypes.c_int, [ctypes.POINTER(OombOffloadDesc),
                                                 ctypes.POINTER(ctypes.c_void_p)]),
@@ -201,32 +202,42 @@ def oomb_select_topk_noalloc(q, chunk_start, reps, kv: PagedKV, top_k, sel, scor
 
 
 def oomb_sparse_attn_fwd(q, kv: PagedKV, sel, n_sel, chunk_start, o, lse, ws, scale=0.0,
-                         stream=None):
+                         stream=None, o_lo=None):
+    """o_lo (bf16 pools, optional): receives the rounding residual of o, for
+    the backward's Delta (see oomb.h)."""
     s = kv.struct()
     c, hq, _ = q.shape
     _check(load().oomb_sparse_attn_fwd(_ptr(q), ctypes.byref(s), _ptr(sel), n_sel, hq, c,
-                                       chunk_start, float(scale), _ptr(o), _ptr(lse), _ptr(ws),
-                                       ws.numel(), _stream(stream)))
+                                       chunk_start, float(scale), _ptr(o), _ptr(o_lo), _ptr(lse),
+                                       _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def oomb_sparse_attn_fwd_own_reps(q, kv: PagedKV, sel, n_sel, chunk_start, o, lse, reps, ws,
-                                  scale=0.0, stream=None):
+                                  scale=0.0, stream=None, o_lo=None):
     """The forward plus the representatives of the chunk's own pages into ``reps``."""
     s = kv.struct()
     c, hq, _ = q.shape
     _check(load().oomb_sparse_attn_fwd_own_reps(_ptr(q), ctypes.byref(s), _ptr(sel), n_sel, hq,
-                                                c, chunk_start, float(scale), _ptr(o), _ptr(lse),
-                                                _ptr(reps), _ptr(ws), ws.numel(),
-                                                _stream(stream)))
+                                                c, chunk_start, float(scale), _ptr(o),
+                                                _ptr(o_lo), _ptr(lse), _ptr(reps), _ptr(ws),
+                                                ws.numel(), _stream(stream)))
 
 
 def oomb_sparse_attn_bwd(q, o, dout, lse, kv: PagedKV, sel, n_sel, chunk_start, dq, ws,
-                         scale=0.0, stream=None):
+                         scale=0.0, stream=None, o_lo=None):
+    """o_lo: the forward's residual of o (or None: Delta from o alone)."""
     s = kv.struct()
     c, hq, _ = q.shape
-    _check(load().oomb_sparse_attn_bwd(_ptr(q), _ptr(o), _ptr(dout), _ptr(lse), ctypes.byref(s),
-                                       _ptr(sel), n_sel, hq, c, chunk_start, float(scale),
-                                       _ptr(dq), _ptr(ws), ws.numel(), _stream(stream)))
+    _check(load().oomb_sparse_attn_bwd(_ptr(q), _ptr(o), _ptr(o_lo), _ptr(dout), _ptr(lse),
+                                       ctypes.byref(s), _ptr(sel), n_sel, hq, c, chunk_start,
+                                       float(scale), _ptr(dq), _ptr(ws), ws.numel(),
+                                       _stream(stream)))
+
+
+def o_residual_like(o: torch.Tensor) -> Optional[torch.Tensor]:
+    """A buffer for the forward's rounding residual of ``o`` (bf16 only; None
+    for fp32, whose o is not rounded)."""
+    return torch.empty_like(o) if o.dtype == torch.bfloat16 else None
 
 
 def oomb_device_status(ws: torch.Tensor, stream=None):
@@ -274,12 +285,14 @@ def sparse_attention_step(q, dout, kv: PagedKV, chunk_start, top_k, reps=None, s
     ws_s = workspace(OOMB_OP_SELECT_TOPK, kv, hq, c, top_k)
     oomb_select_topk(q, chunk_start, reps, kv, n_sel, sel, ws_s, stream=stream)
     o = torch.empty_like(q)
+    o_lo = o_residual_like(o)
     lse = torch.empty((hq, c), dtype=torch.float32, device=dev)
     ws_f = workspace(OOMB_OP_ATTN_FWD, kv, hq, c)
-    oomb_sparse_attn_fwd(q, kv, sel, n_sel, chunk_start, o, lse, ws_f, stream=stream)
+    oomb_sparse_attn_fwd(q, kv, sel, n_sel, chunk_start, o, lse, ws_f, stream=stream, o_lo=o_lo)
     dq = torch.empty_like(q)
     ws_b = workspace(OOMB_OP_ATTN_BWD, kv, hq, c)
-    oomb_sparse_attn_bwd(q, o, dout, lse, kv, sel, n_sel, chunk_start, dq, ws_b, stream=stream)
+    oomb_sparse_attn_bwd(q, o, dout, lse, kv, sel, n_sel, chunk_start, dq, ws_b, stream=stream,
+                         o_lo=o_lo)
     for w in (ws_r, ws_s, ws_f, ws_b):
         code, where, blk = oomb_device_status(w, stream)
         if code != OOMB_OK:
@@ -312,6 +325,7 @@ class StepPipeline:
         self.q = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
         self.do = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
         self.o = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
+        self.o_lo = [o_residual_like(o) for o in self.o]     # stays on the device
         self.dq = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
         self.lse = [torch.empty((num_q_heads, chunk_len), dtype=torch.float32, device=dev)
                     for _ in range(2)]
@@ -345,9 +359,10 @@ class StepPipeline:
         oomb_select_topk(self.q[b], self.chunk_start, self.reps, kv, self.top_k, self.sel,
                          self.ws_s, stream=st)
         oomb_sparse_attn_fwd(self.q[b], kv, self.sel, self.n_sel, self.chunk_start, self.o[b],
-                             self.lse[b], self.ws_f, self.scale, st)
+                             self.lse[b], self.ws_f, self.scale, st, o_lo=self.o_lo[b])
         oomb_sparse_attn_bwd(self.q[b], self.o[b], self.do[b], self.lse[b], kv, self.sel,
-                             self.n_sel, self.chunk_start, self.dq[b], self.ws_b, self.scale, st)
+                             self.n_sel, self.chunk_start, self.dq[b], self.ws_b, self.scale, st,
+                             o_lo=self.o_lo[b])
         done = torch.cuda.Event()
         done.record(self.comp)
         self.comp_done[b] = done
@@ -374,6 +389,10 @@ class StepPipeline:
             code, where, blk = oomb_device_status(w, self.comp)
             if code != OOMB_OK:
                 raise OombError(code, f"device status (where {where}, block {blk})")
+
+
+def _rows(t: Optional[torch.Tensor], r0, n):
+    return None if t is None else t[r0:r0 + n]
 
 
 def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale=0.0,
@@ -413,6 +432,7 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
     ws_f = workspace(OOMB_OP_ATTN_FWD, kv, hq, chunk_len)
     ws_b = workspace(OOMB_OP_ATTN_BWD, kv, hq, chunk_len)
     o_full = torch.empty_like(q_full)
+    o_lo_full = o_residual_like(o_full)
     dq_full = torch.empty_like(q_full)
     lses, sels = [], []
     n_chunks = -(-t // chunk_len)                 # the last chunk may be shorter
@@ -426,7 +446,7 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
             oomb_select_topk(q, t0, reps, kv, n_sel, sel, ws_s, stream=stream)
         lse = torch.empty((hq, q.shape[0]), dtype=torch.float32, device=dev)
         oomb_sparse_attn_fwd_own_reps(q, kv, sel, n_sel, t0, o_full[r0:r0 + chunk_len], lse, reps,
-                                      ws_f, scale, stream)
+                                      ws_f, scale, stream, o_lo=_rows(o_lo_full, r0, chunk_len))
         lses.append(lse)
         sels.append((sel, n_sel))
     for c in reversed(range(n_chunks)):
@@ -434,7 +454,8 @@ def chunk_recurrent_pass(q_full, dout_full, kv: PagedKV, chunk_len, top_k, scale
         sel, n_sel = sels[c]
         oomb_sparse_attn_bwd(q_full[r0:r0 + chunk_len], o_full[r0:r0 + chunk_len],
                              dout_full[r0:r0 + chunk_len], lses[c], kv, sel, n_sel, start + r0,
-                             dq_full[r0:r0 + chunk_len], ws_b, scale, stream)
+                             dq_full[r0:r0 + chunk_len], ws_b, scale, stream,
+                             o_lo=_rows(o_lo_full, r0, chunk_len))
     for w in (ws_s, ws_f, ws_b):
         code, where, blk = oomb_device_status(w, stream)
         if code != OOMB_OK:
@@ -580,6 +601,7 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     ws_f = workspace(OOMB_OP_ATTN_FWD, kv0, hq, chunk_len)
     ws_b = workspace(OOMB_OP_ATTN_BWD, kv0, hq, chunk_len)
     o_full = torch.empty_like(q_full)
+    o_lo_full = o_residual_like(o_full)
     dq_full = torch.empty_like(q_full)
     n_chunks = -(-t // chunk_len)                 # the last chunk may be shorter
     last = n_chunks - 1
@@ -631,7 +653,8 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
         sel, _, n_sel = sels[c]
         lses[c] = torch.empty((hq, length(c)), dtype=torch.float32, device=dev)
         oomb_sparse_attn_fwd(q_full[r0:r0 + chunk_len], cache.device_kv(pts[c % 2]), sel, n_sel,
-                             start + r0, o_full[r0:r0 + chunk_len], lses[c], ws_f, scale, comp)
+                             start + r0, o_full[r0:r0 + chunk_len], lses[c], ws_f, scale, comp,
+                             o_lo=_rows(o_lo_full, r0, chunk_len))
         done[c] = torch.cuda.Event()
         done[c].record(comp)
         if c + 1 < n_chunks:
@@ -653,7 +676,8 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
         pt = pt_last if c == last else pts[c % 2]
         oomb_sparse_attn_bwd(q_full[r0:r0 + chunk_len], o_full[r0:r0 + chunk_len],
                              dout_full[r0:r0 + chunk_len], lses[c], cache.device_kv(pt),
-                             sel, n_sel, start + r0, dq_full[r0:r0 + chunk_len], ws_b, scale, comp)
+                             sel, n_sel, start + r0, dq_full[r0:r0 + chunk_len], ws_b, scale, comp,
+                             o_lo=_rows(o_lo_full, r0, chunk_len))
         done[c] = torch.cuda.Event()
         done[c].record(comp)
         with torch.cuda.stream(copy):

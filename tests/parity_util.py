@@ -104,22 +104,25 @@ def gpu_select(x, kv, reps, top_k):
     return sel[:, :n_sel], scores
 
 
-def gpu_fwd(x, kv, sel_t, n_sel):
+def gpu_fwd(x, kv, sel_t, n_sel, with_lo=False):
+    """O and LSE (and, with ``with_lo``, the bf16 rounding residual of O that
+    the backward takes for its Delta)."""
     wl = x.wl
     o = torch.empty_like(x.q)
+    o_lo = oomb.o_residual_like(o)
     lse = torch.empty((wl.num_q_heads, wl.chunk_len), dtype=torch.float32, device=x.q.device)
     ws = oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv, wl.num_q_heads, wl.chunk_len)
-    oomb.oomb_sparse_attn_fwd(x.q, kv, sel_t, n_sel, wl.start, o, lse, ws)
+    oomb.oomb_sparse_attn_fwd(x.q, kv, sel_t, n_sel, wl.start, o, lse, ws, o_lo=o_lo)
     assert_status_ok(ws)
-    return o, lse
+    return (o, lse, o_lo) if with_lo else (o, lse)
 
 
-def gpu_bwd(x, kv, sel_t, n_sel, o, lse, dout=None):
+def gpu_bwd(x, kv, sel_t, n_sel, o, lse, dout=None, o_lo=None):
     wl = x.wl
     dq = torch.empty_like(x.q)
     ws = oomb.workspace(oomb.OOMB_OP_ATTN_BWD, kv, wl.num_q_heads, wl.chunk_len)
     oomb.oomb_sparse_attn_bwd(x.q, o, x.do if dout is None else dout, lse, kv, sel_t, n_sel,
-                              wl.start, dq, ws)
+                              wl.start, dq, ws, o_lo=o_lo)
     assert_status_ok(ws)
     return dq
 

@@ -63,9 +63,11 @@ def _kv(**kw):
     return oomb.OombPagedKV(**d)
 
 
-def _fwd(lib, kv, q=FAKE, n_sel=0, hq=28, clen=256, cstart=3840, ws=FAKE, ws_bytes=1 << 20):
+def _fwd(lib, kv, q=FAKE, n_sel=0, hq=28, clen=256, cstart=3840, ws=FAKE, ws_bytes=1 << 20,
+         o_lo=0):
     return lib.oomb_sparse_attn_fwd(ctypes.c_void_p(q), ctypes.byref(kv), ctypes.c_void_p(FAKE),
                                     n_sel, hq, clen, cstart, 0.0, ctypes.c_void_p(FAKE),
+                                    ctypes.c_void_p(o_lo) if o_lo else None,
                                     ctypes.c_void_p(FAKE), ctypes.c_void_p(ws), ws_bytes, None)
 
 
@@ -97,6 +99,7 @@ def test_bad_cache_rejected(lib, kw, code, msg):
     (dict(ws_bytes=16), "ws has"),
     (dict(ws=FAKE + 64), "256-byte"),
     (dict(q=FAKE + 4), "aligned"),
+    (dict(o_lo=FAKE + 8), "aligned"),
 ])
 def test_bad_call_rejected(lib, args, msg):
     rc = _fwd(lib, _kv(), **args)
@@ -109,7 +112,7 @@ def test_fwd_own_reps_checks_reps(lib, reps, msg):
     kv = _kv()
     rc = lib.oomb_sparse_attn_fwd_own_reps(ctypes.c_void_p(FAKE), ctypes.byref(kv),
                                            ctypes.c_void_p(FAKE), 8, 28, 256, 3840, 0.0,
-                                           ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                                           ctypes.c_void_p(FAKE), None, ctypes.c_void_p(FAKE),
                                            ctypes.c_void_p(reps) if reps else None,
                                            ctypes.c_void_p(FAKE), 1 << 30, None)
     assert rc == oomb.OOMB_ERR_INVALID_ARG and msg in oomb.oomb_last_error()
@@ -151,12 +154,29 @@ def test_offload_create_checks_memory_kinds(lib):
     assert not h.value
 
 
+def _bwd(lib, kv, o_lo=None):
+    return lib.oomb_sparse_attn_bwd(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                                    ctypes.c_void_p(o_lo) if o_lo else None,
+                                    *(ctypes.c_void_p(FAKE),) * 2, ctypes.byref(kv),
+                                    ctypes.c_void_p(FAKE), 0, 28, 256, 3840, 0.0,
+                                    ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1 << 30, None)
+
+
 def test_bwd_requires_grad_buffers(lib):
-    kv = _kv(dk=0)
-    rc = lib.oomb_sparse_attn_bwd(*(ctypes.c_void_p(FAKE),) * 4, ctypes.byref(kv),
-                                  ctypes.c_void_p(FAKE), 0, 28, 256, 3840, 0.0,
-                                  ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1 << 30, None)
+    rc = _bwd(lib, _kv(dk=0))
     assert rc == oomb.OOMB_ERR_INVALID_ARG and "dk" in oomb.oomb_last_error()
+
+
+def test_o_residual_checks(lib):
+    """The residual of O is a bf16 buffer: misaligned, or given with fp32
+    pools, it is refused on the host."""
+    rc = _bwd(lib, _kv(), o_lo=FAKE + 2)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "aligned" in oomb.oomb_last_error()
+    kv32 = _kv(head_dim=64, dtype=oomb.OOMB_FP32)
+    rc = _bwd(lib, kv32, o_lo=FAKE)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "o_lo" in oomb.oomb_last_error()
+    rc = _fwd(lib, kv32, o_lo=FAKE)
+    assert rc == oomb.OOMB_ERR_INVALID_ARG and "o_lo" in oomb.oomb_last_error()
 
 
 def test_select_rejects_bad_pages(lib):

@@ -4,7 +4,9 @@ must return exactly what oomb_select_topk returns with a caller workspace, on
 two calls in a row (the second one reuses the scratch the first one left).
 
 Kept in a file of its own that pytest collects last; it passes alone in a
-fresh process and after the other tests."""
+fresh process and after the other tests.  The refusal of shapes larger than
+the fixed scratch happens on the host before any CUDA call, so it is tested
+without a GPU (tests/test_abi_cpu.py)."""
 import pytest
 import torch
 
@@ -52,20 +54,3 @@ def test_noalloc_matches_workspace_call_twice(wl):
         assert torch.equal(sel, ref_sel)
         assert torch.equal(scores, ref_scores)
 
-
-def test_noalloc_refuses_shapes_beyond_its_scratch():
-    import ctypes
-    n_pages, p = 1 << 19, 16                  # scores alone: 4 heads x 2^19 pages x 4 B = 8 MiB
-    q = torch.zeros((4096, 28, 128), dtype=torch.bfloat16, device=DEV)
-    k = torch.zeros((1, 4, p, 128), dtype=torch.bfloat16, device=DEV)
-    kv = oomb.PagedKV(k, k, torch.zeros(1, dtype=torch.int32, device=DEV))
-    s = kv.struct()
-    s.num_pages = s.num_slots = n_pages       # shapes only: the call refuses before any launch
-    reps = torch.zeros(16, device=DEV)
-    sel = torch.zeros((4, 64), dtype=torch.int32, device=DEV)
-    rc = oomb.load().oomb_select_topk_noalloc(
-        ctypes.c_void_p(q.data_ptr()), 28, 4096, n_pages * p - 4096,
-        ctypes.c_void_p(reps.data_ptr()), ctypes.byref(s), 64, ctypes.c_void_p(sel.data_ptr()),
-        None, None)
-    assert rc == oomb.OOMB_ERR_INVALID_ARG
-    assert "fixed scratch" in oomb.oomb_last_error()
