@@ -297,10 +297,156 @@ def measure_chunk_pass(dev, peak_t, passes=3):
 
 
 # DRAM bytes (read + write) of one backward call -- bwd_prep_kernel +
-# sparse_attn_bwd_kernel + dq_convert_kernel -- from one ncu capture of the
-# current kernels (dram__bytes_read.sum + dram__bytes_write.sum, one pass).
-# Must be re-captured whenever those kernels change.
-BWD_DRAM_BYTES = {"qwen7b_ctx4m_k128": 2_147_636_224}
+# sparse_attn_bwd_kernel + dq_convert_kernel -- from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
+# SHA-256 of the backward's source files at the time of the capture: when the
+# sources differ the figure describes another kernel and the bench reports
+# the traffic as null.
+BWD_TRAFFIC = {}
+BWD_SOURCES = ["k_attn_bwd_bf16.cu", "sm100.cuh", "tmap.h"]
+
+
+def bwd_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in BWD_SOURCES:
+        with open(os.path.join(ROOT, "paged_sparse_attention_oomb_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+class PathStep:
+    """Buffers and workspaces of one step of the path on one workload: page
+    representatives of all pages -> Top-K selection -> forward -> backward
+    (dK/dV in place), the four C ABI calls, on the current stream."""
+    NAMES = ["page_reps", "select_topk", "attn_fwd", "attn_bwd"]
+    LAUNCHES = 1 + 3 + 1 + 3          # kernels per step: reps; qbar/scores/top-k; fwd; prep/bwd/convert
+
+    def __init__(self, wl, dev):
+        from paged_sparse_attention_oomb_gb300 import oomb
+        self.oomb, self.wl = oomb, wl
+        self.x = x = make_inputs(wl, seed=0, device=dev)
+        self.kv = kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, torch.zeros_like(x.k_pool),
+                                    torch.zeros_like(x.v_pool))
+        hkv, d, c, hq = wl.num_kv_heads, wl.head_dim, wl.chunk_len, wl.num_q_heads
+        self.reps = torch.empty((wl.num_pages, hkv, d), dtype=torch.float32, device=dev)
+        self.sel = torch.empty((hkv, max(wl.n_sel, 1)), dtype=torch.int32, device=dev)
+        self.o = torch.empty_like(x.q)
+        self.o_lo = oomb.o_residual_like(self.o)
+        self.lse = torch.empty((hq, c), dtype=torch.float32, device=dev)
+        self.dq = torch.empty_like(x.q)
+        self.ws = [oomb.workspace(oomb.OOMB_OP_PAGE_REPS, kv),
+                   oomb.workspace(oomb.OOMB_OP_SELECT_TOPK, kv, hq, c, wl.top_k),
+                   oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv, hq, c),
+                   oomb.workspace(oomb.OOMB_OP_ATTN_BWD, kv, hq, c)]
+        self.stream = torch.cuda.current_stream()
+
+    def __call__(self, ev=None):
+        oomb, wl, kv, st = self.oomb, self.wl, self.kv, self.stream
+        q, dout = self.x.q, self.x.do
+        ws_r, ws_s, ws_f, ws_b = self.ws
+        if ev is not None:
+            ev[0].record(st)
+        oomb.oomb_page_reps(kv, 0, wl.num_pages, self.reps, ws_r, st)
+        if ev is not None:
+            ev[1].record(st)
+        oomb.oomb_select_topk(q, wl.start, self.reps, kv, wl.top_k, self.sel, ws_s, stream=st)
+        if ev is not None:
+            ev[2].record(st)
+        oomb.oomb_sparse_attn_fwd(q, kv, self.sel, wl.n_sel, wl.start, self.o, self.lse, ws_f,
+                                  stream=st, o_lo=self.o_lo)
+        if ev is not None:
+            ev[3].record(st)
+        oomb.oomb_sparse_attn_bwd(q, self.o, dout, self.lse, kv, self.sel, wl.n_sel, wl.start,
+                                  self.dq, ws_b, stream=st, o_lo=self.o_lo)
+        if ev is not None:
+            ev[4].record(st)
+
+    def check_status(self):
+        for w in self.ws:
+            code, where, blk = self.oomb.oomb_device_status(w)
+            if code != 0:
+                raise RuntimeError(f"device status {self.oomb.oomb_status_string(code)} "
+                                   f"at {where}/{blk}")
+
+    def time(self, steps):
+        """Per-call CUDA events over `steps` steps on the launching stream;
+        returns (total ms, {call: [ms per step]})."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        for i in range(steps):
+            self(evs[i])
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        per = {n: [evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(steps)]
+               for k, n in enumerate(self.NAMES)}
+        return t0.elapsed_time(t1), per
+
+
+def kernel_figures(wl, per, pk, peak_key):
+    """Per-call rooflines: bytes (HBM-bound calls) or flops (attention) per call
+    over the mean CUDA-event time, against the measured peaks."""
+    hkv, d, c, hq = wl.num_kv_heads, wl.head_dim, wl.chunk_len, wl.num_q_heads
+    pairs_total = pairs_per_head(wl) * hq
+    bytes_reps = wl.num_pages * hkv * wl.page_size * d * 2 + wl.num_pages * hkv * d * 4
+    bytes_sel = c * hq * d * 2 + wl.num_candidates * hkv * d * 4 + hkv * wl.n_sel * 4
+    work = {"page_reps": ("GB/s", bytes_reps / 1e6, pk["hbm_gbs"], "frac_hbm"),
+            "select_topk": ("GB/s", bytes_sel / 1e6, pk["hbm_gbs"], "frac_hbm"),
+            "attn_fwd": ("TFLOP/s", 4.0 * d * pairs_total / 1e9, pk[peak_key], "frac_bf16"),
+            "attn_bwd": ("TFLOP/s", 10.0 * d * pairs_total / 1e9, pk[peak_key], "frac_bf16")}
+    out = {}
+    for n, v in per.items():
+        ms = statistics.mean(v)
+        unit, amount, peak, fkey = work[n]
+        out[n] = {"ms": ms, unit: amount / ms, fkey: amount / ms / peak,
+                  "ms_median": statistics.median(v), "ms_min": min(v)}
+    return out
+
+
+def replica_timing(run, world, sync, barrier):
+    """The timed region of one replica: barrier and device sync on both sides
+    of ``run()`` (which returns its own elapsed ms), then the slowest rank's
+    time (replicas: the job ends when the last one does)."""
+    if world > 1:
+        barrier()
+    sync()
+    ms = run()
+    sync()
+    if world > 1:
+        barrier()
+    return ms, max_over_ranks(ms, world)
+
+
+def measure_configs(names, dev, steps, warmup, pk, peak_key):
+    """The other workloads of the evaluation ladder, one after another: a few
+    warm-up steps, then `steps` timed steps each (per-call CUDA events)."""
+    out = {}
+    for name in names:
+        wl = WORKLOADS[name]
+        step = PathStep(wl, dev)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        step.check_status()
+        total, per = step.time(steps)
+        step.check_status()
+        ms = total / steps
+        fwd_bwd_ms = statistics.mean(per["attn_fwd"]) + statistics.mean(per["attn_bwd"])
+        flops = attn_flops(wl)
+        out[name] = {"context": wl.context, "page_size": wl.page_size, "chunk_len": wl.chunk_len,
+                     "top_k": wl.top_k, "steps": steps, "ms_per_step": ms,
+                     "TFLOP/s": flops / ms / 1e9, "frac_of_bf16_peak": flops / ms / 1e9 / pk[peak_key],
+                     "fwd_bwd_ms": fwd_bwd_ms, "fwd_bwd_TFLOP/s": flops / fwd_bwd_ms / 1e9,
+                     "fwd_bwd_frac": flops / fwd_bwd_ms / 1e9 / pk[peak_key],
+                     "tokens_per_s_per_chunk": wl.chunk_len / (ms / 1e3),
+                     "kernels": kernel_figures(wl, per, pk, peak_key)}
+        del step
+        torch.cuda.empty_cache()
+    return out
+
+
+OTHER_CONFIGS = ["qwen7b_ctx256k_k64", "qwen7b_ctx1m_k128", "qwen7b_dense_ctx32k"]
 
 
 def run_ours(args, rank, world, dev):
@@ -308,71 +454,30 @@ def run_ours(args, rank, world, dev):
 
     wl = WORKLOADS[args.workload]
     torch.cuda.set_device(dev)
-    x = make_inputs(wl, seed=0, device=dev)
-    kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, torch.zeros_like(x.k_pool),
-                      torch.zeros_like(x.v_pool))
+    step = PathStep(wl, dev)
+    x, kv, stream = step.x, step.kv, step.stream
     hkv, d, c, hq = wl.num_kv_heads, wl.head_dim, wl.chunk_len, wl.num_q_heads
-    n_sel = wl.n_sel
-    reps = torch.empty((wl.num_pages, hkv, d), dtype=torch.float32, device=dev)
-    sel = torch.empty((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
-    o = torch.empty_like(x.q)
-    o_lo = oomb.o_residual_like(o)
-    lse = torch.empty((hq, c), dtype=torch.float32, device=dev)
-    dq = torch.empty_like(x.q)
-    ws_r = oomb.workspace(oomb.OOMB_OP_PAGE_REPS, kv)
-    ws_s = oomb.workspace(oomb.OOMB_OP_SELECT_TOPK, kv, hq, c, wl.top_k)
-    ws_f = oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv, hq, c)
-    ws_b = oomb.workspace(oomb.OOMB_OP_ATTN_BWD, kv, hq, c)
-    stream = torch.cuda.current_stream()
-    names = ["page_reps", "select_topk", "attn_fwd", "attn_bwd"]
-
-    def step(q, dout, ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        oomb.oomb_page_reps(kv, 0, wl.num_pages, reps, ws_r, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        oomb.oomb_select_topk(q, wl.start, reps, kv, wl.top_k, sel, ws_s, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-        oomb.oomb_sparse_attn_fwd(q, kv, sel, n_sel, wl.start, o, lse, ws_f, stream=stream,
-                                  o_lo=o_lo)
-        if ev is not None:
-            ev[3].record(stream)
-        oomb.oomb_sparse_attn_bwd(q, o, dout, lse, kv, sel, n_sel, wl.start, dq, ws_b,
-                                  stream=stream, o_lo=o_lo)
-        if ev is not None:
-            ev[4].record(stream)
-
     for _ in range(args.warmup):
-        step(x.q, x.do)
+        step()
     torch.cuda.synchronize()
-    for w in (ws_r, ws_s, ws_f, ws_b):
-        code, where, blk = oomb.oomb_device_status(w)
-        if code != 0:
-            raise RuntimeError(f"device status {oomb.oomb_status_string(code)} at {where}/{blk}")
+    step.check_status()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     phys = vis.split(",")[dev.index] if vis and vis.split(",")[0].isdigit() else dev.index
+    box = {}
+
+    def run():
+        box["total"], box["per"] = step.time(args.steps)
+        return box["total"]
+
     with ClockSampler(phys) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(x.q, x.do, evs[i])
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    samples = {n: [evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps)]
-               for k, n in enumerate(names)}
-    per = {n: statistics.mean(v) for n, v in samples.items()}
-    ms = max_over_ranks(total_ms / args.steps, world, dev)
+        total_ms, slowest_ms = replica_timing(run, world, torch.cuda.synchronize,
+                                              torch.distributed.barrier if world > 1 else None)
+    per = box["per"]
+    ms = slowest_ms / args.steps
+    timed_s = total_ms / 1e3
+    step.check_status()
+    sel_gpu = step.sel[:, :wl.n_sel].cpu().numpy()
 
     # end to end through the public API with host buffers: per step the chunk's
     # queries and output grads come from pinned host memory and the outputs (O,
@@ -383,33 +488,35 @@ def run_ours(args, rank, world, dev):
     do_h = x.do.cpu().pin_memory()
     o_h = torch.empty_like(q_h).pin_memory()
     dq_h = torch.empty_like(q_h).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    lse_h = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
     pipe = oomb.StepPipeline(kv, wl.start, c, hq, wl.top_k)
     for _ in range(2):
         pipe.step(q_h, do_h, o_h, lse_h, dq_h)
     pipe.finish()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, args.steps // 2)
     e0.record(stream)
     pipe.begin()
-    for _ in range(e2e_steps):
+    for _ in range(args.steps):
         pipe.step(q_h, do_h, o_h, lse_h, dq_h)
     stream.wait_stream(pipe.d2h)
     e1.record(stream)
     torch.cuda.synchronize()
     pipe.finish()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     h2d = q_h.numel() * q_h.element_size() + do_h.numel() * do_h.element_size()
     d2h = (o_h.numel() * o_h.element_size() + dq_h.numel() * dq_h.element_size()
            + lse_h.numel() * lse_h.element_size())
-    for w in (ws_r, ws_s, ws_f, ws_b):
-        code, where, blk = oomb.oomb_device_status(w)
-        if code != 0:
-            raise RuntimeError(f"device status {oomb.oomb_status_string(code)} at {where}/{blk}")
+    del pipe
+    step.check_status()
 
     flops = attn_flops(wl)
     pk, pk_src = peaks()
+    # the timed region lasts well under a second at the maximum clock: the
+    # burst peak is the one that applies; a region of seconds would hold the
+    # sustained one (the peak measured under the power cap)
+    peak_key = "bf16_tflops" if timed_s < 1.0 else "bf16_tflops_sustained"
+
     def optional(fn):
         # the side measurements must not cost the step's line: a failure (for
         # example pinned host memory refused) is reported in place of the figures
@@ -419,31 +526,18 @@ def run_ours(args, rank, world, dev):
             torch.cuda.synchronize()
             return {"error": f"{type(e).__name__}: {e}"[:300]}
 
-    chunk_pass = (optional(lambda: measure_chunk_pass(dev, pk["bf16_tflops_sustained"]))
+    chunk_pass = (optional(lambda: measure_chunk_pass(dev, pk[peak_key]))
                   if args.chunk_pass and wl.dtype == "bf16" else None)
-    offload = (optional(lambda: measure_offload(wl, x, kv, reps, dev))
+    offload = (optional(lambda: measure_offload(wl, x, kv, step.reps, dev))
                if args.offload and wl.dtype == "bf16" and wl.n_sel > 0 else None)
-    pairs_total = pairs_per_head(wl) * hq
-    bwd_flops = 10.0 * d * pairs_total
-    fwd_flops = 4.0 * d * pairs_total
-    bytes_reps = wl.num_pages * hkv * wl.page_size * d * 2 + wl.num_pages * hkv * d * 4
-    bytes_sel = c * hq * d * 2 + wl.num_candidates * hkv * d * 4 + hkv * n_sel * 4
-    peak_t = pk["bf16_tflops_sustained"]
-    peak_b = pk["hbm_gbs"]
-    kern = {
-        "page_reps": {"ms": per["page_reps"], "GB/s": bytes_reps / per["page_reps"] / 1e6,
-                      "frac_hbm": bytes_reps / per["page_reps"] / 1e6 / peak_b},
-        "select_topk": {"ms": per["select_topk"], "GB/s": bytes_sel / per["select_topk"] / 1e6,
-                        "frac_hbm": bytes_sel / per["select_topk"] / 1e6 / peak_b},
-        "attn_fwd": {"ms": per["attn_fwd"], "TFLOP/s": fwd_flops / per["attn_fwd"] / 1e9,
-                     "frac_bf16": fwd_flops / per["attn_fwd"] / 1e9 / peak_t},
-        "attn_bwd": {"ms": per["attn_bwd"], "TFLOP/s": bwd_flops / per["attn_bwd"] / 1e9,
-                     "frac_bf16": bwd_flops / per["attn_bwd"] / 1e9 / peak_t},
-    }
-    for n, v in samples.items():          # spread of the per-call times over the timed steps
-        kern[n]["ms_median"] = statistics.median(v)
-        kern[n]["ms_min"] = min(v)
-    achieved = bwd_flops / per["attn_bwd"] / 1e9
+    kern = kernel_figures(wl, per, pk, peak_key)
+    for n in ("attn_fwd", "attn_bwd"):
+        kern[n]["frac_bf16_sustained"] = kern[n]["TFLOP/s"] / pk["bf16_tflops_sustained"]
+    achieved = kern["attn_bwd"]["TFLOP/s"]
+    sha = bwd_source_sha()
+    rec = BWD_TRAFFIC.get(wl.name)
+    fresh = rec is not None and rec["sha"] == sha
+    clocks = clk.summary()
     res = {
         "metric": METRIC,
         "value": job_value(flops, ms, world),
@@ -464,22 +558,49 @@ def run_ours(args, rank, world, dev):
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: each step streams the whole K pool"},
         "tokens_per_s_per_chunk": world * c / (ms / 1e3),
-        "frac_of_bf16_peak": flops / ms / 1e9 / peak_t,
+        "frac_of_bf16_peak": flops / ms / 1e9 / pk[peak_key],
         "kernels": kern,
         "chunk_pass": chunk_pass,
         "offload": offload,
         "roofline": {"kernel": "oomb_sparse_attn_bwd (delta prep + sparse_attn_bwd_kernel + dq convert)",
-                     "bound": "tensor", "achieved": achieved, "peak": peak_t,
-                     "peak_source": f"{pk_src} bf16_tflops_sustained", "unit": "TFLOP/s",
-                     "frac": achieved / peak_t,
-                     "traffic": BWD_DRAM_BYTES.get(wl.name),
-                     "traffic_source": "profiles/dram_traffic_qwen7b_ctx4m_k128.md (ncu, one launch)"},
+                     "bound": "tensor", "achieved": achieved, "peak": pk[peak_key],
+                     "peak_source": f"{pk_src} {peak_key}: timed region {timed_s:.2f} s at a "
+                                    f"median {clocks.get('sm_mhz')} MHz",
+                     "unit": "TFLOP/s", "frac": achieved / pk[peak_key],
+                     "frac_sustained": achieved / pk["bf16_tflops_sustained"],
+                     "traffic": rec["bytes"] if fresh else None,
+                     "traffic_source": (rec["how"] if fresh else
+                                        "no capture of the current backward sources "
+                                        f"(sha {sha})")},
         "e2e": {"value": world * flops / e2e_ms / 1e9, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * (1 + 3 + 1 + 3),
-        "clocks": clk.summary(),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "steps": args.steps},
+        "gpu_launches": args.steps * PathStep.LAUNCHES,
+        "clocks": clocks,
     }
-    return res, x, wl
+    return res, step, sel_gpu, peak_key
+
+
+def selection_vs_oracle(sel_gpu, sel_o, scores_o, gap=1e-4):
+    """The GPU selection against the oracle's: per KV head, the pages only one
+    side picked must pair up with oracle fp32 scores closer than ``gap``
+    (near-ties, counted); anything else is a mismatch."""
+    swaps, worst, mismatch = 0, 0.0, 0
+    for g in range(sel_o.shape[0]):
+        a = sorted(set(sel_gpu[g].tolist()) - set(sel_o[g].tolist()))
+        b = sorted(set(sel_o[g].tolist()) - set(sel_gpu[g].tolist()))
+        if len(a) != len(b):
+            mismatch += 1
+            continue
+        sa = sorted(float(scores_o[g][i]) for i in a)
+        sb = sorted(float(scores_o[g][i]) for i in b)
+        for u, v in zip(sa, sb):
+            if abs(u - v) >= gap:
+                mismatch += 1
+            worst = max(worst, abs(u - v))
+        swaps += len(a)
+    return {"heads": int(sel_o.shape[0]), "k": int(sel_o.shape[1]), "near_tie_swaps": swaps,
+            "largest_swap_gap": worst, "mismatches": mismatch, "gap_exempt": gap}
 
 
 # ---------------------------------------------------------------------------
@@ -499,8 +620,9 @@ def oracle_setup(wl, x=None):
                            for b in range(0, wl.num_pages, 512)])
     q = to_numpy64(x.q)
     do = to_numpy64(x.do)
-    sel = oracle.select_topk(oracle.page_scores(oracle.query_summary(q, wl.num_kv_heads), reps,
-                                                wl.num_candidates), wl.top_k)
+    scores = oracle.page_scores(oracle.query_summary(q, wl.num_kv_heads), reps,
+                                wl.num_candidates)
+    sel = oracle.select_topk(scores, wl.top_k)
     own = np.arange(wl.start // wl.page_size, (wl.start + wl.chunk_len) // wl.page_size)
     need = np.unique(np.concatenate([sel.reshape(-1), own]))
     slots = pt.numpy()[need]
@@ -508,7 +630,7 @@ def oracle_setup(wl, x=None):
     vc = x.v_pool.cpu()[torch.as_tensor(slots)].float().numpy()
     ptc = np.full(wl.num_pages, -1, np.int64)
     ptc[need] = np.arange(need.size)
-    return dict(q=q, do=do, sel=sel, kc=kc, vc=vc, ptc=ptc)
+    return dict(q=q, do=do, sel=sel, scores=scores, kc=kc, vc=vc, ptc=ptc)
 
 
 def oracle_step(wl, st, rows):
@@ -557,6 +679,23 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def relaunch_as_replicas(n):
+    """bench.py --gpus N started without torchrun: start it again under
+    torchrun with one rank (one replica) per GPU; refuse if there are fewer."""
+    have = torch.cuda.device_count() if torch.cuda.is_available() else 0
+    if have < n:
+        sys.stderr.write(f"bench.py: --gpus {n} asks for {n} GPUs, {have} visible\n")
+        sys.exit(2)
+    import socket
+    with socket.socket() as s_:
+        s_.bind(("127.0.0.1", 0))
+        port = s_.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__)] + sys.argv[1:]
+    os.execv(sys.executable, cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,12 +710,16 @@ def main():
                     help="skip the whole-sequence chunk-recurrent pass measurement")
     ap.add_argument("--no-offload", dest="offload", action="store_false",
                     help="skip the host-offload measurement")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the 256K, 1M and dense 32K workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world == 1 and args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        relaunch_as_replicas(args.gpus)
     if world > 1:
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         backend = "nccl" if torch.cuda.is_available() else "gloo"
@@ -588,11 +731,19 @@ def main():
             print(json.dumps(res), flush=True)
     else:
         dev = torch.device("cuda", local)
-        res, x, wl = run_ours(args, rank, world, dev)
+        res, step, sel_gpu, peak_key = run_ours(args, rank, world, dev)
+        wl = step.wl
+        st = None
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            st = oracle_setup(wl, x)
-            del x
-            torch.cuda.empty_cache()
+            st = oracle_setup(wl, step.x)          # host copies, then the device frees them
+        del step
+        torch.cuda.empty_cache()
+        if rank == 0 and args.configs:
+            pk, _ = peaks()
+            res["configs"] = measure_configs([n for n in OTHER_CONFIGS if n != wl.name], dev,
+                                             min(args.steps, 20), args.warmup, pk, peak_key)
+        if st is not None:
+            res["selection_vs_oracle"] = selection_vs_oracle(sel_gpu, st["sel"], st["scores"])
             res["cpu_baseline"] = cpu_baseline(wl, st, args.cpu_rows)
         if rank == 0:
             print(json.dumps(res), flush=True)
