@@ -140,7 +140,10 @@ oomb_status oomb_page_reps(const oomb_paged_kv *kv, int32_t first_page, int32_t 
  * equal scores go to the lower page index; sel[g][0..n_sel) is written in
  * ascending page order.  scores_opt, if not NULL, receives float
  * [Hkv][num_pages] (non-candidates = -inf).  Deterministic: the fp32
- * reductions run in a fixed order.  ws: oomb_workspace_bytes(SELECT_TOPK). */
+ * reductions run in a fixed order.  One cooperative kernel with one CTA per
+ * SM (its CTAs wait for one another; each wait is bounded and records
+ * OOMB_ERR_TIMEOUT in the status word of ws if it runs out).
+ * ws: oomb_workspace_bytes(SELECT_TOPK). */
 oomb_status oomb_select_topk(const void *q, int32_t num_q_heads, int32_t chunk_len,
                              int32_t chunk_start, const float *reps, const oomb_paged_kv *kv,
                              int32_t top_k, int32_t *sel, float *scores_opt, void *ws,
@@ -155,15 +158,17 @@ oomb_status oomb_select_topk(const void *q, int32_t num_q_heads, int32_t chunk_l
  * library: a file-scope device array of OOMB_NOALLOC_SCRATCH_BYTES (4 MiB),
  * which every GPU that loads the library holds until the process exits.  It
  * must hold oomb_workspace_bytes(OOMB_OP_SELECT_TOPK, ...) for these shapes
- * (about 256 B + 2.4 KiB * Hkv * D / 16 + 4 B * Hkv * num_pages); larger
- * requests return OOMB_ERR_INVALID_ARG before anything is launched.  The
+ * (about 256 B + 1152 B * Hkv * D + 256 KiB * Hkv + 4 B * Hkv * num_pages,
+ * e.g. up to ~157K pages at Hkv = 4, D = 128); larger requests return
+ * OOMB_ERR_INVALID_ARG before anything is launched.  The
  * first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  The call
  * never calls cudaMalloc, cudaFree or any allocating routine.  All calls
  * share the one array, which keeps the last call's contents: the call clears
  * the part that must start at zero, and calls that overlap on the GPU (other
- * streams, other host threads) race on it -- serialise them.  The selection
- * kernels record no device-side status, so there is no status word to read. */
+ * streams, other host threads) race on it -- serialise them.  The status word
+ * where the selection records a bounded wait that ran out is in that array,
+ * which a caller of this entry point cannot read. */
 #define OOMB_NOALLOC_SCRATCH_BYTES (4u << 20)
 oomb_status oomb_select_topk_noalloc(const void *q, int32_t num_q_heads, int32_t chunk_len,
                                      int32_t chunk_start, const float *reps,

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cooperative_groups.h>
+
 #include <cstdint>
 #include <mutex>
 
@@ -131,187 +133,99 @@ cudaError_t reps_dispatch(const KvDesc& kv, int first_page, int n_pages, int las
 }
 
 // ---------------------------------------------------------------------------
-// Step 2a: qbar[g][:] = mean of q over the chunk's tokens and the G heads of
-// group g.  kQbarBlocks CTAs each sum a contiguous token slice (two token rows
-// per step, 8 rows in flight per thread); the CTA then folds its heads into
-// groups and writes a partial.  The last CTA to finish (ticket counter) sums
-// the partials in a fixed tree: 7 sub-slices of consecutive partials per
-// float4 column, then the 7 sub-sums in order.
+// Copies of 16 bytes global -> shared that stay in flight without holding
+// registers; each thread waits only for its own (commit groups), so a thread
+// that reads back exactly the slots it filled needs no barrier.
 // ---------------------------------------------------------------------------
-constexpr int kQbarThreads = 896;
-constexpr int kTailMax = 12;                      // partials per sub-slice of the tree
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// ---------------------------------------------------------------------------
+// Step 2: the Top-K page selection as one cooperative kernel, one CTA per SM
+// (every CTA resident at once, so the CTAs can wait for one another: each
+// such wait is bounded and records OOMB_ERR_TIMEOUT if it runs out).
+//
+//  2a  qbar[g][:] = mean of q over the chunk's tokens and the G heads of
+//      group g.  Each CTA streams a contiguous slice of token rows: a thread
+//      owns one 16-byte column of a row (R rows side by side per step) and
+//      keeps kSelDepth row copies in flight through shared memory.  The CTA
+//      folds its rows and the heads of each group into a partial; partials
+//      are added in two levels, each by whichever CTA finishes last (ticket
+//      counters): the last CTA of each group of kSelGroup consecutive CTAs
+//      adds the group's partials in CTA order, the last group adds the group
+//      sums in group order and publishes qbar (a generation counter).  Every
+//      sum runs in a fixed order: the result does not depend on timing.
+//  2b  score[g][l] = qbar[g] . reps[l][g] for l < n_cand (else -inf).  A
+//      group of D/4 lanes covers one (page, KV head) row, one 16-byte column
+//      per lane, with kSelDepth rows in flight; a CTA issues its first row
+//      copies before it waits for qbar (the representatives do not depend on
+//      it).  Products are summed by a fixed shuffle pattern.  Each score is
+//      also counted in a per-head histogram of the top 16 bits of its
+//      order-preserving key: the first digit of the radix select below.
+//  2c  Once every CTA has counted its scores (an arrival counter), CTA g <
+//      Hkv keeps the top_k best scores of KV head g (ties -> lower page),
+//      written in ascending page order: the first digit's bin where the
+//      count from the top reaches k, then two 8-bit digits from shared-memory
+//      histograms of the keys that share the digits found so far give the
+//      k-th largest key T and how many keys equal to T are kept (the
+//      lowest-indexed ones); an index-ordered compaction writes every key
+//      above T and those ties.  Ties and degenerate score ranges take the
+//      same path as everything else.
+// ---------------------------------------------------------------------------
+constexpr int kSelThreads = 1024;
+constexpr int kSelDepth = 8;                      // 16-byte copies in flight per thread
+constexpr int kSelGroup = 8;                      // CTAs per first-level group
+constexpr int kSelMaxBlocks = 256;
+constexpr int kSelCacheKeys = 40 * 1024;          // keys cached for the radix passes
+constexpr int kSelSortMax = 4096;                 // keys sorted on the fast path
+constexpr size_t kSelRingBytes = sizeof(uint4) * kSelDepth * kSelThreads;
+constexpr size_t kSelCacheBytes =
+    kSelRingBytes > 4 * kSelCacheKeys ? kSelRingBytes : 4 * static_cast<size_t>(kSelCacheKeys);
+constexpr size_t kSelListBytes = 8 * 4096 + 4 * 4096;   // the fast path's sort buffers
+constexpr size_t kSelDynSmem = kSelCacheBytes + kSelListBytes;
+static_assert(kGroupTicketIdx + (kSelMaxBlocks + kSelGroup - 1) / kSelGroup <= 64,
+              "tickets fit the status block");
 
-template <typename T>
-__global__ void __launch_bounds__(kQbarThreads) qbar_kernel(const T* __restrict__ q, int chunk_len,
-                                                            int hq, int hkv, int head_dim,
-                                                            float* __restrict__ partials,
-                                                            float* __restrict__ qbar,
-                                                            int* status) {
-  constexpr int E = Vec<T>::kElems;
-  constexpr int U = 8;                            // token rows in flight per thread
-  extern __shared__ float sm[];                   // [R][hq*head_dim], reused by the tree
-  __shared__ int is_last;
-  const int row_elems = hq * head_dim;
-  const int row_vecs = row_elems / E;             // 16-byte vectors per token row
-  const int R = blockDim.x / row_vecs;            // token rows per step (>= 1)
-  const int nb = gridDim.x;
-  const int t_per = (chunk_len + nb - 1) / nb;
-  const int t0 = blockIdx.x * t_per;
-  const int t1 = min(chunk_len, t0 + t_per);
-  const int sub = threadIdx.x / row_vecs;
-  const int col = threadIdx.x % row_vecs;
-  if (sub < R) {
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    const T* base = q + static_cast<size_t>(col) * E;
-    // rounds of U predicated loads, all in flight together (no serial remainder)
-    for (int t = t0 + sub; t < t1; t += U * R) {
-      uint4 v[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        v[u] = (t + u * R < t1) ? ldg_stream(base + static_cast<size_t>(t + u * R) * row_elems)
-                                : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float f[E];
-        Vec<T>::to_float(v[u], f);
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] += f[e];
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) sm[sub * row_elems + col * E + e] = acc[e];
-  }
-  __syncthreads();
-  const int grp = hq / hkv;
-  for (int o = threadIdx.x; o < hkv * head_dim; o += blockDim.x) {
-    const int g = o / head_dim, d = o % head_dim;
-    float s = 0.f;
-    for (int j = 0; j < grp; ++j) {
-      const int idx = (g * grp + j) * head_dim + d;
-      for (int r = 0; r < R; ++r) s += sm[r * row_elems + idx];
-    }
-    partials[static_cast<size_t>(blockIdx.x) * hkv * head_dim + o] = s;
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int ticket = atomicAdd(&status[kTicketIdx], 1);
-    is_last = (ticket == nb - 1);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // Fixed-order tree over the nb partials.
-  const int n_out4 = hkv * head_dim / 4;          // float4 columns
-  const int n_sub = blockDim.x / n_out4 < 7 ? blockDim.x / n_out4 : 7;
-  float4* red = reinterpret_cast<float4*>(sm);    // [n_sub][n_out4]
-  if (threadIdx.x < n_sub * n_out4) {
-    const int c4 = threadIdx.x % n_out4, s = threadIdx.x / n_out4;
-    const int per = (nb + n_sub - 1) / n_sub;
-    const int b0 = s * per, b1 = min(nb, b0 + per);
-    const float4* p4 = reinterpret_cast<const float4*>(partials);
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = b0; base < b1; base += kTailMax) {   // kTailMax loads in flight
-      float4 x[kTailMax];
-#pragma unroll
-      for (int u = 0; u < kTailMax; ++u)
-        x[u] = (base + u < b1) ? __ldcg(p4 + static_cast<size_t>(base + u) * n_out4 + c4)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int u = 0; u < kTailMax; ++u) {
-        a.x += x[u].x; a.y += x[u].y; a.z += x[u].z; a.w += x[u].w;
-      }
-    }
-    red[s * n_out4 + c4] = a;
-  }
-  __syncthreads();
-  if (threadIdx.x < n_out4) {
-    float4 a = red[threadIdx.x];
-    for (int s = 1; s < n_sub; ++s) {
-      const float4 x = red[s * n_out4 + threadIdx.x];
-      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
-    }
-    const float inv = 1.0f / (static_cast<float>(chunk_len) * grp);
-    a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
-    reinterpret_cast<float4*>(qbar)[threadIdx.x] = a;
-  }
-  if (threadIdx.x == 0) status[kTicketIdx] = 0;   // leave the counter at zero
+// Bring `bytes` (a multiple of 16) at `p` into L2, without waiting.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// Step 2b: score[g][l] = qbar[g] . reps[l][g] for l < n_cand (else -inf).
-// A group of D/4 lanes covers one 4*D-byte rep row with float4 loads; each
-// warp keeps 4 row-steps in flight; shuffle reduction in a fixed pattern.
-// ---------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(256) page_scores_kernel(const float* __restrict__ reps,
-                                                          const float* __restrict__ qbar,
-                                                          int n_cand, int num_pages, int hkv,
-                                                          float* __restrict__ scores) {
-  constexpr int L = D / 4;                        // lanes per row
-  constexpr int RPW = 32 / L;                     // rows per warp-step
-  constexpr int U = 8;
-  __shared__ float4 qs[16 * L];                   // hkv <= 16
-  for (int i = threadIdx.x; i < hkv * L; i += blockDim.x)
-    qs[i] = reinterpret_cast<const float4*>(qbar)[i];
-  __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int sub = lane / L, li = lane % L;
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  // rows = (page, KV head) pairs; below 2^31 for every supported pool
-  const int rows = num_pages * hkv;
-  const int cand_rows = n_cand * hkv;
-  for (int r0 = wid * RPW * U; r0 < rows; r0 += warps_total * RPW * U) {
-    float4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int r = r0 + u * RPW + sub;
-      v[u] = (r < cand_rows) ? __ldcs(reinterpret_cast<const float4*>(reps) + static_cast<long>(r) * L + li)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int r = r0 + u * RPW + sub;
-      const int g = r % hkv;
-      const float4 qv = qs[g * L + li];
-      float s = v[u].x * qv.x;
-      s = fmaf(v[u].y, qv.y, s);
-      s = fmaf(v[u].z, qv.z, s);
-      s = fmaf(v[u].w, qv.w, s);
-#pragma unroll
-      for (int off = L / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (li == 0 && r < rows) {
-        const int l = r / hkv;
-        scores[static_cast<long>(g) * num_pages + l] = (r < cand_rows) ? s : -INFINITY;
+// In-place bitonic sort of n (a power of two) values in shared memory by the
+// whole block: descending if `desc`, else ascending.
+template <typename V>
+__device__ __forceinline__ void block_bitonic_sort(V* a, int n, bool desc) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < (n >> 1); t += blockDim.x) {
+        const int i = 2 * t - (t & (stride - 1));
+        const int j = i + stride;
+        const bool d = ((i & size) == 0) == desc;
+        const V x = a[i], y = a[j];
+        if ((x < y) == d) {
+          a[i] = y;
+          a[j] = x;
+        }
       }
+      __syncthreads();
     }
   }
 }
-
-// ---------------------------------------------------------------------------
-// Step 2c: per KV head, keep the top_k best scores (ties -> lower page),
-// written in ascending page order.  One CTA of 1024 threads per KV head.
-// Radix select on order-preserving 32-bit keys (11 + 11 + 10 bits) finds the
-// k-th key T; then every key > T is kept plus the lowest-indexed keys == T
-// until k are kept.  Compaction runs in index order, so the output is sorted.
-// ---------------------------------------------------------------------------
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkSmemKeys = 48 * 1024;          // keys cached in shared memory
-constexpr int kTopkCand = 2048;                   // keys of one value bin resolved exactly
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   if (f != f) return 0u;                          // NaN never outranks a number
   if (f == 0.f) f = 0.f;                          // -0 == +0
   const uint32_t b = __float_as_uint(f);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// The float a key stands for (inverse of order_key on numbers).
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
@@ -341,213 +255,484 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
   return before;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores,
-                                                            int num_pages, int n_cand, int top_k,
-                                                            int32_t* __restrict__ sel) {
-  extern __shared__ uint32_t keys_sm[];           // n_cand keys when they fit
-  __shared__ int hist[2048];
+// Thread 0 waits until `*word - base` (unsigned) reaches `target`, for at
+// most limit_ns; returns false (and records a timeout) if it does not.
+__device__ __forceinline__ bool wait_counter(const int* word, uint32_t base, uint32_t target,
+                                             int* status, uint64_t limit_ns, int where) {
+  const uint64_t t0 = global_timer_ns();
+  while (static_cast<uint32_t>(*reinterpret_cast<const volatile int*>(word)) - base < target) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      raise_status(status, kStatusTimeout, where);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  __threadfence();                                // acquire: what was published before it
+  return true;
+}
+
+struct SelParams {
+  const void* q;
+  const float* reps;
+  float* scores;                  // [hkv][num_pages]
+  int32_t* sel;                   // [hkv][n_sel]
+  float* partials;                // [kSelMaxBlocks][hkv * D]
+  float* gsums;                   // [groups][hkv * D]
+  float* qbar;                    // [hkv * D]
+  int* hist;                      // [hkv][65536]
+  int* status;
+  int chunk_len, hq, hkv, n_cand, num_pages, top_k;
+  uint64_t wait_ns;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams p) {
+  constexpr int E = Vec<T>::kElems;
+  constexpr int L = D / 4;                        // lanes per (page, head) row
+  constexpr int RPW = 32 / L;                     // rows per warp step
+  extern __shared__ __align__(16) uint4 ring[];   // copies in flight; the fold; the key cache
+  __shared__ float4 qs[16 * L];                   // qbar (hkv <= 16)
+  __shared__ int hist[256];
   __shared__ int warp_tot[32];
   __shared__ int total;
-  __shared__ uint32_t sh_prefix, sh_min, sh_max;
+  __shared__ int flag;
+  __shared__ uint32_t base_q, base_s, sh_digit;
   __shared__ int sh_need;
-  const int g = blockIdx.x;
-  const float* sc = scores + static_cast<long>(g) * num_pages;
-  const int k = top_k < n_cand ? top_k : n_cand;  // n_sel: row stride of sel
-  int32_t* out = sel + static_cast<long>(g) * k;
-  if (k == n_cand) {                              // every candidate is kept
-    for (int i = threadIdx.x; i < n_cand; i += blockDim.x) out[i] = i;
+  const int tid = threadIdx.x, nt = kSelThreads;
+  const int nb = gridDim.x, bid = blockIdx.x;
+  int* status = p.status;
+  if (tid == 0) {
+    // generation counters as they stand: nothing changes them before every
+    // CTA of this grid has finished its query slice
+    base_q = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(&status[kSelQbarGenIdx]));
+    base_s = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(&status[kSelScoreCntIdx]));
+  }
+  // the key histogram starts at zero (counted into only after qbar exists,
+  // i.e. after every CTA has passed this point)
+  const long hist_words = static_cast<long>(p.hkv) << 16;
+  for (long i = static_cast<long>(bid) * nt + tid; i < hist_words; i += static_cast<long>(nb) * nt)
+    p.hist[i] = 0;
+
+  // ---------------------------------------------------------------- 2a
+  const int hq = p.hq, hkv = p.hkv;
+  const int row_elems = hq * D;
+  const int row_vecs = row_elems / E;             // 16-byte vectors per token row
+  const int R = 896 / row_vecs;                   // token rows per step (>= 1)
+  const int t_per = (p.chunk_len + nb - 1) / nb;
+  const int t0 = min(p.chunk_len, bid * t_per);
+  const int t1 = min(p.chunk_len, t0 + t_per);
+  const int sub = tid / row_vecs, col = tid % row_vecs;
+  {
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    if (sub < R) {
+      const T* base = static_cast<const T*>(p.q) + static_cast<size_t>(col) * E;
+      const int n_j = t1 > t0 + sub ? (t1 - t0 - sub + R - 1) / R : 0;
+      auto row = [&](int j) { return base + static_cast<size_t>(t0 + sub + j * R) * row_elems; };
+#pragma unroll
+      for (int j = 0; j < kSelDepth; ++j) {
+        if (j < n_j) cp_async16(&ring[j * nt + tid], row(j));
+        cp_async_commit();
+      }
+      for (int j = 0; j < n_j; ++j) {
+        cp_async_wait<kSelDepth - 1>();           // row j has landed
+        uint4* slot = &ring[(j % kSelDepth) * nt + tid];
+        const uint4 v = *slot;
+        if (j + kSelDepth < n_j) cp_async16(slot, row(j + kSelDepth));
+        cp_async_commit();
+        float f[E];
+        Vec<T>::to_float(v, f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += f[e];
+      }
+    }
+    cp_async_wait<0>();
+    if (tid == 0) {
+      // this CTA's representative rows (2b), into L2 while the query summary
+      // is folded and waited for: the loads of 2b then mostly hit L2
+      const int cand_rows0 = p.n_cand * p.hkv;
+      const int r_per0 = (cand_rows0 + nb - 1) / nb;
+      const int a0 = min(cand_rows0, bid * r_per0), a1 = min(cand_rows0, a0 + r_per0);
+      const char* base = reinterpret_cast<const char*>(p.reps) + static_cast<size_t>(a0) * D * 4;
+      const size_t bytes = static_cast<size_t>(a1 - a0) * D * 4;
+      for (size_t off = 0; off < bytes; off += 65536)
+        prefetch_l2(base + off, static_cast<uint32_t>(bytes - off < 65536 ? bytes - off : 65536));
+    }
+    __syncthreads();                              // the ring becomes the fold area
+    float* sm = reinterpret_cast<float*>(ring);   // [R][row_elems]
+    if (sub < R) {                                // 16-byte stores: no bank conflicts
+      float4* dst = reinterpret_cast<float4*>(sm + sub * row_elems + col * E);
+#pragma unroll
+      for (int e = 0; e < E; e += 4) dst[e / 4] = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+    }
+    __syncthreads();
+  }
+  const int grp = hq / hkv;
+  const int n_out = hkv * D;
+  {
+    const float* sm = reinterpret_cast<const float*>(ring);
+    for (int o = tid; o < n_out; o += nt) {
+      const int g = o / D, d = o % D;
+      float s = 0.f;
+      for (int j = 0; j < grp; ++j) {
+        const int idx = (g * grp + j) * D + d;
+        for (int r = 0; r < R; ++r) s += sm[r * row_elems + idx];
+      }
+      p.partials[static_cast<size_t>(bid) * n_out + o] = s;
+    }
+  }
+  const int n_groups = (nb + kSelGroup - 1) / kSelGroup;
+  const int group = bid / kSelGroup;
+  const int in_group = min(kSelGroup, nb - group * kSelGroup);
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    flag = atomicAdd(&status[kGroupTicketIdx + group], 1) == in_group - 1;
+  }
+  __syncthreads();
+  if (flag) {                                     // last of its group
+    __threadfence();
+    for (int o = tid; o < n_out; o += nt) {
+      float s = 0.f;
+      for (int c = 0; c < in_group; ++c)
+        s += __ldcg(p.partials + static_cast<size_t>(group * kSelGroup + c) * n_out + o);
+      p.gsums[static_cast<size_t>(group) * n_out + o] = s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      status[kGroupTicketIdx + group] = 0;        // leave the counter at zero
+      __threadfence();
+      atomicAdd(&status[kSelQbarGenIdx], 1);      // one more group summed
+    }
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- 2b
+  // rows = (page, KV head) pairs of the candidates; this CTA's contiguous
+  // range, walked by its warps in steps of RPW rows; kSelDepth rows per lane
+  // in flight, the first ones requested before qbar exists
+  const int cand_rows = p.n_cand * hkv;
+  const int r_per = (cand_rows + nb - 1) / nb;
+  const int rb0 = min(cand_rows, bid * r_per), rb1 = min(cand_rows, rb0 + r_per);
+  const int lane = tid & 31, w = tid >> 5;
+  const int rsub = lane / L, li = lane % L;
+  const int stride = (nt / 32) * RPW;
+  const int r0 = rb0 + w * RPW + rsub;            // this lane's first row
+  const int n_j = r0 < rb1 ? (rb1 - r0 + stride - 1) / stride : 0;
+  const int w0 = rb0 + w * RPW;                   // the warp steps together
+  const int n_w = w0 < rb1 ? (rb1 - w0 + stride - 1) / stride : 0;
+  const float4* src = reinterpret_cast<const float4*>(p.reps) + li;
+#pragma unroll
+  for (int j = 0; j < kSelDepth; ++j) {
+    if (j < n_j) cp_async16(&ring[j * nt + tid], src + static_cast<long>(r0 + j * stride) * L);
+    cp_async_commit();
+  }
+  if (tid == 0)
+    flag = wait_counter(&status[kSelQbarGenIdx], base_q, static_cast<uint32_t>(n_groups), status,
+                        p.wait_ns, kWhereSelect);
+  __syncthreads();
+  if (!flag) {
+    cp_async_wait<0>();
     return;
   }
-  const bool cached = n_cand <= kTopkSmemKeys;
-  if (threadIdx.x == 0) {
-    sh_min = 0xFFFFFFFFu;
-    sh_max = 0u;
-  }
-  __syncthreads();
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  constexpr int kU = 8;                           // loads in flight per thread
-  for (int base = threadIdx.x; base < n_cand; base += kU * blockDim.x) {
-    float v[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = base + u * blockDim.x;
-      v[u] = i < n_cand ? __ldcg(sc + i) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = base + u * blockDim.x;
-      if (i < n_cand) {
-        const uint32_t key = order_key(v[u]);
-        if (cached) keys_sm[i] = key;
-        kmin = min(kmin, key);
-        kmax = max(kmax, key);
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  if ((threadIdx.x & 31) == 0) {
-    atomicMin(&sh_min, kmin);
-    atomicMax(&sh_max, kmax);
-  }
-  __syncthreads();
-  auto key_at = [&](int i) -> uint32_t { return cached ? keys_sm[i] : order_key(__ldcg(sc + i)); };
-
-  // Fast path: a histogram of the score values in 2048 equal-width bins
-  // between the smallest and the largest score.  The scores of a head sit in
-  // a narrow range of either sign, where the bits of their encodings put
-  // most keys in a few radix bins; equal-width value bins spread them.  The
-  // bin is monotone in the score, so every key of a higher bin ranks above
-  // every key of a lower one, and the k-th largest key is found exactly among
-  // the keys of its own bin (ranked by counting).  Degenerate ranges, or a bin
-  // with more than kTopkCand keys, take the radix passes below.
-  __shared__ uint32_t cand[kTopkCand];
-  __shared__ int sh_nc, sh_bin;
-  uint32_t prefix = 0;
-  int need = k;                                   // still to take at or below `prefix`
-  bool fast = false;
+  // qbar: the group sums in group order (every CTA adds them the same way)
   {
-    const float fmin = key_value(sh_min), fmax = key_value(sh_max);
-    const float inv_w = 2048.f / (fmax - fmin);
-    if (fmax > fmin && isfinite(fmin) && isfinite(fmax) && isfinite(inv_w)) {
-      auto vbin = [&](uint32_t key) -> int {
-        const int b = static_cast<int>((key_value(key) - fmin) * inv_w);
-        return b < 2047 ? b : 2047;
-      };
-      for (int i = threadIdx.x; i < 2048; i += blockDim.x) hist[i] = 0;
-      if (threadIdx.x == 0) sh_nc = 0;
-      __syncthreads();
-      for (int i = threadIdx.x; i < n_cand; i += blockDim.x) atomicAdd(&hist[vbin(key_at(i))], 1);
-      __syncthreads();
-      // bin counts from the top: thread t owns bins 2047 - 2t and 2046 - 2t
-      const int b_hi = 2047 - 2 * static_cast<int>(threadIdx.x);
-      const int c0 = hist[b_hi], c1 = hist[b_hi - 1];
-      const int before = block_excl_scan(c0 + c1, warp_tot, &total);
-      if (before < k && before + c0 >= k) {
-        sh_bin = b_hi;
-        sh_need = k - before;
-      } else if (before + c0 < k && before + c0 + c1 >= k) {
-        sh_bin = b_hi - 1;
-        sh_need = k - before - c0;
+    const float inv = 1.0f / (static_cast<float>(p.chunk_len) * grp);
+    const float4* gs4 = reinterpret_cast<const float4*>(p.gsums);
+    for (int i = tid; i < hkv * L; i += nt) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < n_groups; ++c) {
+        const float4 v = __ldcg(gs4 + static_cast<size_t>(c) * (n_out / 4) + i);
+        a.x += v.x;
+        a.y += v.y;
+        a.z += v.z;
+        a.w += v.w;
       }
-      __syncthreads();
-      const int bin = sh_bin, need_b = sh_need, c_b = hist[bin];
-      if (c_b <= kTopkCand) {
-        for (int i = threadIdx.x; i < n_cand; i += blockDim.x) {
-          const uint32_t key = key_at(i);
-          if (vbin(key) == bin) cand[atomicAdd(&sh_nc, 1)] = key;
-        }
-        __syncthreads();
-        // the need_b-th largest key of the bin: gt keys above it, eq equal to it
-        for (int c = threadIdx.x; c < c_b; c += blockDim.x) {
-          const uint32_t x = cand[c];
-          int gt = 0, eq = 0;
-          for (int u = 0; u < c_b; ++u) {
-            gt += cand[u] > x;
-            eq += cand[u] == x;
-          }
-          if (gt < need_b && need_b <= gt + eq) {  // every writer writes the same values
-            sh_prefix = x;
-            sh_nc = need_b - gt;
-          }
-        }
-        __syncthreads();
-        prefix = sh_prefix;
-        need = sh_nc;
-        fast = true;
-      }
-      __syncthreads();
+      qs[i] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
     }
   }
-  // Radix passes: every key shares the bits above the highest bit where min
-  // and max differ, so the digits start just below that common prefix.
-  const uint32_t diff = sh_min ^ sh_max;
-  int lo_bit = (fast || !diff) ? 0 : 32 - __clz(diff);   // bits [0, lo_bit) still vary
-  if (!fast) {
-    const uint32_t low = (lo_bit >= 32) ? 0xFFFFFFFFu : ((1u << lo_bit) - 1u);
-    prefix = sh_max & ~low;                       // the common high bits
+  __syncthreads();
+  for (int j = 0; j < n_w; ++j) {
+    cp_async_wait<kSelDepth - 1>();
+    const bool valid = j < n_j;
+    uint4* slot = &ring[(j % kSelDepth) * nt + tid];
+    const uint4 raw = valid ? *slot : make_uint4(0, 0, 0, 0);
+    const int r = r0 + j * stride;
+    if (j + kSelDepth < n_j) cp_async16(slot, src + static_cast<long>(r + kSelDepth * stride) * L);
+    cp_async_commit();
+    const int g = r % hkv;
+    const float4 qv = qs[g * L + li];
+    float sc = __uint_as_float(raw.x) * qv.x;
+    sc = fmaf(__uint_as_float(raw.y), qv.y, sc);
+    sc = fmaf(__uint_as_float(raw.z), qv.z, sc);
+    sc = fmaf(__uint_as_float(raw.w), qv.w, sc);
+    // lanes of one row reduce among themselves (the row's L lanes are aligned)
+#pragma unroll
+    for (int off = L / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+    if (valid && li == 0) {
+      p.scores[static_cast<long>(g) * p.num_pages + r / hkv] = sc;
+      atomicAdd(&p.hist[(static_cast<long>(g) << 16) + (order_key(sc) >> 16)], 1);
+    }
   }
-  uint32_t mask = (lo_bit >= 32) ? 0u : ~((1u << lo_bit) - 1u);
-  while (lo_bit > 0) {
-    const int width = lo_bit < 11 ? lo_bit : 11;
-    const int sh = lo_bit - width, nbins = 1 << width;
-    for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
+  cp_async_wait<0>();
+  __syncthreads();                                // the ring is free again
+  // pages that are not candidates
+  const int n_other = (p.num_pages - p.n_cand) * hkv;
+  for (int i = bid * nt + tid; i < n_other; i += nb * nt) {
+    const int g = i % hkv, l = p.n_cand + i / hkv;
+    p.scores[static_cast<long>(g) * p.num_pages + l] = -INFINITY;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(&status[kSelScoreCntIdx], 1);       // this CTA's scores are counted
+  }
+  if (bid >= hkv || p.top_k == 0 || p.n_cand == 0) return;
+
+  // ---------------------------------------------------------------- 2c
+  const int g = bid;
+  const float* sc = p.scores + static_cast<long>(g) * p.num_pages;
+  const int n_cand = p.n_cand;
+  const int k = p.top_k < n_cand ? p.top_k : n_cand;   // n_sel: row stride of sel
+  int32_t* out = p.sel + static_cast<long>(g) * k;
+  if (k == n_cand) {                              // every candidate is kept
+    for (int i = tid; i < n_cand; i += nt) out[i] = i;
+    return;
+  }
+  if (tid == 0)
+    flag = wait_counter(&status[kSelScoreCntIdx], base_s, static_cast<uint32_t>(nb), status,
+                        p.wait_ns, kWhereSelect);
+  __syncthreads();
+  if (!flag) return;
+  uint32_t* keys_sm = reinterpret_cast<uint32_t*>(ring);
+  const bool cached = n_cand <= kSelCacheKeys;
+  // digit 1: the 16-bit bin where the count from the top reaches k.  Warp w
+  // owns bins [2048 w, 2048 w + 2048) and reads them coalesced; the warp
+  // holding the bin then narrows it down to a lane's 64 bins, then to the bin.
+  __shared__ int wcount[32];
+  __shared__ int sh_above;
+  {
+    const int* hg = p.hist + (static_cast<long>(g) << 16);
+    const int4* h4 = reinterpret_cast<const int4*>(hg + 2048 * w);
+    int cw = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int4 v = __ldcg(h4 + 32 * j + lane);
+      cw += (v.x + v.y) + (v.z + v.w);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cw += __shfl_xor_sync(0xffffffffu, cw, o);
+    if (lane == 0) wcount[w] = cw;
     __syncthreads();
-    for (int i = threadIdx.x; i < n_cand; i += blockDim.x) {
-      const uint32_t key = key_at(i);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (nbins - 1)], 1);
+    if (w == 0) {                                 // from the top: lane l holds warp 31 - l
+      const int c = wcount[31 - lane];
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (x - c < k && x >= k) {
+        sh_digit = static_cast<uint32_t>(31 - lane);
+        sh_above = x - c;
+      }
     }
     __syncthreads();
-    // Bin counts from the top: thread t owns bins [2t, 2t+1] of the reversed order.
-    const int b_hi = nbins - 1 - 2 * static_cast<int>(threadIdx.x);
-    const int c0 = (2 * static_cast<int>(threadIdx.x) < nbins) ? hist[b_hi] : 0;
-    const int c1 = (2 * static_cast<int>(threadIdx.x) + 1 < nbins) ? hist[b_hi - 1] : 0;
+    const int bw = static_cast<int>(sh_digit);
+    if (w == bw) {
+      // lane l: bins [2048 bw + 64 l, +64), counted from the top (lane 31 first)
+      const int4* l4 = reinterpret_cast<const int4*>(hg + 2048 * bw + 64 * lane);
+      int cl = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int4 v = __ldcg(l4 + j);
+        cl += (v.x + v.y) + (v.z + v.w);
+      }
+      const int c = __shfl_sync(0xffffffffu, cl, 31 - lane);
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const int above_w = sh_above;
+      const int hit = __ballot_sync(0xffffffffu, above_w + x - c < k && above_w + x >= k);
+      const int src = __ffs(hit) - 1;             // exactly one lane
+      const int bl = 31 - src;                    // the lane range holding the bin
+      const int run0 = above_w + __shfl_sync(0xffffffffu, x - c, src);
+      // that range's 64 bins, two per lane from the top
+      const int* hb = hg + 2048 * bw + 64 * bl;
+      const int c0 = __ldcg(hb + 63 - 2 * lane), c1 = __ldcg(hb + 62 - 2 * lane);
+      int y = c0 + c1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int z = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) y += z;
+      }
+      const int ex = run0 + y - (c0 + c1);        // keys above this lane's two bins
+      if (ex < k && ex + c0 >= k) {
+        sh_digit = static_cast<uint32_t>(2048 * bw + 64 * bl + 63 - 2 * lane);
+        sh_need = k - ex;
+        sh_above = c0;                            // keys in the bin
+      } else if (ex + c0 < k && ex + c0 + c1 >= k) {
+        sh_digit = static_cast<uint32_t>(2048 * bw + 64 * bl + 62 - 2 * lane);
+        sh_need = k - ex - c0;
+        sh_above = c1;
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t b16 = sh_digit;
+  const int in_bin = sh_above;                    // keys in the boundary bin
+  const int list_n = k - sh_need + in_bin;        // keys above the bin, and the bin's
+  if (list_n <= kSelSortMax) {
+    // Fast path: those keys (with their indices) into shared memory, sorted by
+    // key descending and index ascending; the first k are kept, then sorted by
+    // index for the output.
+    unsigned long long* list = reinterpret_cast<unsigned long long*>(
+        reinterpret_cast<char*>(ring) + kSelCacheBytes);
+    uint32_t* idx = reinterpret_cast<uint32_t*>(list + kSelSortMax);
+    __shared__ int n_list;
+    if (tid == 0) n_list = 0;
+    __syncthreads();
+    const uint32_t below = (1u << lane) - 1u;
+    constexpr int kU = 8;                         // loads in flight per thread
+    for (int base0 = 0; base0 < n_cand; base0 += kU * nt) {   // warp-uniform steps
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base0 + tid + u * nt;
+        v[u] = i < n_cand ? __ldcg(sc + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base0 + tid + u * nt;
+        const uint32_t key = order_key(v[u]);
+        const bool take = i < n_cand && (key >> 16) >= b16;
+        const uint32_t m = __ballot_sync(0xffffffffu, take);
+        if (m) {
+          const int leader = __ffs(m) - 1;
+          int at = 0;
+          if (lane == leader) at = atomicAdd(&n_list, __popc(m));
+          at = __shfl_sync(0xffffffffu, at, leader) + __popc(m & below);
+          if (take && at < kSelSortMax)
+            list[at] = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
+        }
+      }
+    }
+    __syncthreads();
+    int np = 1;
+    while (np < list_n) np <<= 1;
+    for (int i = list_n + tid; i < np; i += nt) list[i] = 0ull;   // below every real entry
+    __syncthreads();
+    int kp = 1;
+    while (kp < k) kp <<= 1;
+    block_bitonic_sort(list, np, true);
+    for (int i = tid; i < kp; i += nt)
+      idx[i] = i < k ? 0xFFFFFFFFu - static_cast<uint32_t>(list[i] & 0xFFFFFFFFull) : 0xFFFFFFFFu;
+    __syncthreads();
+    block_bitonic_sort(idx, kp, false);
+    for (int i = tid; i < k; i += nt) out[i] = static_cast<int32_t>(idx[i]);
+    return;
+  }
+  uint32_t prefix = sh_digit << 16;               // the k-th key's bits found so far
+  int need = sh_need;                             // keys still to take with that prefix
+  // digits 2 and 3: 8 bits each, over the keys that share the prefix
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shb = 8 - 8 * pass;                 // bits [shb, shb + 8)
+    const uint32_t mask = 0xFFFFFFFFu << (shb + 8);
+    for (int i = tid; i < 256; i += nt) hist[i] = 0;
+    __syncthreads();
+    constexpr int kU = 8;                         // loads in flight per thread
+    for (int base0 = 0; base0 < n_cand; base0 += kU * nt) {   // warp-uniform steps
+      uint32_t key[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base0 + tid + u * nt;
+        key[u] = 0u;
+        if (i < n_cand) {
+          if (pass == 0 || !cached) {
+            key[u] = order_key(__ldcg(sc + i));
+            if (pass == 0 && cached) keys_sm[i] = key[u];
+          } else {
+            key[u] = keys_sm[i];
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base0 + tid + u * nt;
+        const bool in = i < n_cand && (key[u] & mask) == prefix;
+        const int b = in ? static_cast<int>((key[u] >> shb) & 255u) : -1;
+        // a warp whose 32 keys fall in one bin (many equal keys) adds once
+        const int b0 = __shfl_sync(0xffffffffu, b, 0);
+        if (__all_sync(0xffffffffu, b == b0)) {
+          if (lane == 0 && b0 >= 0) atomicAdd(&hist[b0], 32);
+        } else if (in) {
+          atomicAdd(&hist[b], 1);
+        }
+      }
+    }
+    __syncthreads();
+    // bin counts from the top: thread t < 128 owns bins 255 - 2t and 254 - 2t
+    const int b_hi = 255 - 2 * tid;
+    const int c0 = tid < 128 ? hist[b_hi] : 0;
+    const int c1 = tid < 128 ? hist[b_hi - 1] : 0;
     const int before = block_excl_scan(c0 + c1, warp_tot, &total);
-    // the bin where the running count from the top first reaches `need`
-    if (2 * static_cast<int>(threadIdx.x) < nbins) {
+    if (tid < 128) {
       if (before < need && before + c0 >= need) {
-        sh_prefix = prefix | (static_cast<uint32_t>(b_hi) << sh);
+        sh_digit = static_cast<uint32_t>(b_hi);
         sh_need = need - before;
-      } else if (2 * static_cast<int>(threadIdx.x) + 1 < nbins && before + c0 < need &&
-                 before + c0 + c1 >= need) {
-        sh_prefix = prefix | (static_cast<uint32_t>(b_hi - 1) << sh);
+      } else if (before + c0 < need && before + c0 + c1 >= need) {
+        sh_digit = static_cast<uint32_t>(b_hi - 1);
         sh_need = need - before - c0;
       }
     }
     __syncthreads();
-    prefix = sh_prefix;
+    prefix |= sh_digit << shb;
     need = sh_need;
-    mask |= static_cast<uint32_t>(nbins - 1) << sh;
-    lo_bit = sh;
     __syncthreads();
   }
-  // prefix == T (the k-th key), need == how many keys equal to T are kept.
+  // prefix is the k-th key, need == how many keys equal to it are kept.
   // Index-ordered compaction: warp w owns the contiguous index range
-  // [w * span, (w + 1) * span) and walks it 32 consecutive indices at a time
+  // [w span, (w + 1) span) and walks it 32 consecutive indices at a time
   // (lane = index within the step: conflict-free shared loads), so ballots
   // give each key's rank in index order.
-  const uint32_t T = prefix;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
+  const uint32_t kth = prefix;
+  auto key_at = [&](int i) -> uint32_t { return cached ? keys_sm[i] : order_key(__ldcg(sc + i)); };
+  const int nw = nt >> 5;
   const int span = ((n_cand + nw - 1) / nw + 31) & ~31;
-  const int j0 = w * span, j1 = min(n_cand, j0 + span);
+  const int j0 = min(n_cand, w * span), j1 = min(n_cand, j0 + span);
   const uint32_t below = (1u << lane) - 1u;
-  int n_eq = 0;
-  for (int base = j0; base < j1; base += 32) {
-    const int i = base + lane;
-    n_eq += __popc(__ballot_sync(0xffffffffu, i < j1 && key_at(i) == T));
-  }
-  // exclusive scan over warps of the equal-key counts, then of the kept counts
-  __shared__ int wsum[32];
-  if (lane == 0) wsum[w] = n_eq;
-  __syncthreads();
-  int eq_before = 0;
-  for (int u = 0; u < w; ++u) eq_before += wsum[u];
-  __syncthreads();
-  int n_keep = 0, eq_rank = eq_before;
+  int n_gt = 0, n_eq = 0;
   for (int base = j0; base < j1; base += 32) {
     const int i = base + lane;
     const uint32_t key = i < j1 ? key_at(i) : 0u;
-    const uint32_t eqm = __ballot_sync(0xffffffffu, i < j1 && key == T);
-    const bool keep = i < j1 && (key > T || (key == T && eq_rank + __popc(eqm & below) < need));
-    n_keep += __popc(__ballot_sync(0xffffffffu, keep));
-    eq_rank += __popc(eqm);
+    n_gt += __popc(__ballot_sync(0xffffffffu, i < j1 && key > kth));
+    n_eq += __popc(__ballot_sync(0xffffffffu, i < j1 && key == kth));
   }
-  if (lane == 0) wsum[w] = n_keep;
+  int* wsum_gt = reinterpret_cast<int*>(hist);          // the digit histogram is done
+  int* wsum_eq = wsum_gt + 32;
+  if (lane == 0) {
+    wsum_gt[w] = n_gt;
+    wsum_eq[w] = n_eq;
+  }
   __syncthreads();
-  int pos = 0;
-  for (int u = 0; u < w; ++u) pos += wsum[u];
-  eq_rank = eq_before;
+  int eq_rank = 0, pos = 0;
+  for (int u = 0; u < w; ++u) {
+    const int e = wsum_eq[u];
+    pos += wsum_gt[u] + max(0, min(e, need - eq_rank));
+    eq_rank += e;
+  }
   for (int base = j0; base < j1; base += 32) {
     const int i = base + lane;
     const uint32_t key = i < j1 ? key_at(i) : 0u;
-    const uint32_t eqm = __ballot_sync(0xffffffffu, i < j1 && key == T);
-    const bool keep = i < j1 && (key > T || (key == T && eq_rank + __popc(eqm & below) < need));
+    const uint32_t eqm = __ballot_sync(0xffffffffu, i < j1 && key == kth);
+    const bool keep = i < j1 && (key > kth || (key == kth && eq_rank + __popc(eqm & below) < need));
     const uint32_t km = __ballot_sync(0xffffffffu, keep);
-    if (keep) out[pos + __popc(km & below)] = i;
+    const int at = pos + __popc(km & below);
+    if (keep && at < k) out[at] = i;              // k writes in all, by the counts above
     pos += __popc(km);
     eq_rank += __popc(eqm);
   }
@@ -574,7 +759,6 @@ __global__ void debug_wait_kernel(int* status, uint64_t limit_ns) {
   __shared__ alignas(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
-    abort_flag = 0;
     mbar_init(smem_u32(&bar), 1);
     fence_barrier_init();
     WaitCtl wc{status, &abort_flag, limit_ns};
@@ -593,55 +777,96 @@ cudaError_t launch_page_reps(const KvDesc& kv, bool bf16, int first_page, int n_
 }
 
 size_t select_ws_bytes(int num_pages, int hkv, int head_dim) {
+  const size_t row = static_cast<size_t>(hkv) * head_dim * 4;
   size_t b = kStatusBytes;
-  b += align_up(static_cast<size_t>(kQbarBlocks) * hkv * head_dim * 4, 256);  // partials
-  b += align_up(static_cast<size_t>(hkv) * head_dim * 4, 256);                // qbar
+  b += align_up(kSelMaxBlocks * row, 256);                                    // partials
+  b += align_up((kSelMaxBlocks / kSelGroup) * row, 256);                      // group sums
+  b += align_up(row, 256);                                                    // qbar
   b += align_up(static_cast<size_t>(hkv) * num_pages * 4, 256);              // scores
+  b += static_cast<size_t>(hkv) * 65536 * 4;                                  // key histogram
   return b;
 }
 
-cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, int n_cand,
-                               const float* reps, int num_pages, int hkv, int head_dim, int top_k,
-                               int32_t* sel, float* scores_opt, void* ws, cudaStream_t st) {
-  char* w = static_cast<char*>(ws);
-  int* status = reinterpret_cast<int*>(w);
-  float* partials = reinterpret_cast<float*>(w + kStatusBytes);
-  float* qbar = reinterpret_cast<float*>(
-      w + kStatusBytes + align_up(static_cast<size_t>(kQbarBlocks) * hkv * head_dim * 4, 256));
-  float* scores = scores_opt ? scores_opt
-                             : reinterpret_cast<float*>(reinterpret_cast<char*>(qbar) +
-                                                        align_up(static_cast<size_t>(hkv) *
-                                                                     head_dim * 4, 256));
-  // R token rows per step of hq*head_dim floats each, or the tree's 7 x hkv*head_dim
-  const size_t row_vecs = static_cast<size_t>(hq) * head_dim / (bf16 ? 8 : 4);
-  const size_t rows = kQbarThreads / row_vecs;
-  const size_t a = rows * hq * head_dim, b = 7 * static_cast<size_t>(hkv) * head_dim;
-  const size_t qsm = sizeof(float) * (a > b ? a : b);
-  if (bf16)
-    qbar_kernel<__nv_bfloat16><<<kQbarBlocks, kQbarThreads, qsm, st>>>(
-        static_cast<const __nv_bfloat16*>(q), chunk_len, hq, hkv, head_dim, partials, qbar,
-        status);
-  else
-    qbar_kernel<float><<<kQbarBlocks, kQbarThreads, qsm, st>>>(
-        static_cast<const float*>(q), chunk_len, hq, hkv, head_dim, partials, qbar, status);
-  cudaError_t e = cudaGetLastError();
+namespace {
+// The grid of the selection kernel on the current device: every CTA must be
+// resident at once (cooperative launch), one per SM.
+template <typename T, int D>
+cudaError_t sel_grid(int* blocks) {
+  static PerDeviceOnce once;
+  static int cached[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int blocks = 152 * 8;
-  if (head_dim == 128)
-    page_scores_kernel<128><<<blocks, 256, 0, st>>>(reps, qbar, n_cand, num_pages, hkv, scores);
-  else
-    page_scores_kernel<64><<<blocks, 256, 0, st>>>(reps, qbar, n_cand, num_pages, hkv, scores);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || top_k == 0 || n_cand == 0) return e;
-  const size_t ksm = n_cand <= kTopkSmemKeys ? static_cast<size_t>(n_cand) * 4 : 0;
-  static PerDeviceOnce attr;
-  e = once_per_device(attr, [] {
-    return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kTopkSmemKeys * 4);
+  e = once_per_device(once, [&] {
+    cudaError_t r = cudaFuncSetAttribute(select_kernel<T, D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSelDynSmem));
+    if (r != cudaSuccess) return r;
+    int sms = 0, per_sm = 0;
+    r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (r != cudaSuccess) return r;
+    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_kernel<T, D>, kSelThreads,
+                                                      kSelDynSmem);
+    if (r != cudaSuccess) return r;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    cached[dev & 127] = sms < kSelMaxBlocks ? sms : kSelMaxBlocks;
+    return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  topk_kernel<<<hkv, kTopkThreads, ksm, st>>>(scores, num_pages, n_cand, top_k, sel);
-  return cudaGetLastError();
+  *blocks = cached[dev & 127];
+  return cudaSuccess;
+}
+
+template <typename T, int D>
+cudaError_t launch_select(const SelParams& prm, cudaStream_t st) {
+  int blocks = 0;
+  cudaError_t e = sel_grid<T, D>(&blocks);
+  if (e != cudaSuccess) return e;
+  if (blocks < prm.hkv) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = kSelDynSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: they wait for one another
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, select_kernel<T, D>, prm);
+}
+}  // namespace
+
+cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, int n_cand,
+                               const float* reps, int num_pages, int hkv, int head_dim, int top_k,
+                               int32_t* sel, float* scores_opt, void* ws, uint64_t wait_ns,
+                               cudaStream_t st) {
+  const size_t row = static_cast<size_t>(hkv) * head_dim * 4;
+  char* w = static_cast<char*>(ws);
+  SelParams prm;
+  prm.status = reinterpret_cast<int*>(w);
+  w += kStatusBytes;
+  prm.partials = reinterpret_cast<float*>(w);
+  w += align_up(kSelMaxBlocks * row, 256);
+  prm.gsums = reinterpret_cast<float*>(w);
+  w += align_up((kSelMaxBlocks / kSelGroup) * row, 256);
+  prm.qbar = reinterpret_cast<float*>(w);
+  w += align_up(row, 256);
+  float* scores_ws = reinterpret_cast<float*>(w);
+  w += align_up(static_cast<size_t>(hkv) * num_pages * 4, 256);
+  prm.hist = reinterpret_cast<int*>(w);
+  prm.scores = scores_opt ? scores_opt : scores_ws;
+  prm.q = q;
+  prm.reps = reps;
+  prm.sel = sel;
+  prm.chunk_len = chunk_len;
+  prm.hq = hq;
+  prm.hkv = hkv;
+  prm.n_cand = n_cand;
+  prm.num_pages = num_pages;
+  prm.top_k = top_k;
+  prm.wait_ns = wait_ns;
+  return bf16 ? launch_select<__nv_bfloat16, 128>(prm, st) : launch_select<float, 64>(prm, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -676,7 +901,7 @@ cudaError_t select_scratch_addr(void** out) {
 cudaError_t launch_select_topk_noalloc(const void* q, bool bf16, int hq, int chunk_len,
                                        int n_cand, const float* reps, int num_pages, int hkv,
                                        int head_dim, int top_k, int32_t* sel, float* scores_opt,
-                                       bool* too_big, cudaStream_t st) {
+                                       bool* too_big, uint64_t wait_ns, cudaStream_t st) {
   *too_big = select_ws_bytes(num_pages, hkv, head_dim) > OOMB_NOALLOC_SCRATCH_BYTES;
   if (*too_big) return cudaSuccess;
   void* scratch = nullptr;
@@ -686,7 +911,7 @@ cudaError_t launch_select_topk_noalloc(const void* q, bool bf16, int hq, int chu
   e = cudaMemsetAsync(scratch, 0, kStatusBytes, st);
   if (e != cudaSuccess) return e;
   return launch_select_topk(q, bf16, hq, chunk_len, n_cand, reps, num_pages, hkv, head_dim,
-                            top_k, sel, scores_opt, scratch, st);
+                            top_k, sel, scores_opt, scratch, wait_ns, st);
 }
 
 cudaError_t launch_validate_page_table(const int32_t* pt, int num_pages, int num_slots,

@@ -262,7 +262,7 @@ oomb_status oomb_select_topk(const void* q, int32_t num_q_heads, int32_t chunk_l
   if (s != OOMB_OK) return s;
   cudaError_t e = oomb::launch_select_topk(q, kv->dtype == OOMB_BF16, num_q_heads, chunk_len,
                                            n_cand, reps, kv->num_pages, kv->num_kv_heads,
-                                           kv->head_dim, n_sel, sel, scores_opt, ws,
+                                           kv->head_dim, n_sel, sel, scores_opt, ws, g_wait_ns,
                                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OOMB_OK : cuda_fail(e, "oomb_select_topk launch");
 }
@@ -289,7 +289,7 @@ oomb_status oomb_select_topk_noalloc(const void* q, int32_t num_q_heads, int32_t
   bool too_big = false;
   cudaError_t e = oomb::launch_select_topk_noalloc(
       q, kv->dtype == OOMB_BF16, num_q_heads, chunk_len, n_cand, reps, kv->num_pages,
-      kv->num_kv_heads, kv->head_dim, n_sel, sel, scores_opt, &too_big,
+      kv->num_kv_heads, kv->head_dim, n_sel, sel, scores_opt, &too_big, g_wait_ns,
       static_cast<cudaStream_t>(stream));
   if (too_big)
     return fail(OOMB_ERR_INVALID_ARG,

@@ -31,11 +31,17 @@ struct NvtxRange {
 
 // Workspace: a 256-byte status block first.
 //   int[0] status code (0 = ok), int[1] where, int[2] block
-//   int[16] qbar "last block" ticket counter (self-resetting)
+//   int[16] query-summary ticket counter of the groups (self-resetting)
 //   int[17] debug flag that nothing sets
+//   int[18] selection: query summary published (generation, counts up)
+//   int[19] selection: CTAs done scoring (counts up)
+//   int[32..32+kQbarBlocks/8) query-summary ticket counters within each group
 constexpr size_t kStatusBytes = 256;
 constexpr int kTicketIdx = 16;
 constexpr int kDebugFlagIdx = 17;
+constexpr int kSelQbarGenIdx = 18;      // query summary published (generation counter)
+constexpr int kSelScoreCntIdx = 19;     // CTAs done scoring (monotonic counter)
+constexpr int kGroupTicketIdx = 32;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -64,6 +70,7 @@ cudaError_t once_per_device(PerDeviceOnce& once, F&& fn) {
 enum Where : int {
   kWhereReps = 10,
   kWhereTopk = 20,
+  kWhereSelect = 21,
   kWhereFwdProducer = 30,
   kWhereFwdMma = 31,
   kWhereFwdSoftmax = 32,
@@ -88,17 +95,17 @@ struct KvDesc {
 // last_rows: rows of the last page of the range that hold keys (P: whole pages)
 cudaError_t launch_page_reps(const KvDesc& kv, bool bf16, int first_page, int n_pages,
                              int last_rows, float* reps, int* status, cudaStream_t st);
-constexpr int kQbarBlocks = 152;
 size_t select_ws_bytes(int num_pages, int hkv, int head_dim);
 cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, int n_cand,
                                const float* reps, int num_pages, int hkv, int head_dim, int top_k,
-                               int32_t* sel, float* scores_opt, void* ws, cudaStream_t st);
+                               int32_t* sel, float* scores_opt, void* ws, uint64_t wait_ns,
+                               cudaStream_t st);
 // The selection with its scratch in a fixed device array of the library
 // (oomb_select_topk_noalloc); sets *too_big when the shapes need more.
 cudaError_t launch_select_topk_noalloc(const void* q, bool bf16, int hq, int chunk_len,
                                        int n_cand, const float* reps, int num_pages, int hkv,
                                        int head_dim, int top_k, int32_t* sel, float* scores_opt,
-                                       bool* too_big, cudaStream_t st);
+                                       bool* too_big, uint64_t wait_ns, cudaStream_t st);
 cudaError_t launch_validate_page_table(const int32_t* pt, int num_pages, int num_slots,
                                        uint32_t* bitmap, int* status, cudaStream_t st);
 cudaError_t launch_debug_wait(int* status, uint64_t limit_ns, cudaStream_t st);
