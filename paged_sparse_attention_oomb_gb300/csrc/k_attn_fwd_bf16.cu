@@ -160,28 +160,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     const int32_t* sel_g = p.sel + static_cast<long>(g) * p.n_sel;
     int issued = 0;                                // ring loads issued (K_0, V_0, K_1, ...)
-    for (int j = 0; j < n_tiles; ++j) {
-      int rows[8];
-      for (int u = 0; u < ppt; ++u) {
-        int lp;
-        if (j < p.t_sel) {
-          const int pi = j * ppt + u;
-          lp = sel_g[pi < p.n_sel ? pi : 0];
-          if (lp < 0 || lp >= own_page0) {
-            raise_status(p.status, kStatusBounds, kWhereFwdProducer);
-            lp = own_page0;
-          }
-        } else {
-          lp = own_page0 + (j - p.t_sel) * ppt + u;
-          if (lp >= own_page0 + n_own_pages) lp = own_page0;
+    // Page lookups run ahead of the loads that need them, in three stages one
+    // key tile apart: the selection entry of tile j+2, then the page table
+    // entry of tile j+1, then the row of tile j -- each load's value is first
+    // used a tile later, so its latency hides behind a tile's work.  Lane u
+    // (< pages per tile) resolves page u of a tile.  An entry out of range is
+    // recorded when its tile is loaded, and never followed (row 0 instead).
+    const bool my_page = lane < ppt;
+    auto sel_raw = [&](int j) -> int {             // stage A: selection entry
+      if (!my_page || j >= n_tiles || j >= p.t_sel) return 0;
+      const int pi = j * ppt + lane;
+      return sel_g[pi < p.n_sel ? pi : 0];
+    };
+    auto page_of = [&](int j, int raw, bool* bad) -> int {   // stage B: logical page
+      *bad = false;
+      if (!my_page || j >= n_tiles) return own_page0;
+      if (j < p.t_sel) {
+        if (raw < 0 || raw >= own_page0) {
+          *bad = true;
+          return own_page0;
         }
-        int slot = p.pt[lp];
-        if (slot < 0 || slot >= p.num_slots) {
-          raise_status(p.status, kStatusBounds, kWhereFwdProducer);
-          slot = 0;
-        }
-        rows[u] = (slot * p.hkv + g) * p.page_size;
+        return raw;
       }
+      const int lp = own_page0 + (j - p.t_sel) * ppt + lane;
+      return lp < own_page0 + n_own_pages ? lp : own_page0;
+    };
+    bool bad_b;
+    int slot_b = p.pt[page_of(0, sel_raw(0), &bad_b)];        // tile 0, stages A and B
+    int raw_a = sel_raw(1);                                     // tile 1, stage A
+    for (int j = 0; j < n_tiles; ++j) {
+      const int slot = slot_b;                                  // tile j (stage C)
+      const bool bad_lp = bad_b;
+      const int lp_next = page_of(j + 1, raw_a, &bad_b);        // tile j+1 (stage B)
+      slot_b = (my_page && j + 1 < n_tiles) ? p.pt[lp_next] : 0;
+      raw_a = sel_raw(j + 2);                                   // tile j+2 (stage A)
+      const bool bad = my_page && (bad_lp || slot < 0 || slot >= p.num_slots);
+      if (__any_sync(0xffffffffu, bad)) raise_status(p.status, kStatusBounds, kWhereFwdProducer);
+      const int row = (my_page && !bad) ? (slot * p.hkv + g) * p.page_size : 0;
+      int rows[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) rows[u] = __shfl_sync(0xffffffffu, row, u);
       bool ok = true;
       for (int kv = 0; kv < 2 && ok; ++kv) {
         const int q = 2 * j + kv;
