@@ -759,6 +759,7 @@ __global__ void debug_wait_kernel(int* status, uint64_t limit_ns) {
   __shared__ alignas(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
+    abort_flag = 0;
     mbar_init(smem_u32(&bar), 1);
     fence_barrier_init();
     WaitCtl wc{status, &abort_flag, limit_ns};
