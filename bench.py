@@ -320,7 +320,7 @@ class PathStep:
     representatives of all pages -> Top-K selection -> forward -> backward
     (dK/dV in place), the four C ABI calls, on the current stream."""
     NAMES = ["page_reps", "select_topk", "attn_fwd", "attn_bwd"]
-    LAUNCHES = 1 + 3 + 1 + 3          # kernels per step: reps; qbar/scores/top-k; fwd; prep/bwd/convert
+    LAUNCHES = 1 + 1 + 1 + 3          # kernels per step: reps; selection; fwd; prep/bwd/convert
 
     def __init__(self, wl, dev):
         from paged_sparse_attention_oomb_gb300 import oomb
@@ -449,10 +449,25 @@ def measure_configs(names, dev, steps, warmup, pk, peak_key):
 OTHER_CONFIGS = ["qwen7b_ctx256k_k64", "qwen7b_ctx1m_k128", "qwen7b_dense_ctx32k"]
 
 
+def workload_of(args):
+    """The named workload, or with ``--context`` the same chunk, heads, page
+    size and Top-K over a shorter cache: the attention kernels then do the same
+    work per launch (the same number of selected and own pages) on a pool that
+    fits a profiler's capture."""
+    wl = WORKLOADS[args.workload]
+    ctx = args.context
+    if not ctx or ctx == wl.context:
+        return wl
+    if ctx % wl.page_size or (ctx - wl.chunk_len) // wl.page_size < min(wl.top_k, 1 << 20):
+        raise SystemExit(f"--context {ctx}: needs whole pages of {wl.page_size} and at least "
+                         f"top_k={wl.top_k} candidate pages before the last chunk")
+    return wl.with_(name=f"{wl.name}@ctx{ctx}", context=ctx)
+
+
 def run_ours(args, rank, world, dev):
     from paged_sparse_attention_oomb_gb300 import oomb
 
-    wl = WORKLOADS[args.workload]
+    wl = workload_of(args)
     torch.cuda.set_device(dev)
     step = PathStep(wl, dev)
     x, kv, stream = step.x, step.kv, step.stream
@@ -656,7 +671,7 @@ def cpu_baseline(wl, st, rows, reps=1):
 
 
 def run_reference(args, rank, world):
-    wl = WORKLOADS[args.workload]
+    wl = workload_of(args)
     if rank != 0:
         return None
     st = oracle_setup(wl)
@@ -703,6 +718,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--context", type=int, default=0,
+                    help="shorter cache for the workload (same chunk, Top-K and heads): "
+                         "a small case for profiler captures")
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")

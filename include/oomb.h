@@ -25,7 +25,8 @@
  *   - Argument errors are detected on the host and returned before anything
  *     is launched (OOMB_ERR_INVALID_ARG / OOMB_ERR_UNSUPPORTED, with a message
  *     from oomb_last_error()).  Errors found on the device (a bounded wait that
- *     timed out, an index out of range) are recorded in the status word at the
+ *     timed out, an index out of range, a non-finite unused row of a partial
+ *     last page) are recorded in the status word at the
  *     start of `ws` and read with oomb_device_status.  No call traps or
  *     asserts on the device.
  *   - Tensor layouts (row-major, innermost last):
@@ -56,6 +57,11 @@
  *     tensor-core kernels load them with the page and weight them by zero, so
  *     their K and V values must be finite (a zero-initialised pool is; in fp8
  *     backing pools of an offload cache, codes other than the NaN codes).
+ *     On bf16 pools oomb_sparse_attn_fwd(_own_reps) and oomb_sparse_attn_bwd
+ *     check those rows first whenever the chunk ends inside a page (one small
+ *     launch reading only the unused rows) and record OOMB_ERR_NONFINITE in
+ *     the workspace status when any of them holds an inf or a NaN; the
+ *     outputs of that call are then not meaningful.
  */
 #ifndef OOMB_H
 #define OOMB_H
@@ -73,7 +79,9 @@ typedef enum {
   OOMB_ERR_UNSUPPORTED = 2,   /* valid request this build does not serve */
   OOMB_ERR_CUDA = 3,          /* a CUDA runtime call failed              */
   OOMB_ERR_TIMEOUT = 4,       /* a device-side bounded wait gave up      */
-  OOMB_ERR_DEVICE_BOUNDS = 5  /* a device-side index check failed        */
+  OOMB_ERR_DEVICE_BOUNDS = 5, /* a device-side index check failed        */
+  OOMB_ERR_NONFINITE = 6      /* inf/NaN in the unused rows of a partial
+                                 last page (device check, bf16 pools)     */
 } oomb_status;
 
 /* OOMB_FP8_E4M3: 8-bit E4M3 codes (OCP 8-bit floating point specification),
@@ -354,8 +362,9 @@ oomb_status oomb_offload_stats(const oomb_offload *h, int64_t *out);
 void oomb_offload_destroy(oomb_offload *h);
 
 /* Reads and clears the device status word at the start of ws (synchronises
- * `stream`).  Returns OOMB_OK, OOMB_ERR_TIMEOUT or OOMB_ERR_DEVICE_BOUNDS;
- * info (optional, 2 ints) receives {where, block} of the first error. */
+ * `stream`).  Returns OOMB_OK, OOMB_ERR_TIMEOUT, OOMB_ERR_DEVICE_BOUNDS or
+ * OOMB_ERR_NONFINITE; info (optional, 2 ints) receives {where, block} of the
+ * first error. */
 oomb_status oomb_device_status(void *ws, void *stream, int32_t *info);
 
 /* Upper bound, in nanoseconds, of every device-side wait (default 2e9).

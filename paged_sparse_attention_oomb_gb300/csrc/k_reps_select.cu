@@ -754,6 +754,30 @@ __global__ void validate_pt_kernel(const int32_t* __restrict__ pt, int num_pages
   if (atomicOr(&bitmap[s >> 5], bit) & bit) raise_status(status, kStatusBounds, 2);
 }
 
+// The rows of a partial last page past the chunk's end hold no token.  The
+// tensor-core attention kernels still load them with the page and weight them
+// by zero, so an inf or NaN there would reach O and dQ (0 * inf); this reads
+// only those rows, one CTA per KV head, and records kStatusNonFinite.
+__global__ void __launch_bounds__(256) tail_rows_kernel(const uint16_t* __restrict__ k,
+                                                        const uint16_t* __restrict__ v,
+                                                        const int32_t* __restrict__ pt, int page,
+                                                        int valid_rows, int page_size, int hkv,
+                                                        int d, int num_slots, int* status) {
+  const int slot = pt[page];
+  if (slot < 0 || slot >= num_slots) {
+    if (threadIdx.x == 0) raise_status(status, kStatusBounds, kWhereTailRows);
+    return;
+  }
+  const int g = blockIdx.x;
+  const size_t base = ((static_cast<size_t>(slot) * hkv + g) * page_size + valid_rows) * d;
+  const int n = (page_size - valid_rows) * d;
+  bool bad = false;
+  for (int i = threadIdx.x; i < n; i += blockDim.x)   // bf16 inf/NaN: all exponent bits set
+    bad |= ((k[base + i] & 0x7f80u) == 0x7f80u) | ((v[base + i] & 0x7f80u) == 0x7f80u);
+  if (__syncthreads_or(bad) && threadIdx.x == 0)
+    raise_status(status, kStatusNonFinite, kWhereTailRows);
+}
+
 // A wait on an mbarrier nothing arrives on: exercises the bounded-wait path.
 __global__ void debug_wait_kernel(int* status, uint64_t limit_ns) {
   __shared__ alignas(8) uint64_t bar;
@@ -920,6 +944,16 @@ cudaError_t launch_validate_page_table(const int32_t* pt, int num_pages, int num
   if (num_pages == 0) return cudaSuccess;
   validate_pt_kernel<<<(num_pages + 255) / 256, 256, 0, st>>>(pt, num_pages, num_slots, bitmap,
                                                               status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_check_tail_rows(const KvDesc& kv, int page, int valid_rows, int* status,
+                                   cudaStream_t st) {
+  if (valid_rows <= 0 || valid_rows >= kv.page_size) return cudaSuccess;
+  tail_rows_kernel<<<kv.hkv, 256, 0, st>>>(static_cast<const uint16_t*>(kv.k),
+                                           static_cast<const uint16_t*>(kv.v), kv.page_table, page,
+                                           valid_rows, kv.page_size, kv.hkv, kv.head_dim,
+                                           kv.num_slots, status);
   return cudaGetLastError();
 }
 

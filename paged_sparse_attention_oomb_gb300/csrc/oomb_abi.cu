@@ -129,6 +129,7 @@ const char* oomb_status_string(int s) {
     case OOMB_ERR_CUDA: return "OOMB_ERR_CUDA";
     case OOMB_ERR_TIMEOUT: return "OOMB_ERR_TIMEOUT";
     case OOMB_ERR_DEVICE_BOUNDS: return "OOMB_ERR_DEVICE_BOUNDS";
+    case OOMB_ERR_NONFINITE: return "OOMB_ERR_NONFINITE";
     default: return "OOMB_ERR_UNKNOWN";
   }
 }
@@ -193,6 +194,9 @@ oomb_status oomb_device_status(void* ws, void* stream, int32_t* info) {
   if (h[0] == 0) return OOMB_OK;
   if (h[0] == OOMB_ERR_TIMEOUT)
     return fail(OOMB_ERR_TIMEOUT, "device wait timed out (where %d, block %d)", h[1], h[2]);
+  if (h[0] == OOMB_ERR_NONFINITE)
+    return fail(OOMB_ERR_NONFINITE, "inf or NaN in the unused rows of a partial last page "
+                "(KV head %d)", h[2]);
   return fail(OOMB_ERR_DEVICE_BOUNDS, "device index check failed (where %d, block %d)", h[1],
               h[2]);
 }
@@ -300,6 +304,16 @@ oomb_status oomb_select_topk_noalloc(const void* q, int32_t num_q_heads, int32_t
   return e == cudaSuccess ? OOMB_OK : cuda_fail(e, "oomb_select_topk_noalloc");
 }
 
+// A chunk that ends inside a page: check that the page's unused rows are finite
+// (the tensor-core kernels weight them by zero).
+static cudaError_t check_tail_rows(const oomb_paged_kv* kv, int chunk_len, int chunk_start,
+                                   int* status, cudaStream_t st) {
+  const int end = chunk_start + chunk_len;
+  const int P = kv->page_size;
+  if (end % P == 0) return cudaSuccess;
+  return oomb::launch_check_tail_rows(desc(kv), end / P, end % P, status, st);
+}
+
 static oomb_status attn_fwd(const char* name, const void* q, const oomb_paged_kv* kv,
                             const int32_t* sel, int32_t n_sel, int32_t num_q_heads,
                             int32_t chunk_len, int32_t chunk_start, float scale, void* o,
@@ -325,9 +339,11 @@ static oomb_status attn_fwd(const char* name, const void* q, const oomb_paged_kv
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (kv->dtype == OOMB_BF16) {
-    e = oomb::launch_attn_fwd_bf16(q, desc(kv), sel, n_sel, num_q_heads, chunk_len, chunk_start,
-                                   sc, o, o_lo, lse, own_reps, static_cast<int*>(ws), g_wait_ns,
-                                   st);
+    e = check_tail_rows(kv, chunk_len, chunk_start, static_cast<int*>(ws), st);
+    if (e == cudaSuccess)
+      e = oomb::launch_attn_fwd_bf16(q, desc(kv), sel, n_sel, num_q_heads, chunk_len, chunk_start,
+                                     sc, o, o_lo, lse, own_reps, static_cast<int*>(ws),
+                                     g_wait_ns, st);
   } else {
     e = oomb::launch_attn_fwd_fp32(static_cast<const float*>(q), desc(kv), sel, n_sel,
                                    num_q_heads, chunk_len, chunk_start, sc,
@@ -392,10 +408,12 @@ oomb_status oomb_sparse_attn_bwd(const void* q, const void* o, const void* o_lo,
   const float sc = resolve_scale(scale, kv->head_dim);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (kv->dtype == OOMB_BF16)
-    e = oomb::launch_attn_bwd_bf16(q, o, o_lo, dout, lse, desc(kv), sel, n_sel, num_q_heads,
-                                   chunk_len, chunk_start, sc, dq, ws, g_wait_ns, st);
-  else
+  if (kv->dtype == OOMB_BF16) {
+    e = check_tail_rows(kv, chunk_len, chunk_start, static_cast<int*>(ws), st);
+    if (e == cudaSuccess)
+      e = oomb::launch_attn_bwd_bf16(q, o, o_lo, dout, lse, desc(kv), sel, n_sel, num_q_heads,
+                                     chunk_len, chunk_start, sc, dq, ws, g_wait_ns, st);
+  } else
     e = oomb::launch_attn_bwd_fp32(static_cast<const float*>(q), static_cast<const float*>(o),
                                    static_cast<const float*>(dout), lse, desc(kv), sel, n_sel,
                                    num_q_heads, chunk_len, chunk_start, sc,

@@ -79,6 +79,7 @@ enum Where : int {
   kWhereBwdCompute = 42,
   kWhereBwdEpilogue = 43,
   kWhereFp32 = 50,
+  kWhereTailRows = 60,
   kWhereDebug = 90,
 };
 
@@ -108,6 +109,10 @@ cudaError_t launch_select_topk_noalloc(const void* q, bool bf16, int hq, int chu
                                        bool* too_big, uint64_t wait_ns, cudaStream_t st);
 cudaError_t launch_validate_page_table(const int32_t* pt, int num_pages, int num_slots,
                                        uint32_t* bitmap, int* status, cudaStream_t st);
+// bf16 pools: raises kStatusNonFinite when a K or V entry in rows [valid_rows, P)
+// of logical page `page` is inf or NaN.
+cudaError_t launch_check_tail_rows(const KvDesc& kv, int page, int valid_rows, int* status,
+                                   cudaStream_t st);
 cudaError_t launch_debug_wait(int* status, uint64_t limit_ns, cudaStream_t st);
 
 // --- k_attn_fp32.cu

@@ -69,16 +69,18 @@ __device__ __forceinline__ uint4 expand8(uint32_t w0, uint32_t w1) {   // 8 code
                     e4m3x2_to_bf16x2(static_cast<uint16_t>(w1 >> 16)));
 }
 
-// One CTA per tile of n16 16-byte words (of the destination): 8 loads in
-// flight per thread, then the stores.  Either side may be pinned host memory
-// (zero-copy) or device memory.  An expanding task reads n16 / 2 words of
-// codes and writes two words per word read; a zero fill only writes.  128
-// threads: small enough (in threads and registers) to share an SM with a
-// forward-attention CTA.
-constexpr int kCopyThreads = 128;
-__global__ void __launch_bounds__(kCopyThreads) tile_copy_kernel(
-    const TileCopy* __restrict__ tasks, int n16) {
-  const TileCopy t = tasks[blockIdx.x];
+// Tiles of n16 16-byte words (of the destination), tile blockIdx.x,
+// blockIdx.x + gridDim.x, ...: 8 loads in flight per thread, then the stores.
+// Either side may be pinned host memory (zero-copy) or device memory.  An
+// expanding task reads n16 / 2 words of codes and writes two words per word
+// read; a zero fill only writes.  64 threads (80 registers each): small
+// enough to share an SM with a running forward-attention CTA.  The grid is at
+// most one CTA per SM whatever the number of tiles: moves over the CPU-GPU
+// link are latency-bound, so a grid of one CTA per tile would take every SM
+// that an attention kernel frees for the whole length of the move, where a
+// bounded grid takes a few SMs' worth and keeps the link as busy.
+constexpr int kCopyThreads = 64;
+__device__ __forceinline__ void copy_tile(const TileCopy& t, int n16) {
   if (t.mode == kZeroFill) {
     for (int k = threadIdx.x; k < n16; k += kCopyThreads) t.dst[k] = make_uint4(0, 0, 0, 0);
     return;
@@ -116,6 +118,11 @@ __global__ void __launch_bounds__(kCopyThreads) tile_copy_kernel(
       if (k < n16) t.dst[k] = v[i];
     }
   }
+}
+
+__global__ void __launch_bounds__(kCopyThreads) tile_copy_kernel(
+    const TileCopy* __restrict__ tasks, int n_tasks, int n16) {
+  for (int i = blockIdx.x; i < n_tasks; i += gridDim.x) copy_tile(tasks[i], n16);
 }
 
 // Host threads that run the host-side tile copies of the staged path.  A
@@ -283,6 +290,7 @@ oomb_status take_stage(oomb_offload* h, Staging** out) {
 // Launch the copies list[0, n) (device-readable list) with the copy kernel.
 cudaError_t launch_list(const oomb_offload* h, const TileCopy* list, size_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
+  if (n > static_cast<size_t>(INT32_MAX)) return cudaErrorInvalidValue;
   // Same shared-memory carveout as the attention kernels, so that a copy CTA
   // can share an SM with one of theirs instead of waiting for the SM to drain.
   static oomb::PerDeviceOnce carveout;
@@ -293,8 +301,18 @@ cudaError_t launch_list(const oomb_offload* h, const TileCopy* list, size_t n, c
     });
     if (e != cudaSuccess) return e;
   }
-  tile_copy_kernel<<<static_cast<unsigned>(n), kCopyThreads, 0, s>>>(
-      list, static_cast<int>(h->tile_bytes / 16));
+  static oomb::PerDeviceOnce sm_once;
+  static int sms[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = oomb::once_per_device(sm_once, [dev] {
+    return cudaDeviceGetAttribute(&sms[dev & 127], cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (e != cudaSuccess) return e;
+  const size_t grid = std::min<size_t>(n, sms[dev & 127] > 0 ? sms[dev & 127] : 1);
+  tile_copy_kernel<<<static_cast<unsigned>(grid), kCopyThreads, 0, s>>>(
+      list, static_cast<int>(n), static_cast<int>(h->tile_bytes / 16));
   return cudaGetLastError();
 }
 

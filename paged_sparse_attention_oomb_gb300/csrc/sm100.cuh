@@ -79,6 +79,7 @@ struct WaitCtl {
 
 constexpr int kStatusTimeout = 4;
 constexpr int kStatusBounds = 5;
+constexpr int kStatusNonFinite = 6;
 
 __device__ __forceinline__ void raise_status(int* status, int code, int where) {
   if (atomicCAS(status, 0, code) == 0) {

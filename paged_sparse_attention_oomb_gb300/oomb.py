@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "liboomb.so")
 
 OOMB_OK, OOMB_ERR_INVALID_ARG, OOMB_ERR_UNSUPPORTED = 0, 1, 2
-OOMB_ERR_CUDA, OOMB_ERR_TIMEOUT, OOMB_ERR_DEVICE_BOUNDS = 3, 4, 5
+OOMB_ERR_CUDA, OOMB_ERR_TIMEOUT, OOMB_ERR_DEVICE_BOUNDS, OOMB_ERR_NONFINITE = 3, 4, 5, 6
 OOMB_BF16, OOMB_FP32, OOMB_FP8_E4M3 = 0, 1, 2
 OOMB_OP_VALIDATE, OOMB_OP_PAGE_REPS, OOMB_OP_SELECT_TOPK = 0, 1, 2
 OOMB_OP_ATTN_FWD, OOMB_OP_ATTN_BWD = 3, 4
@@ -41,7 +41,8 @@ class OombError(RuntimeError):
 
 
 _STATUS_NAMES = {0: "OOMB_OK", 1: "OOMB_ERR_INVALID_ARG", 2: "OOMB_ERR_UNSUPPORTED",
-                 3: "OOMB_ERR_CUDA", 4: "OOMB_ERR_TIMEOUT", 5: "OOMB_ERR_DEVICE_BOUNDS"}
+                 3: "OOMB_ERR_CUDA", 4: "OOMB_ERR_TIMEOUT", 5: "OOMB_ERR_DEVICE_BOUNDS",
+                 6: "OOMB_ERR_NONFINITE"}
 
 
 class OombOffloadDesc(ctypes.Structure):
@@ -509,6 +510,27 @@ class OffloadCache:
         _check(load().oomb_offload_create(ctypes.byref(desc), ctypes.byref(h)))
         self._h = h
 
+    def pass_state(self, dev, hq, chunk_len, top_k) -> dict:
+        """The copy stream, device page tables and workspaces of
+        chunk_recurrent_pass_offloaded for these shapes, made on first use and
+        kept, so that a pass does not allocate them each time."""
+        key = (str(dev), hq, chunk_len, top_k)
+        cached = getattr(self, "_pass_states", None)
+        if cached is None:
+            cached = self._pass_states = {}
+        if key not in cached:
+            pts = [torch.full((self.num_pages,), -1, dtype=torch.int32, device=dev)
+                   for _ in range(3)]
+            kv0 = self.device_kv(pts[0])
+            cached[key] = {
+                "copy": torch.cuda.Stream(dev, priority=-1),
+                "pts": pts[:2], "pt_last": pts[2],
+                "ws": [workspace(OOMB_OP_PAGE_REPS, kv0),
+                       workspace(OOMB_OP_SELECT_TOPK, kv0, hq, chunk_len, top_k),
+                       workspace(OOMB_OP_ATTN_FWD, kv0, hq, chunk_len),
+                       workspace(OOMB_OP_ATTN_BWD, kv0, hq, chunk_len)]}
+        return cached[key]
+
     def device_kv(self, page_table_dev) -> PagedKV:
         """The cache as a PagedKV for the chunk whose acquire wrote page_table_dev."""
         return PagedKV(self.ck, self.cv, page_table_dev, self.cdk, self.cdv)
@@ -563,10 +585,11 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     Fourth optimisation of the method (asynchronous CPU offloading): each
     chunk's tiles are brought into the device cache by oomb_offload_acquire.
     With ``prefetch``, a second stream does the moves while the compute stream
-    runs the attention: in the forward, the representatives of chunk c's
-    pages, chunk c+1's selection and its acquire overlap chunk c's forward (and
-    the last chunk's gradient tiles come in during the forward of the chunk
-    before it); in the backward, chunk c-1's acquire overlaps chunk c's
+    runs the attention: in the forward, chunk c+1's acquire overlaps chunk c's
+    forward (the representatives of chunk c's pages and chunk c+1's selection,
+    which need chunk c's tiles and every SM, run just before chunk c's forward),
+    and the last chunk's gradient tiles come in during the forward of the chunk
+    before it; in the backward, chunk c-1's acquire overlaps chunk c's
     backward, and chunk c's own pages -- final once its backward is done, since
     no earlier chunk reads them -- go back to the host during the backward of
     chunk c-1.  O, the selections and the host dK/dV are bit-identical to
@@ -586,20 +609,18 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
         raise OombError(OOMB_ERR_INVALID_ARG, "reps of the pages before start are required")
     dev = q_full.device
     comp = torch.cuda.current_stream(dev)
+    st = cache.pass_state(dev, hq, chunk_len, top_k)
     # the moves run at high priority: their CTAs are scheduled as soon as an SM
     # frees up between attention CTAs, rather than after the whole attention grid
-    copy = torch.cuda.Stream(dev, priority=-1) if prefetch else comp
+    copy = st["copy"] if prefetch else comp
+    copy.wait_stream(comp)                        # after everything before this pass
     # device page tables: chunks c and c+1 in flight use pts[c % 2]; the last
     # chunk's backward uses pt_last (written while its forward may still run)
-    pts = [torch.full((n_pages,), -1, dtype=torch.int32, device=dev) for _ in range(2)]
-    pt_last = torch.full((n_pages,), -1, dtype=torch.int32, device=dev)
+    pts, pt_last = st["pts"], st["pt_last"]
     if reps is None:
         reps = torch.empty((n_pages, hkv, d), dtype=torch.float32, device=dev)
     kv0 = cache.device_kv(pts[0])
-    ws_r = workspace(OOMB_OP_PAGE_REPS, kv0)
-    ws_s = workspace(OOMB_OP_SELECT_TOPK, kv0, hq, chunk_len, top_k)
-    ws_f = workspace(OOMB_OP_ATTN_FWD, kv0, hq, chunk_len)
-    ws_b = workspace(OOMB_OP_ATTN_BWD, kv0, hq, chunk_len)
+    ws_r, ws_s, ws_f, ws_b = st["ws"]
     o_full = torch.empty_like(q_full)
     o_lo_full = o_residual_like(o_full)
     dq_full = torch.empty_like(q_full)
@@ -621,16 +642,22 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
         return ev
 
     def select(c):
-        # on the current stream; needs the representatives of pages < t0 / P
+        # on the current stream; needs the representatives of pages < t0 / P.
+        # The host copy of the selection is taken later (host_sel).
         t0 = start + c * chunk_len
         n_sel = min(top_k, t0 // p)
         sel = torch.zeros((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
         if n_sel:
             oomb_select_topk(q_full[c * chunk_len:(c + 1) * chunk_len], t0, reps, kv0, n_sel, sel,
                              ws_s, stream=cur())
-        return sel, sel.cpu(), n_sel            # the copy synchronises the current stream
+        return [sel, None, n_sel]
+
+    def host_sel(c):
+        if sels[c][1] is None:
+            sels[c][1] = sels[c][0].cpu()         # synchronises the current stream
 
     def acquire(c, grads, pt):
+        host_sel(c)
         _, sel_h, n_sel = sels[c]
         cache.acquire(sel_h, n_sel, start + c * chunk_len, length(c), grads, pt, cur())
 
@@ -643,12 +670,24 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
             acquire(c, True, pt_last)
             ready_last[0] = mark()
 
-    # forward, chunks in order
+    # forward, chunks in order.  Chunk c+1's selection needs the representatives
+    # of chunk c's pages, which need chunk c's tiles: on the copy stream, after
+    # chunk c's acquire and between the forwards of chunks c-1 and c (the
+    # selection is one kernel over every SM; run beside a forward it would
+    # stall it), then chunk c+1's acquire runs beside chunk c's forward.
     with torch.cuda.stream(copy):
         sels[0] = select(0)
         acquire_fwd(0)
     for c in range(n_chunks):
         r0 = c * chunk_len
+        if c + 1 < n_chunks:
+            with torch.cuda.stream(copy):
+                if c >= 1:
+                    copy.wait_event(done[c - 1])
+                oomb_page_reps(cache.device_kv(pts[c % 2]), (start + r0) // p, chunk_len // p,
+                               reps, ws_r, copy)
+                sels[c + 1] = select(c + 1)
+                comp.wait_event(mark())
         comp.wait_event(ready[c])
         sel, _, n_sel = sels[c]
         lses[c] = torch.empty((hq, length(c)), dtype=torch.float32, device=dev)
@@ -659,11 +698,7 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
         done[c].record(comp)
         if c + 1 < n_chunks:
             with torch.cuda.stream(copy):
-                # this chunk's pages are resident: their representatives, then the
-                # next chunk's selection and tiles
-                oomb_page_reps(cache.device_kv(pts[c % 2]), (start + r0) // p, chunk_len // p,
-                               reps, ws_r, copy)
-                sels[c + 1] = select(c + 1)
+                host_sel(c + 1)                   # before the wait: the host waits only for it
                 if c >= 1:
                     copy.wait_event(done[c - 1])  # slots of chunk c-1 may be reused now
                 acquire_fwd(c + 1)
@@ -687,7 +722,10 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
                 copy.wait_event(fwd_done if c == last else done[c + 1])
                 acquire(c - 1, True, pts[(c - 1) % 2])
                 ready[c - 1] = mark()
-            # chunk c's own pages are final: no earlier chunk reads them
+            # chunk c's own pages are final: no earlier chunk reads them.  (Writing
+            # back here the pages that only later chunks selected as well measured
+            # slower: the final flush shrinks, but those moves take SMs from the
+            # backward.)
             copy.wait_event(done[c])
             cache.writeback((start + r0) // p, -(-length(c) // p), copy)
     comp.wait_stream(copy)

@@ -39,6 +39,7 @@ def test_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     assert oomb.oomb_status_string(0) == "OOMB_OK"
     assert oomb.oomb_status_string(4) == "OOMB_ERR_TIMEOUT"
+    assert oomb.oomb_status_string(6) == "OOMB_ERR_NONFINITE"
     assert oomb.oomb_status_string(99) == "OOMB_ERR_UNKNOWN"
 
 

@@ -347,6 +347,38 @@ def test_partial_last_page(wl):
     assert np.array_equal(dk_g[p1:], k0[p1:]) and np.array_equal(dv_g[p1:], v0[p1:])
 
 
+@pytest.mark.parametrize("what", ["k_nan", "v_inf", "finite"])
+def test_partial_last_page_non_finite_rows_are_flagged(what):
+    """A NaN or inf in an unused row of the partial last page (where a
+    torch.empty pool leaves garbage) is recorded as OOMB_ERR_NONFINITE by the
+    forward and the backward; finite garbage there is not an error."""
+    wl = PARTIAL[0]
+    x = make_inputs(wl, seed=6, device=DEV)
+    end = wl.start + wl.chunk_len
+    p = wl.page_size
+    slot = int(x.page_table[end // p])
+    _spoil_tail(x, end)
+    row = end % p + (p - end % p) // 2                  # a row past the chunk's end
+    if what == "k_nan":
+        x.k_pool[slot, 1, row, 77] = float("nan")
+    elif what == "v_inf":
+        x.v_pool[slot, 0, p - 1, 0] = float("-inf")
+    kv = gpu_kv(x)
+    sel = sel_tensor(np.tile(np.arange(wl.n_sel, dtype=np.int32), (wl.num_kv_heads, 1)), DEV)
+    want = oomb.OOMB_OK if what == "finite" else oomb.OOMB_ERR_NONFINITE
+    o = torch.empty_like(x.q)
+    lse = torch.empty((wl.num_q_heads, wl.chunk_len), dtype=torch.float32, device=DEV)
+    ws = oomb.workspace(oomb.OOMB_OP_ATTN_FWD, kv, wl.num_q_heads, wl.chunk_len)
+    oomb.oomb_sparse_attn_fwd(x.q, kv, sel, wl.n_sel, wl.start, o, lse, ws)
+    assert oomb.oomb_device_status(ws)[0] == want
+    dq = torch.empty_like(x.q)
+    ws = oomb.workspace(oomb.OOMB_OP_ATTN_BWD, kv, wl.num_q_heads, wl.chunk_len)
+    oomb.oomb_sparse_attn_bwd(x.q, o, x.do, lse, kv, sel, wl.n_sel, wl.start, dq, ws)
+    assert oomb.oomb_device_status(ws)[0] == want
+    if what == "finite":
+        assert torch.isfinite(o).all() and torch.isfinite(dq).all()
+
+
 @pytest.mark.parametrize("top_k", [3, 1 << 20])
 def test_chunk_recurrent_pass_ragged_sequence(top_k):
     """The sequence of test_chunk_recurrent_pass cut 19 tokens before its end:
