@@ -139,16 +139,23 @@ def chunk_pass_flops(wl):
     return 14.0 * wl.head_dim * wl.num_q_heads * pairs
 
 
-def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=3):
+def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=5):
     """The last ``n_chunks`` chunks of the workload as a chunk-recurrent pass
-    (forward in order, backward in reverse), once with the pools resident in
-    HBM and once with the K, V, dK, dV pools in pinned host memory behind a
-    device page cache (oomb_offload_*), the next chunk's tiles brought in on a
-    second stream while the current chunk computes.  The cache starts empty
-    in every offloaded pass.  Both passes are timed with CUDA events; the
-    difference is the offload overhead.  Then the same offloaded pass with the
-    host K/V pools stored as E4M3 codes (an fp8 KV cache, expanded to bf16 as
-    tiles are fetched), against the same resident time."""
+    (forward in order, backward in reverse), with the pools resident in HBM and
+    with the K, V, dK, dV pools in pinned host memory behind a device page cache
+    (oomb_offload_*), the next chunk's tiles brought in on a second stream while
+    the current chunk computes.  Offloaded passes start from an empty cache
+    ("cold": the host gradients hold earlier sums, so gradient tiles are copied
+    in) or, in addition, from zeroed host gradients declared with zero_grads()
+    ("zero_grads": a new pass of training, gradient tiles zero-filled in the
+    cache).  Then the same two with the host K/V pools stored as E4M3 codes (an
+    fp8 KV cache, expanded to bf16 as tiles are fetched).  Every pass is timed
+    alone with CUDA events after an untimed preparation (emptying the cache,
+    zeroing the host gradients), the variants interleaved pass by pass with the
+    resident pass; each figure is the median over ``passes`` rounds after one
+    warm-up round, and each overhead is against the resident median of the same
+    rounds."""
+    import statistics
     from paged_sparse_attention_oomb_gb300 import oomb
     c, p, hkv = wl.chunk_len, wl.page_size, wl.num_kv_heads
     start = wl.context - n_chunks * c
@@ -168,68 +175,68 @@ def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=3):
     host.dk.zero_()
     host.dv.zero_()
     setup_s = time.time() - t_host0
-    per_chunk = wl.top_k * hkv + c // p
-    cache = oomb.OffloadCache(host, 2 * per_chunk + 64, dev)
+    slots = 2 * (wl.top_k * hkv + c // p) + 64
 
-    def timed(fn):
-        fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(passes):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / passes
+    def resident():
+        oomb.chunk_recurrent_pass(q, do, kv, c, wl.top_k, start=start, reps=reps)
 
-    ms_res = timed(lambda: oomb.chunk_recurrent_pass(q, do, kv, c, wl.top_k, start=start,
-                                                     reps=reps))
-    before = cache.stats()
-    def offloaded():
-        cache.flush(drop=True)          # cold cache: every tile of the pass comes from the host
-        oomb.chunk_recurrent_pass_offloaded(q, do, cache, c, wl.top_k, start=start, reps=reps)
-    ms_off = timed(offloaded)
-    after = cache.stats()
-    n_pass = passes + 1
+    def offloaded(cache, zero):
+        def prep():
+            if zero:
+                host.dk.zero_()
+                host.dv.zero_()
+                cache.zero_grads()
+            cache.flush(drop=True)
+        return prep, lambda: oomb.chunk_recurrent_pass_offloaded(q, do, cache, c, wl.top_k,
+                                                                 start=start, reps=reps)
+
+    def rounds(variants):
+        """variants: name -> (cache or None, prep or None, run); medians in ms
+        and per-pass move counters over the timed rounds."""
+        times = {k: [] for k in variants}
+        moved = {k: {} for k in variants}
+        for i in range(passes + 1):
+            for name, (cache, prep, run) in variants.items():
+                if prep is not None:
+                    prep()
+                torch.cuda.synchronize()
+                s0 = cache.stats() if cache is not None else None
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                run()
+                e1.record()
+                torch.cuda.synchronize()
+                if i == 0:
+                    continue                     # warm-up round
+                times[name].append(e0.elapsed_time(e1))
+                if cache is not None:
+                    s1 = cache.stats()
+                    for key in ("bytes_in", "bytes_out", "tiles_zero_filled"):
+                        moved[name][key] = moved[name].get(key, 0) + (s1[key] - s0[key]) / passes
+        return ({k: statistics.median(v) for k, v in times.items()},
+                {k: [round(t, 3) for t in v] for k, v in times.items()}, moved)
+
+    def entry(name, med, all_ms, moved, res_key):
+        m = moved[name]
+        return {"ms_per_pass_offloaded": med[name], "overhead": med[name] / med[res_key] - 1.0,
+                "ms_per_pass_resident": med[res_key], "passes_ms": all_ms[name],
+                "bytes_in_per_pass": m["bytes_in"], "bytes_out_per_pass": m["bytes_out"],
+                "tiles_zero_filled_per_pass": m["tiles_zero_filled"]}
+
+    cache = oomb.OffloadCache(host, slots, dev)
+    med, all_ms, moved = rounds({"resident": (None, None, resident),
+                                 "cold": (cache,) + offloaded(cache, False),
+                                 "zero_grads": (cache,) + offloaded(cache, True)})
     res = {"workload": f"{wl.name}, last {n_chunks} chunks", "chunks": n_chunks,
            "cache_slots": cache.cache_slots,
            "cache_bytes": 4 * cache.ck.numel() * cache.ck.element_size(),
            "host_pool_bytes": 4 * host.k.numel() * host.k.element_size(),
-           "ms_per_pass_resident": ms_res, "ms_per_pass_offloaded": ms_off,
-           "overhead": ms_off / ms_res - 1.0,
-           "bytes_in_per_pass": (after["bytes_in"] - before["bytes_in"]) / n_pass,
-           "bytes_out_per_pass": (after["bytes_out"] - before["bytes_out"]) / n_pass,
-           "host_setup_s": setup_s,
-           "what": "fwd in order + bwd in reverse, cold cache per pass; next chunk's tiles "
-                   "fetched on a second stream"}
-    def new_passes(cch):
-        # each pass a new pass: host gradients zeroed (untimed) and declared
-        # zero, so the first touch of a gradient tile is a fill on the device
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        tot, z0 = 0.0, None
-        for i in range(passes + 1):              # the first pass is a warm-up
-            host.dk.zero_()
-            host.dv.zero_()
-            cch.zero_grads()
-            cch.flush(drop=True)
-            torch.cuda.synchronize()
-            if i == 1:
-                z0 = cch.stats()
-            e0.record()
-            oomb.chunk_recurrent_pass_offloaded(q, do, cch, c, wl.top_k, start=start, reps=reps)
-            e1.record()
-            torch.cuda.synchronize()
-            if i > 0:
-                tot += e0.elapsed_time(e1)
-        z1 = cch.stats()
-        ms_z = tot / passes
-        return {"ms_per_pass_offloaded": ms_z, "overhead": ms_z / ms_res - 1.0,
-                "bytes_in_per_pass": (z1["bytes_in"] - z0["bytes_in"]) / passes,
-                "bytes_out_per_pass": (z1["bytes_out"] - z0["bytes_out"]) / passes,
-                "tiles_zero_filled_per_pass":
-                    (z1["tiles_zero_filled"] - z0["tiles_zero_filled"]) / passes}
-
-    res["zero_grads"] = new_passes(cache)
+           "host_setup_s": setup_s, "timing": f"median of {passes} interleaved passes",
+           "resident_passes_ms": all_ms["resident"]}
+    res.update(entry("cold", med, all_ms, moved, "resident"))
+    res["what"] = ("fwd in order + bwd in reverse, cold cache per pass; next chunk's tiles "
+                   "fetched on a second stream")
+    res["zero_grads"] = entry("zero_grads", med, all_ms, moved, "resident")
     res["zero_grads"]["what"] = ("each pass starts a new pass: host dK/dV zeroed (untimed) and "
                                  "declared with zero_grads(); gradient tiles still zero on the "
                                  "host are zero-filled in the cache")
@@ -244,22 +251,16 @@ def measure_offload(wl, x, kv, reps, dev, n_chunks=4, passes=3):
             dst[b0:b0 + 4096].copy_(src[b0:b0 + 4096].to(torch.float8_e4m3fn))
     setup8 = time.time() - t_host0
     cache8 = oomb.OffloadCache(oomb.PagedKV(k8, v8, x.page_table.cpu(), host.dk, host.dv),
-                               2 * per_chunk + 64, dev)
-    before = cache8.stats()
-
-    def offloaded8():
-        cache8.flush(drop=True)
-        oomb.chunk_recurrent_pass_offloaded(q, do, cache8, c, wl.top_k, start=start, reps=reps)
-    ms8 = timed(offloaded8)
-    after = cache8.stats()
-    res["fp8_kv"] = {"ms_per_pass_offloaded": ms8, "overhead": ms8 / ms_res - 1.0,
-                     "host_pool_bytes": 2 * k8.numel() + 4 * k8.numel(),
-                     "bytes_in_per_pass": (after["bytes_in"] - before["bytes_in"]) / n_pass,
-                     "bytes_out_per_pass": (after["bytes_out"] - before["bytes_out"]) / n_pass,
-                     "host_setup_s": setup8,
-                     "what": "host K/V as E4M3 codes expanded to bf16 on fetch; overhead "
-                             "against the resident bf16 pass above"}
-    res["fp8_kv"]["new_pass"] = new_passes(cache8)
+                               slots, dev)
+    med, all_ms, moved = rounds({"resident": (None, None, resident),
+                                 "cold": (cache8,) + offloaded(cache8, False),
+                                 "zero_grads": (cache8,) + offloaded(cache8, True)})
+    res["fp8_kv"] = entry("cold", med, all_ms, moved, "resident")
+    res["fp8_kv"].update({"host_pool_bytes": 2 * k8.numel() + 4 * k8.numel(),
+                          "host_setup_s": setup8,
+                          "what": "host K/V as E4M3 codes expanded to bf16 on fetch; overhead "
+                                  "against the resident bf16 pass of the same rounds"})
+    res["fp8_kv"]["new_pass"] = entry("zero_grads", med, all_ms, moved, "resident")
     cache8.close()
     return res
 

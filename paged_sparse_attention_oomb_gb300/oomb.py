@@ -643,22 +643,24 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
 
     def select(c):
         # on the current stream; needs the representatives of pages < t0 / P.
-        # The host copy of the selection is taken later (host_sel).
+        # The selection is copied to pinned host memory behind it; host_sel
+        # waits for that copy alone, not for what the stream does next.
         t0 = start + c * chunk_len
         n_sel = min(top_k, t0 // p)
         sel = torch.zeros((hkv, max(n_sel, 1)), dtype=torch.int32, device=dev)
         if n_sel:
             oomb_select_topk(q_full[c * chunk_len:(c + 1) * chunk_len], t0, reps, kv0, n_sel, sel,
                              ws_s, stream=cur())
-        return [sel, None, n_sel]
+        sel_h = torch.empty(sel.shape, dtype=torch.int32, pin_memory=True)
+        sel_h.copy_(sel, non_blocking=True)
+        return [sel, sel_h, n_sel, mark()]
 
     def host_sel(c):
-        if sels[c][1] is None:
-            sels[c][1] = sels[c][0].cpu()         # synchronises the current stream
+        sels[c][3].synchronize()
 
     def acquire(c, grads, pt):
         host_sel(c)
-        _, sel_h, n_sel = sels[c]
+        sel_h, n_sel = sels[c][1], sels[c][2]
         cache.acquire(sel_h, n_sel, start + c * chunk_len, length(c), grads, pt, cur())
 
     def acquire_fwd(c):
@@ -675,12 +677,21 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     # chunk c's acquire and between the forwards of chunks c-1 and c (the
     # selection is one kernel over every SM; run beside a forward it would
     # stall it), then chunk c+1's acquire runs beside chunk c's forward.
+    # Chunk 0's own pages do not depend on its selection: they come in first,
+    # and chunk 1's selection (which needs their representatives) runs while
+    # the host plans the rest of chunk 0's acquire.
+    early = prefetch and start > 0 and n_chunks > 1
     with torch.cuda.stream(copy):
+        if early:
+            cache.acquire(None, 0, start, length(0), False, pts[0], cur())
         sels[0] = select(0)
+        if early:
+            oomb_page_reps(cache.device_kv(pts[0]), start // p, chunk_len // p, reps, ws_r, copy)
+            sels[1] = select(1)
         acquire_fwd(0)
     for c in range(n_chunks):
         r0 = c * chunk_len
-        if c + 1 < n_chunks:
+        if c + 1 < n_chunks and not (early and c == 0):
             with torch.cuda.stream(copy):
                 if c >= 1:
                     copy.wait_event(done[c - 1])
@@ -689,7 +700,7 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
                 sels[c + 1] = select(c + 1)
                 comp.wait_event(mark())
         comp.wait_event(ready[c])
-        sel, _, n_sel = sels[c]
+        sel, n_sel = sels[c][0], sels[c][2]
         lses[c] = torch.empty((hq, length(c)), dtype=torch.float32, device=dev)
         oomb_sparse_attn_fwd(q_full[r0:r0 + chunk_len], cache.device_kv(pts[c % 2]), sel, n_sel,
                              start + r0, o_full[r0:r0 + chunk_len], lses[c], ws_f, scale, comp,
@@ -707,7 +718,7 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     for c in reversed(range(n_chunks)):
         r0 = c * chunk_len
         comp.wait_event(ready_last[0] if c == last else ready[c])
-        sel, _, n_sel = sels[c]
+        sel, n_sel = sels[c][0], sels[c][2]
         pt = pt_last if c == last else pts[c % 2]
         oomb_sparse_attn_bwd(q_full[r0:r0 + chunk_len], o_full[r0:r0 + chunk_len],
                              dout_full[r0:r0 + chunk_len], lses[c], cache.device_kv(pt),
