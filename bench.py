@@ -303,7 +303,15 @@ def measure_chunk_pass(dev, peak_t, passes=3):
 # SHA-256 of the backward's source files at the time of the capture: when the
 # sources differ the figure describes another kernel and the bench reports
 # the traffic as null.
-BWD_TRAFFIC = {}
+BWD_TRAFFIC = {
+    "qwen7b_ctx4m_k128": {
+        "bytes": 2205717504, "sha": "bae900ecdadd924e",
+        "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum of bwd_prep_kernel (253.5 MB), "
+               "sparse_attn_bwd_kernel (1811.3 MB) and dq_convert_kernel (141.0 MB), first "
+               "backward call, captured on the same backward launches over a 512K-token cache "
+               "(bench.py --context 524288: same chunk, Top-K, page size and heads, so the same "
+               "selected and own pages per launch)"},
+}
 BWD_SOURCES = ["k_attn_bwd_bf16.cu", "sm100.cuh", "tmap.h"]
 
 
