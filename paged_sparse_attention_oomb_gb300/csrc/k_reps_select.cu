@@ -174,12 +174,11 @@ __device__ __forceinline__ void cp_async_wait() {
 //  2c  Once every CTA has counted its scores (an arrival counter), CTA g <
 //      Hkv keeps the top_k best scores of KV head g (ties -> lower page),
 //      written in ascending page order.  The first digit's bin where the
-//      count from the top reaches k is found by reading the histogram
-//      downwards from the bin of the head's largest key (a per-head maximum
-//      kept while scoring), 2048 bins per round.  Fast path: the keys at or
-//      above that bin (k plus the bin's few) go with their indices into
-//      shared memory, and the k largest by (key, then lower index) are written
-//      in index order -- ranked by counting when there are at most
+//      count from the top reaches k comes from the histogram (coalesced warp
+//      sums, then the warp holding the bin narrows it down).  Fast path: the
+//      keys at or above that bin (k plus the bin's few) go with their indices
+//      into shared memory, and the k largest by (key, then lower index) are
+//      written in index order -- ranked by counting when there are at most
 //      kSelRankMax of them, else sorted.  When more than kSelSortMax keys
 //      share the bins (many equal scores), two 8-bit digits from
 //      shared-memory histograms of the keys that share the digits found so
@@ -188,22 +187,24 @@ __device__ __forceinline__ void cp_async_wait() {
 //      key above T and those ties.
 // ---------------------------------------------------------------------------
 constexpr int kSelThreads = 1024;
-constexpr int kSelDepth = 12;                     // 16-byte copies in flight per thread
+constexpr int kSelDepth = 8;                      // 16-byte copies in flight per thread
 constexpr int kSelGroup = 8;                      // CTAs per first-level group
 constexpr int kSelMaxBlocks = 256;
 constexpr int kSelCacheKeys = 40 * 1024;          // keys cached for the radix passes
 constexpr int kSelSortMax = 4096;                 // keys sorted on the fast path
 constexpr int kSelRankMax = 256;                  // keys ranked by counting instead
-// Dynamic shared memory: the copy ring of phases 2a/2b, reused in 2c for the
-// key cache of the radix passes and, after it, the fast path's sort buffers.
 constexpr size_t kSelRingBytes = sizeof(uint4) * kSelDepth * kSelThreads;
-constexpr size_t kSelCacheBytes = 4 * static_cast<size_t>(kSelCacheKeys);
+constexpr size_t kSelCacheBytes =
+    kSelRingBytes > 4 * kSelCacheKeys ? kSelRingBytes : 4 * static_cast<size_t>(kSelCacheKeys);
 constexpr size_t kSelListBytes = 8 * 4096 + 4 * 4096;   // the fast path's sort buffers
-constexpr size_t kSelDynSmem = kSelRingBytes > kSelCacheBytes + kSelListBytes
-                                   ? kSelRingBytes
-                                   : kSelCacheBytes + kSelListBytes;
+constexpr size_t kSelDynSmem = kSelCacheBytes + kSelListBytes;
 static_assert(kGroupTicketIdx + (kSelMaxBlocks + kSelGroup - 1) / kSelGroup <= 64,
               "tickets fit the status block");
+
+// Bring `bytes` (a multiple of 16) at `p` into L2, without waiting.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // In-place bitonic sort of n (a power of two) values in shared memory by the
 // whole block: descending if `desc`, else ascending.
@@ -285,7 +286,6 @@ struct SelParams {
   float* gsums;                   // [groups][hkv * D]
   float* qbar;                    // [hkv * D]
   int* hist;                      // [hkv][65536]
-  unsigned int* maxkey;           // [hkv] largest order key among each head's candidates
   int* status;
   int chunk_len, hq, hkv, n_cand, num_pages, top_k;
   uint64_t wait_ns;
@@ -318,9 +318,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
   const long hist_words = static_cast<long>(p.hkv) << 16;
   for (long i = static_cast<long>(bid) * nt + tid; i < hist_words; i += static_cast<long>(nb) * nt)
     p.hist[i] = 0;
-  if (bid == 0 && tid < p.hkv) p.maxkey[tid] = 0u;
-  __shared__ unsigned int smax[16];               // this CTA's largest key per head
-  if (tid < 16) smax[tid] = 0u;
 
   // ---------------------------------------------------------------- 2a
   const int hq = p.hq, hkv = p.hkv;
@@ -357,6 +354,17 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
       }
     }
     cp_async_wait<0>();
+    if (tid == 0) {
+      // this CTA's representative rows (2b), into L2 while the query summary
+      // is folded and waited for: the loads of 2b then mostly hit L2
+      const int cand_rows0 = p.n_cand * p.hkv;
+      const int r_per0 = (cand_rows0 + nb - 1) / nb;
+      const int a0 = min(cand_rows0, bid * r_per0), a1 = min(cand_rows0, a0 + r_per0);
+      const char* base = reinterpret_cast<const char*>(p.reps) + static_cast<size_t>(a0) * D * 4;
+      const size_t bytes = static_cast<size_t>(a1 - a0) * D * 4;
+      for (size_t off = 0; off < bytes; off += 65536)
+        prefetch_l2(base + off, static_cast<uint32_t>(bytes - off < 65536 ? bytes - off : 65536));
+    }
     __syncthreads();                              // the ring becomes the fold area
     float* sm = reinterpret_cast<float*>(ring);   // [R][row_elems]
     if (sub < R) {                                // 16-byte stores: no bank conflicts
@@ -470,14 +478,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
     for (int off = L / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
     if (valid && li == 0) {
       p.scores[static_cast<long>(g) * p.num_pages + r / hkv] = sc;
-      const uint32_t key = order_key(sc);
-      atomicAdd(&p.hist[(static_cast<long>(g) << 16) + (key >> 16)], 1);
-      atomicMax(&smax[g], key);
+      atomicAdd(&p.hist[(static_cast<long>(g) << 16) + (order_key(sc) >> 16)], 1);
     }
   }
   cp_async_wait<0>();
   __syncthreads();                                // the ring is free again
-  if (tid < hkv && smax[tid] != 0u) atomicMax(&p.maxkey[tid], smax[tid]);
   // pages that are not candidates
   const int n_other = (p.num_pages - p.n_cand) * hkv;
   for (int i = bid * nt + tid; i < n_other; i += nb * nt) {
@@ -508,48 +513,89 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
   if (!flag) return;
   uint32_t* keys_sm = reinterpret_cast<uint32_t*>(ring);
   const bool cached = n_cand <= kSelCacheKeys;
-  // digit 1: the 16-bit bin where the count from the top reaches k.  The bins
-  // are read downwards from the one holding the head's largest key, 2048 at a
-  // time (two a thread, one round of loads), with a block-wide scan of the
-  // counts: the bin is nearly always inside the first window.
-  __shared__ int sh_above, sh_done;
+  // digit 1: the 16-bit bin where the count from the top reaches k.  Warp w
+  // owns bins [2048 w, 2048 w + 2048) and reads them coalesced; the warp
+  // holding the bin then narrows it down to a lane's 64 bins, then to the bin.
+  __shared__ int wcount[32];
+  __shared__ int sh_above;
   {
     const int* hg = p.hist + (static_cast<long>(g) << 16);
-    int hi = static_cast<int>(__ldcg(p.maxkey + g) >> 16);
-    int run = 0;                                  // keys in the bins above hi
-    if (tid == 0) sh_done = 0;
-    __syncthreads();
-    for (;;) {
-      const int b1 = hi - 2 * tid, b0 = b1 - 1;   // this thread's two bins, from the top
-      const int c1 = b1 >= 0 ? __ldcg(hg + b1) : 0;
-      const int c0 = b0 >= 0 ? __ldcg(hg + b0) : 0;
-      const int c = c0 + c1;
-      const int ab = run + block_excl_scan(c, warp_tot, &total);   // keys above my bins
-      if (ab < k && ab + c1 >= k) {
-        sh_digit = static_cast<uint32_t>(b1);
-        sh_need = k - ab;
-        sh_above = c1;                            // keys in the bin
-        sh_done = 1;
-      } else if (ab + c1 < k && ab + c >= k) {
-        sh_digit = static_cast<uint32_t>(b0);
-        sh_need = k - ab - c1;
-        sh_above = c0;
-        sh_done = 1;
-      }
-      __syncthreads();
-      if (sh_done || hi < 2 * nt) break;          // (the window reached bin 0)
-      run += total;
-      hi -= 2 * nt;
+    const int4* h4 = reinterpret_cast<const int4*>(hg + 2048 * w);
+    int cw = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int4 v = __ldcg(h4 + 32 * j + lane);
+      cw += (v.x + v.y) + (v.z + v.w);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cw += __shfl_xor_sync(0xffffffffu, cw, o);
+    if (lane == 0) wcount[w] = cw;
+    __syncthreads();
+    if (w == 0) {                                 // from the top: lane l holds warp 31 - l
+      const int c = wcount[31 - lane];
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (x - c < k && x >= k) {
+        sh_digit = static_cast<uint32_t>(31 - lane);
+        sh_above = x - c;
+      }
+    }
+    __syncthreads();
+    const int bw = static_cast<int>(sh_digit);
+    if (w == bw) {
+      // lane l: bins [2048 bw + 64 l, +64), counted from the top (lane 31 first)
+      const int4* l4 = reinterpret_cast<const int4*>(hg + 2048 * bw + 64 * lane);
+      int cl = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int4 v = __ldcg(l4 + j);
+        cl += (v.x + v.y) + (v.z + v.w);
+      }
+      const int c = __shfl_sync(0xffffffffu, cl, 31 - lane);
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const int above_w = sh_above;
+      const int hit = __ballot_sync(0xffffffffu, above_w + x - c < k && above_w + x >= k);
+      const int src = __ffs(hit) - 1;             // exactly one lane
+      const int bl = 31 - src;                    // the lane range holding the bin
+      const int run0 = above_w + __shfl_sync(0xffffffffu, x - c, src);
+      // that range's 64 bins, two per lane from the top
+      const int* hb = hg + 2048 * bw + 64 * bl;
+      const int c0 = __ldcg(hb + 63 - 2 * lane), c1 = __ldcg(hb + 62 - 2 * lane);
+      int y = c0 + c1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int z = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) y += z;
+      }
+      const int ex = run0 + y - (c0 + c1);        // keys above this lane's two bins
+      if (ex < k && ex + c0 >= k) {
+        sh_digit = static_cast<uint32_t>(2048 * bw + 64 * bl + 63 - 2 * lane);
+        sh_need = k - ex;
+        sh_above = c0;                            // keys in the bin
+      } else if (ex + c0 < k && ex + c0 + c1 >= k) {
+        sh_digit = static_cast<uint32_t>(2048 * bw + 64 * bl + 62 - 2 * lane);
+        sh_need = k - ex - c0;
+        sh_above = c1;
+      }
+    }
+    __syncthreads();
   }
   const uint32_t b16 = sh_digit;
   const int in_bin = sh_above;                    // keys in the boundary bin
   const int list_n = k - sh_need + in_bin;        // keys above the bin, and the bin's
   if (list_n <= kSelSortMax) {
-    // Fast path: those keys (with their indices) into shared memory.  The k
-    // largest by (key descending, index ascending) are kept and written in
-    // index order: a short list (the usual case: k plus the bin's few) ranks
-    // each entry by counting, a longer one is sorted.
+    // Fast path: those keys (with their indices) into shared memory, sorted by
+    // key descending and index ascending; the first k are kept, then sorted by
+    // index for the output.
     unsigned long long* list = reinterpret_cast<unsigned long long*>(
         reinterpret_cast<char*>(ring) + kSelCacheBytes);
     uint32_t* idx = reinterpret_cast<uint32_t*>(list + kSelSortMax);
@@ -557,58 +603,28 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
     if (tid == 0) n_list = 0;
     __syncthreads();
     const uint32_t below = (1u << lane) - 1u;
-    // a value is taken when its key reaches the boundary bin, i.e. when it is
-    // at least the smallest float with such a key (NaN never is; with bin 0
-    // every candidate is; below the key of -inf every number is)
-    const uint32_t kmin = b16 << 16;
-    const float thr = kmin <= 0x007FFFFFu
-                          ? -INFINITY
-                          : __uint_as_float((kmin & 0x80000000u) ? (kmin & 0x7FFFFFFFu) : ~kmin);
-    auto consider = [&](float v, int i) {         // called by whole warps
-      const bool take = i < n_cand && (b16 == 0u || v >= thr);
-      const uint32_t m = __ballot_sync(0xffffffffu, take);
-      if (m) {
-        const int leader = __ffs(m) - 1;
-        int at = 0;
-        if (lane == leader) at = atomicAdd(&n_list, __popc(m));
-        at = __shfl_sync(0xffffffffu, at, leader) + __popc(m & below);
-        if (take && at < kSelSortMax)
-          list[at] = (static_cast<unsigned long long>(order_key(v)) << 32) |
-                     (0xFFFFFFFFu - static_cast<uint32_t>(i));
+    constexpr int kU = 8;                         // loads in flight per thread
+    for (int base0 = 0; base0 < n_cand; base0 += kU * nt) {   // warp-uniform steps
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base0 + tid + u * nt;
+        v[u] = i < n_cand ? __ldcg(sc + i) : 0.f;
       }
-    };
-    if (p.num_pages % 4 == 0 && (reinterpret_cast<uintptr_t>(p.scores) & 15u) == 0) {
-      // 16-byte loads: a 32768-candidate row in one round per thread
-      const float4* sc4 = reinterpret_cast<const float4*>(sc);
-      const int n4 = (n_cand + 3) / 4;            // within the row: num_pages % 4 == 0
-      constexpr int kV = 8;
-      for (int base0 = 0; base0 < n4; base0 += kV * nt) {   // warp-uniform steps
-        float4 v[kV];
 #pragma unroll
-        for (int u = 0; u < kV; ++u) {
-          const int j = base0 + tid + u * nt;
-          v[u] = j < n4 ? __ldcg(sc4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kU; ++u) {
+        const int i = base0 + tid + u * nt;
+        const uint32_t key = order_key(v[u]);
+        const bool take = i < n_cand && (key >> 16) >= b16;
+        const uint32_t m = __ballot_sync(0xffffffffu, take);
+        if (m) {
+          const int leader = __ffs(m) - 1;
+          int at = 0;
+          if (lane == leader) at = atomicAdd(&n_list, __popc(m));
+          at = __shfl_sync(0xffffffffu, at, leader) + __popc(m & below);
+          if (take && at < kSelSortMax)
+            list[at] = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
         }
-#pragma unroll
-        for (int u = 0; u < kV; ++u) {
-          const int i = 4 * (base0 + tid + u * nt);
-          consider(v[u].x, i);
-          consider(v[u].y, i + 1);
-          consider(v[u].z, i + 2);
-          consider(v[u].w, i + 3);
-        }
-      }
-    } else {
-      constexpr int kU = 16;                      // loads in flight per thread
-      for (int base0 = 0; base0 < n_cand; base0 += kU * nt) {   // warp-uniform steps
-        float v[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int i = base0 + tid + u * nt;
-          v[u] = i < n_cand ? __ldcg(sc + i) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) consider(v[u], base0 + tid + u * nt);
       }
     }
     __syncthreads();
@@ -818,7 +834,6 @@ size_t select_ws_bytes(int num_pages, int hkv, int head_dim) {
   b += align_up(row, 256);                                                    // qbar
   b += align_up(static_cast<size_t>(hkv) * num_pages * 4, 256);              // scores
   b += static_cast<size_t>(hkv) * 65536 * 4;                                  // key histogram
-  b += 256;                                                                   // largest keys
   return b;
 }
 
@@ -890,8 +905,6 @@ cudaError_t launch_select_topk(const void* q, bool bf16, int hq, int chunk_len, 
   float* scores_ws = reinterpret_cast<float*>(w);
   w += align_up(static_cast<size_t>(hkv) * num_pages * 4, 256);
   prm.hist = reinterpret_cast<int*>(w);
-  w += static_cast<size_t>(hkv) * 65536 * 4;
-  prm.maxkey = reinterpret_cast<unsigned int*>(w);
   prm.scores = scores_opt ? scores_opt : scores_ws;
   prm.q = q;
   prm.reps = reps;
