@@ -8,8 +8,9 @@
 // Design (one GB300 with its Grace host): the pools of every page are pinned
 // host memory, which the GPU reads and writes directly over the CPU-GPU link.
 // A chunk's tiles -- (page, KV head) blocks of P x D elements -- are moved by
-// one kernel per direction, one CTA per tile, from a task list the host
-// writes into a pinned staging buffer; no per-tile copy call.  The host keeps
+// one kernel per direction (at most one CTA per SM, each looping over tiles)
+// from a task list the host writes into a pinned staging buffer; no per-tile
+// copy call.  The host keeps
 // the cache directory: which logical page sits in which cache slot, which KV
 // heads of it are loaded (K/V, gradients), which gradient tiles are modified,
 // and when the slot was last used.  Slots used by the current and the
