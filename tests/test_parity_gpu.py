@@ -460,6 +460,40 @@ def test_offload_chunk_pass_matches_resident(prefetch, staging):
     cache.close()
 
 
+def test_offload_pass_after_a_prefix_matches_resident():
+    """The last 4 chunks of a sequence (start > 0, the prefix's representatives
+    given): the offloaded pass fetches chunk 0's own pages first and makes
+    chunk 1's selection during the rest of chunk 0's acquire.  Bit-identical O,
+    selections and host dK/dV to the resident pass -- twice on one cache (the
+    second pass reuses the cache's streams, page tables and workspaces)."""
+    wl, x, q_full, do_full, dk0, dv0 = _offload_case(31)
+    start = 2048
+    q, do = q_full[:2048].contiguous(), do_full[:2048].contiguous()
+    kv = oomb.PagedKV(x.k_pool, x.v_pool, x.page_table, dk0.clone(), dv0.clone())
+    reps = gpu_reps(kv)
+    o_r, dq_r, sels_r = oomb.chunk_recurrent_pass(q, do, kv, 512, 3, start=start,
+                                                  reps=reps.clone())
+    host = oomb.PagedKV(x.k_pool.cpu().pin_memory(), x.v_pool.cpu().pin_memory(),
+                        x.page_table.cpu(), dk0.cpu().pin_memory(), dv0.cpu().pin_memory())
+    cache = oomb.OffloadCache(host, 28, DEV)
+    for _ in range(2):
+        host.dk.copy_(dk0.cpu())
+        host.dv.copy_(dv0.cpu())
+        cache.flush(drop=True)
+        torch.cuda.synchronize()
+        o_o, dq_o, sels_o = oomb.chunk_recurrent_pass_offloaded(q, do, cache, 512, 3,
+                                                                start=start, reps=reps.clone())
+        torch.cuda.synchronize()
+        for a, b in zip(sels_r, sels_o):
+            assert torch.equal(a, b)
+        assert torch.equal(_bits(o_r), _bits(o_o))
+        a, b = dq_r.float(), dq_o.float()
+        assert float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(a)) < 1e-3
+        assert torch.equal(_bits(kv.dk.cpu()), _bits(host.dk))
+        assert torch.equal(_bits(kv.dv.cpu()), _bits(host.dv))
+    cache.close()
+
+
 def test_offload_chunk_pass_fp32():
     """The same through the fp32 path (head_dim 64, P = 16, fp32 pools): 8 chunks
     of 128 rows, Top-8, 32 cache slots for 64 pages."""
