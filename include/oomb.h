@@ -343,6 +343,15 @@ oomb_status oomb_offload_flush(oomb_offload *h, int32_t drop, void *stream);
  * final flush has less to move. */
 oomb_status oomb_offload_writeback(oomb_offload *h, int32_t first_page, int32_t n_pages,
                                    void *stream);
+/* The same for a list of logical pages (pages_host: host int32 [n], each in
+ * [0, num_pages), repeats allowed; read before the call returns).  In a
+ * backward over the chunks in reverse order, the gradient tiles of a page are
+ * final once the backward of the last chunk to touch it (as an own or a
+ * selected page) is done.  A page modified again after its write-back is
+ * simply written back again.  OOMB_ERR_INVALID_ARG (nothing enqueued) for a
+ * page out of range. */
+oomb_status oomb_offload_writeback_pages(oomb_offload *h, const int32_t *pages_host, int32_t n,
+                                         void *stream);
 /* Declares that the caller has set every tile of the host dK/dV pools to zero
  * (the start of a new pass over the sequence).  The cache's gradient tiles are
  * forgotten without being written back (their sums belonged to the previous

@@ -625,6 +625,26 @@ oomb_status oomb_offload_writeback(oomb_offload* h, int32_t first_page, int32_t 
                      "offload writeback");
 }
 
+oomb_status oomb_offload_writeback_pages(oomb_offload* h, const int32_t* pages_host,
+                                         int32_t n, void* stream) {
+  OOMB_NVTX_RANGE("oomb_offload_writeback_pages");
+  if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "handle");
+  if (n < 0 || (n > 0 && !pages_host))
+    return oomb::report(OOMB_ERR_INVALID_ARG, "pages_host is NULL or n < 0");
+  for (int32_t i = 0; i < n; ++i)
+    if (pages_host[i] < 0 || pages_host[i] >= h->d.num_pages)
+      return oomb::report(OOMB_ERR_INVALID_ARG, "page %d outside [0, %d)", pages_host[i],
+                          h->d.num_pages);
+  Staging* st = nullptr;
+  oomb_status rs = take_stage(h, &st);
+  if (rs != OOMB_OK) return rs;
+  h->moves.clear();
+  h->dir->collect_writebacks_of(pages_host, n, &h->moves);
+  const size_t m = plan_to_tasks(h, *st);
+  return finish_call(h, *st, m, m, static_cast<cudaStream_t>(stream), nullptr,
+                     "offload writeback of pages");
+}
+
 oomb_status oomb_offload_zero_grads(oomb_offload* h) {
   if (!h) return oomb::report(OOMB_ERR_INVALID_ARG, "handle");
   if (!h->d.dk) return oomb::report(OOMB_ERR_INVALID_ARG, "the cache has no gradient pools");

@@ -154,6 +154,16 @@ class PageCacheDirectory {
     }
   }
 
+  // Appends the write-backs of every modified gradient tile of the listed
+  // pages (each in [0, num_pages), checked by the caller; repeats are
+  // harmless) and marks them clean.
+  void collect_writebacks_of(const int32_t* pages, int n, std::vector<TileMove>* moves) {
+    for (int i = 0; i < n; ++i) {
+      const int s = slot_of_page_[pages[i]];
+      if (s >= 0 && dirty_[s]) add_writebacks(s, moves);
+    }
+  }
+
   // The caller has set every gradient tile of the host pools to zero (a new
   // pass): the cached gradient tiles are forgotten without being written
   // back, and until a tile is written back again, bringing it in is a zero

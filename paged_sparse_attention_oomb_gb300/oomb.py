@@ -28,6 +28,7 @@ EXPORTED = [
     "oomb_page_reps", "oomb_select_topk", "oomb_select_topk_noalloc", "oomb_sparse_attn_fwd",
     "oomb_sparse_attn_fwd_own_reps", "oomb_sparse_attn_bwd",
     "oomb_offload_create", "oomb_offload_acquire", "oomb_offload_flush", "oomb_offload_writeback",
+    "oomb_offload_writeback_pages",
     "oomb_offload_stats", "oomb_offload_destroy", "oomb_offload_zero_grads",
     "oomb_device_status", "oomb_set_wait_limit_ns", "oomb_debug_wait_unset_flag",
     "oomb_status_string", "oomb_last_error",
@@ -97,6 +98,7 @@ def load():
         "oomb_offload_acquire": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp]),
         "oomb_offload_flush": (ctypes.c_int, [vp, i32, vp]),
         "oomb_offload_writeback": (ctypes.c_int, [vp, i32, i32, vp]),
+        "oomb_offload_writeback_pages": (ctypes.c_int, [vp, vp, i32, vp]),
         "oomb_offload_stats": (ctypes.c_int, [vp, vp]),
         "oomb_offload_zero_grads": (ctypes.c_int, [vp]),
         "oomb_offload_destroy": (None, [vp]),
@@ -553,6 +555,12 @@ class OffloadCache:
         """Write the modified gradient tiles of these pages back now."""
         _check(load().oomb_offload_writeback(self._h, first_page, n_pages, _stream(stream)))
 
+    def writeback_pages(self, pages, stream=None):
+        """Write the modified gradient tiles of these logical pages back now."""
+        pages = torch.as_tensor(list(pages), dtype=torch.int32).contiguous()
+        _check(load().oomb_offload_writeback_pages(self._h, ctypes.c_void_p(pages.data_ptr()),
+                                                   pages.numel(), _stream(stream)))
+
     def zero_grads(self):
         """Declare the host dK/dV pools zeroed (a new pass): the cached gradient
         tiles are dropped, and tiles still zero on the host are brought in as
@@ -714,6 +722,14 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
                     copy.wait_event(done[c - 1])  # slots of chunk c-1 may be reused now
                 acquire_fwd(c + 1)
     fwd_done = done[last]
+
+    def touched(c):                               # the pages chunk c reads and adds into
+        c0 = start + c * chunk_len
+        own = set(range(c0 // p, -(-(c0 + length(c)) // p)))
+        n_sel = sels[c][2]
+        return own | (set(sels[c][1][:, :n_sel].flatten().tolist()) if n_sel else set())
+    touched_first = touched(0)
+    touched_later = set().union(*(touched(c) for c in range(1, n_chunks)))
     # backward, chunks in reverse
     for c in reversed(range(n_chunks)):
         r0 = c * chunk_len
@@ -733,10 +749,14 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
                 copy.wait_event(fwd_done if c == last else done[c + 1])
                 acquire(c - 1, True, pts[(c - 1) % 2])
                 ready[c - 1] = mark()
-            # chunk c's own pages are final: no earlier chunk reads them.  (Writing
-            # back here the pages that only later chunks selected as well measured
-            # slower: the final flush shrinks, but those moves take SMs from the
-            # backward.)
+            if c == 0 and n_chunks > 1:
+                # during the last backward the link is otherwise idle: every page
+                # that the first chunk neither owns nor selected is final (the
+                # backward of chunk 1 is done), so its tiles go back now rather than
+                # in the final flush.  (Doing the same after every chunk measured
+                # slower: those moves took SMs from the backwards.)
+                cache.writeback_pages(sorted(touched_later - touched_first), copy)
+            # chunk c's own pages are final: no earlier chunk reads them
             copy.wait_event(done[c])
             cache.writeback((start + r0) // p, -(-length(c) // p), copy)
     comp.wait_stream(copy)

@@ -71,8 +71,12 @@ int main() {
     m.clear();
     d.collect_writebacks(8, 2, &m);
     CHECK(m.empty());
+    const int32_t list[3] = {2, 5, 2};          // page 2 (slot 1, head 1); 5 not cached
+    d.collect_writebacks_of(list, 3, &m);
+    CHECK(m.size() == 1 && has(m, 2, 1, 1, TileMove::kWriteGrad) && d.dirty(1) == 0u);
+    m.clear();
     d.collect_writebacks(0, -1, &m);
-    CHECK(m.size() == 2 && has(m, 1, 0, 0, TileMove::kWriteGrad) && has(m, 2, 1, 1, TileMove::kWriteGrad));
+    CHECK(m.size() == 1 && has(m, 1, 0, 0, TileMove::kWriteGrad));
     // 5. drop forgets every slot.
     d.drop();
     for (int l = 0; l < 10; ++l) CHECK(d.slot_of_page()[l] == -1);

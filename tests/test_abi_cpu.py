@@ -123,6 +123,8 @@ def test_offload_calls_refuse_a_null_handle(lib):
     assert lib.oomb_offload_zero_grads(None) == oomb.OOMB_ERR_INVALID_ARG
     assert lib.oomb_offload_flush(None, 0, None) == oomb.OOMB_ERR_INVALID_ARG
     assert lib.oomb_offload_writeback(None, 0, 1, None) == oomb.OOMB_ERR_INVALID_ARG
+    pages = (ctypes.c_int32 * 1)(0)
+    assert lib.oomb_offload_writeback_pages(None, pages, 1, None) == oomb.OOMB_ERR_INVALID_ARG
     out = (ctypes.c_int64 * 7)()
     assert lib.oomb_offload_stats(None, out) == oomb.OOMB_ERR_INVALID_ARG
 
