@@ -600,7 +600,9 @@ def chunk_recurrent_pass_offloaded(q_full, dout_full, cache: OffloadCache, chunk
     before it; in the backward, chunk c-1's acquire overlaps chunk c's
     backward, and chunk c's own pages -- final once its backward is done, since
     no earlier chunk reads them -- go back to the host during the backward of
-    chunk c-1.  O, the selections and the host dK/dV are bit-identical to
+    chunk c-1; during the last backward, every page the first chunk does not
+    touch goes back as well, so the final flush moves only the first chunk's
+    tiles.  O, the selections and the host dK/dV are bit-identical to
     chunk_recurrent_pass on resident pools (the same kernels run on bit copies
     of the same tiles, and every modified gradient tile is written back); dQ is
     equal up to the order of its fp32 atomic sums.
