@@ -42,11 +42,21 @@ struct Vec<float> {
   }
 };
 
+// L2 policy for data read exactly once: its lines are the first to be replaced,
+// so a stream does not push out lines that are still wanted (the
+// representatives just written, the scores) and mostly replaces its own lines
+// instead of writing dirty ones back while it streams.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+               : "l"(p), "l"(l2_evict_first()));
   return r;
 }
 
@@ -135,11 +145,13 @@ cudaError_t reps_dispatch(const KvDesc& kv, int first_page, int n_pages, int las
 // ---------------------------------------------------------------------------
 // Copies of 16 bytes global -> shared that stay in flight without holding
 // registers; each thread waits only for its own (commit groups), so a thread
-// that reads back exactly the slots it filled needs no barrier.
+// that reads back exactly the slots it filled needs no barrier.  The query
+// rows and the representatives are read once per call: evict-first in L2.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
-               "l"(gsrc)
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(gsrc), "l"(l2_evict_first())
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
@@ -225,6 +237,14 @@ __device__ __forceinline__ void block_bitonic_sort(V* a, int n, bool desc) {
       __syncthreads();
     }
   }
+}
+
+// Where bin b of a head's 65536-bin key histogram is stored: within each
+// window of 2048 bins, bin (hi, lo) = (b >> 6 & 31, b & 63) sits at lo * 32 +
+// hi, so neighbouring bins (which a narrow score distribution fills most)
+// fall in different 128-byte lines and their atomics do not queue on one line.
+__device__ __forceinline__ int hist_slot(uint32_t b) {
+  return static_cast<int>((b & ~2047u) | ((b & 63u) << 5) | ((b >> 6) & 31u));
 }
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -478,7 +498,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
     for (int off = L / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
     if (valid && li == 0) {
       p.scores[static_cast<long>(g) * p.num_pages + r / hkv] = sc;
-      atomicAdd(&p.hist[(static_cast<long>(g) << 16) + (order_key(sc) >> 16)], 1);
+      atomicAdd(&p.hist[(static_cast<long>(g) << 16) + hist_slot(order_key(sc) >> 16)], 1);
     }
   }
   cp_async_wait<0>();
@@ -547,14 +567,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
     __syncthreads();
     const int bw = static_cast<int>(sh_digit);
     if (w == bw) {
-      // lane l: bins [2048 bw + 64 l, +64), counted from the top (lane 31 first)
-      const int4* l4 = reinterpret_cast<const int4*>(hg + 2048 * bw + 64 * lane);
+      // lane l: bins [2048 bw + 64 l, +64), counted from the top (lane 31
+      // first); bin 64 l + y of the window is stored at 32 y + l, so the warp
+      // reads one 128-byte line per y
+      const int* hw = hg + 2048 * bw + lane;
       int cl = 0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int4 v = __ldcg(l4 + j);
-        cl += (v.x + v.y) + (v.z + v.w);
-      }
+#pragma unroll 16
+      for (int y = 0; y < 64; ++y) cl += __ldcg(hw + 32 * y);
       const int c = __shfl_sync(0xffffffffu, cl, 31 - lane);
       int x = c;
 #pragma unroll
@@ -568,8 +587,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
       const int bl = 31 - src;                    // the lane range holding the bin
       const int run0 = above_w + __shfl_sync(0xffffffffu, x - c, src);
       // that range's 64 bins, two per lane from the top
-      const int* hb = hg + 2048 * bw + 64 * bl;
-      const int c0 = __ldcg(hb + 63 - 2 * lane), c1 = __ldcg(hb + 62 - 2 * lane);
+      const int* hb = hg + 2048 * bw + bl;
+      const int c0 = __ldcg(hb + 32 * (63 - 2 * lane)), c1 = __ldcg(hb + 32 * (62 - 2 * lane));
       int y = c0 + c1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -602,49 +621,87 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
     __shared__ int n_list;
     if (tid == 0) n_list = 0;
     __syncthreads();
-    const uint32_t below = (1u << lane) - 1u;
-    constexpr int kU = 8;                         // loads in flight per thread
-    for (int base0 = 0; base0 < n_cand; base0 += kU * nt) {   // warp-uniform steps
-      float v[kU];
+    // Every score whose key has (key >> 16) >= b16 joins the list, in any
+    // order (what follows does not depend on it).  Few do, so the scan first
+    // tests a superset with two integer operations per score -- the order key
+    // without its NaN and -0 cases, against the bin's lowest key minus one --
+    // and applies the exact test only to those.
+    const uint32_t lo = b16 == 0 ? 0u : (b16 << 16) - 1u;
+    auto may_take = [&](float f) {
+      const uint32_t b = __float_as_uint(f);
+      return (b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u)) >= lo;
+    };
+    auto take = [&](float f, int i) {
+      const uint32_t key = order_key(f);
+      if ((key >> 16) >= b16) {
+        const int at = atomicAdd(&n_list, 1);
+        if (at < kSelSortMax)
+          list[at] = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
+      }
+    };
+    // 16-byte loads from the first 16-byte boundary; the scores before it and
+    // after the last whole vector one by one
+    const int h = min(n_cand, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(sc) & 15u)) & 15u) >> 2));
+    const int n4 = (n_cand - h) >> 2;
+    const int tail0 = h + 4 * n4;
+    if (tid < h) {
+      const float f = __ldcg(sc + tid);
+      if (may_take(f)) take(f, tid);
+    }
+    if (tid < n_cand - tail0) {
+      const float f = __ldcg(sc + tail0 + tid);
+      if (may_take(f)) take(f, tail0 + tid);
+    }
+    const float4* sc4 = reinterpret_cast<const float4*>(sc + h);
+    constexpr int kV = 8;                         // 16-byte loads in flight per thread
+    for (int j0 = 0; j0 < n4; j0 += kV * nt) {
+      float4 v[kV];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = base0 + tid + u * nt;
-        v[u] = i < n_cand ? __ldcg(sc + i) : 0.f;
+      for (int u = 0; u < kV; ++u) {
+        const int j = j0 + tid + u * nt;
+        v[u] = j < n4 ? __ldcg(sc4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = base0 + tid + u * nt;
-        const uint32_t key = order_key(v[u]);
-        const bool take = i < n_cand && (key >> 16) >= b16;
-        const uint32_t m = __ballot_sync(0xffffffffu, take);
-        if (m) {
-          const int leader = __ffs(m) - 1;
-          int at = 0;
-          if (lane == leader) at = atomicAdd(&n_list, __popc(m));
-          at = __shfl_sync(0xffffffffu, at, leader) + __popc(m & below);
-          if (take && at < kSelSortMax)
-            list[at] = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
+      for (int u = 0; u < kV; ++u) {
+        const int j = j0 + tid + u * nt;
+        if (j < n4 && (may_take(v[u].x) || may_take(v[u].y) || may_take(v[u].z) || may_take(v[u].w))) {
+          const int i = h + 4 * j;
+          if (may_take(v[u].x)) take(v[u].x, i);
+          if (may_take(v[u].y)) take(v[u].y, i + 1);
+          if (may_take(v[u].z)) take(v[u].z, i + 2);
+          if (may_take(v[u].w)) take(v[u].w, i + 3);
         }
       }
     }
     __syncthreads();
     if (list_n <= kSelRankMax) {
-      // entry i's place in (key descending, index ascending) order is the
+      // entry e's place in (key descending, index ascending) order is the
       // number of entries above it (the composites are distinct); the kept
-      // ones then take their place in index order the same way
-      const unsigned long long mine = tid < list_n ? list[tid] : 0ull;
+      // ones then take their place in index order the same way.  Four
+      // neighbouring threads share an entry, each counting every fourth one.
+      static_assert(4 * kSelRankMax <= kSelThreads, "four threads per ranked entry");
+      const int e = tid >> 2, part = tid & 3;
+      const bool live = e < list_n;
+      const unsigned long long mine = live ? list[e] : 0ull;
       const uint32_t my_idx = 0xFFFFFFFFu - static_cast<uint32_t>(mine & 0xFFFFFFFFull);
       int rank = 0;
-      if (tid < list_n)
-        for (int j = 0; j < list_n; ++j) rank += list[j] > mine ? 1 : 0;
-      const bool kept = tid < list_n && rank < k;
-      if (tid < list_n) idx[tid] = kept ? my_idx : 0xFFFFFFFFu;
-      __syncthreads();
-      if (kept) {
-        int pos = 0;
-        for (int j = 0; j < list_n; ++j) pos += idx[j] < my_idx ? 1 : 0;
-        out[pos] = static_cast<int32_t>(my_idx);
+      if (live) {
+#pragma unroll 4
+        for (int j = part; j < list_n; j += 4) rank += list[j] > mine ? 1 : 0;
       }
+      rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+      rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+      const bool kept = live && rank < k;
+      if (live && part == 0) idx[e] = kept ? my_idx : 0xFFFFFFFFu;
+      __syncthreads();
+      int pos = 0;
+      if (kept) {
+#pragma unroll 4
+        for (int j = part; j < list_n; j += 4) pos += idx[j] < my_idx ? 1 : 0;
+      }
+      pos += __shfl_xor_sync(0xffffffffu, pos, 1);
+      pos += __shfl_xor_sync(0xffffffffu, pos, 2);
+      if (kept && part == 0) out[pos] = static_cast<int32_t>(my_idx);
       return;
     }
     int np = 1;
