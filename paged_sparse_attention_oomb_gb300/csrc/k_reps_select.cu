@@ -210,6 +210,8 @@ constexpr size_t kSelCacheBytes =
     kSelRingBytes > 4 * kSelCacheKeys ? kSelRingBytes : 4 * static_cast<size_t>(kSelCacheKeys);
 constexpr size_t kSelListBytes = 8 * 4096 + 4 * 4096;   // the fast path's sort buffers
 constexpr size_t kSelDynSmem = kSelCacheBytes + kSelListBytes;
+static_assert(kSelRingBytes + sizeof(float4) * kSelThreads <= kSelDynSmem,
+              "the query summary's partial sums fit past the copy ring");
 static_assert(kGroupTicketIdx + (kSelMaxBlocks + kSelGroup - 1) / kSelGroup <= 64,
               "tickets fit the status block");
 
@@ -462,20 +464,39 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
     cp_async_wait<0>();
     return;
   }
-  // qbar: the group sums in group order (every CTA adds them the same way)
+  // qbar from the group sums, added the same way in every CTA: thread
+  // (s, i) adds the groups s, s + S, ... of column i in that order (all its
+  // loads in flight at once), then the S partial sums of a column are added
+  // in slice order (shared memory past the copies still in flight)
   {
     const float inv = 1.0f / (static_cast<float>(p.chunk_len) * grp);
     const float4* gs4 = reinterpret_cast<const float4*>(p.gsums);
-    for (int i = tid; i < hkv * L; i += nt) {
+    const int cols = hkv * L;                     // <= 16 * 32
+    const int S = nt / cols;                      // >= 2
+    float4* qpart = reinterpret_cast<float4*>(reinterpret_cast<char*>(ring) + kSelRingBytes);
+    const int i = tid % cols, sl = tid / cols;
+    if (sl < S) {
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < n_groups; ++c) {
+      for (int c = sl; c < n_groups; c += S) {
         const float4 v = __ldcg(gs4 + static_cast<size_t>(c) * (n_out / 4) + i);
         a.x += v.x;
         a.y += v.y;
         a.z += v.z;
         a.w += v.w;
       }
-      qs[i] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+      qpart[sl * cols + i] = a;
+    }
+    __syncthreads();
+    if (tid < cols) {
+      float4 a = qpart[tid];
+      for (int u = 1; u < S; ++u) {
+        const float4 v = qpart[u * cols + tid];
+        a.x += v.x;
+        a.y += v.y;
+        a.z += v.z;
+        a.w += v.w;
+      }
+      qs[tid] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
     }
   }
   __syncthreads();
@@ -565,15 +586,21 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelParams 
       }
     }
     __syncthreads();
-    const int bw = static_cast<int>(sh_digit);
-    if (w == bw) {
-      // lane l: bins [2048 bw + 64 l, +64), counted from the top (lane 31
-      // first); bin 64 l + y of the window is stored at 32 y + l, so the warp
-      // reads one 128-byte line per y
+    const int bw = static_cast<int>(sh_digit & 31u);
+    // lane range l: bins [2048 bw + 64 l, +64), counted from the top (lane
+    // 31 first).  Bin 64 l + y of the window is stored at 32 y + l: thread
+    // (w, lane) reads y = w and w + 32 of range lane, one load each for the
+    // whole block, and warp bw adds the 32 warps' counts in warp order.
+    int* lsum = reinterpret_cast<int*>(ring);     // [32][32]; the ring is free here
+    {
       const int* hw = hg + 2048 * bw + lane;
+      lsum[32 * w + lane] = __ldcg(hw + 32 * w) + __ldcg(hw + 32 * (w + 32));
+    }
+    __syncthreads();
+    if (w == bw) {
       int cl = 0;
-#pragma unroll 16
-      for (int y = 0; y < 64; ++y) cl += __ldcg(hw + 32 * y);
+#pragma unroll 8
+      for (int u = 0; u < 32; ++u) cl += lsum[32 * u + lane];
       const int c = __shfl_sync(0xffffffffu, cl, 31 - lane);
       int x = c;
 #pragma unroll
