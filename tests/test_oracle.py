@@ -343,6 +343,22 @@ def test_topk_invariants_and_brute_force(k):
         assert sel[g].tolist() == brute
 
 
+@pytest.mark.parametrize("k", [1, 5, 17, 29, 40])
+def test_topk_signed_zero_and_nan(k):
+    """+0 and -0 are the same score (the lower page wins) and a NaN score ranks
+    below every number (NaN pages last, lower page first): brute force with a
+    key that spells both rules out."""
+    rng = np.random.default_rng(100 + k)
+    vals = np.array([1.0, -1.0, 0.0, -0.0, np.nan], np.float32)
+    scores = rng.choice(vals, size=(2, 40))
+    for g in range(2):
+        def key(l):
+            v = float(scores[g, l])
+            return (1, 0.0, l) if math.isnan(v) else (0, -v, l)   # -(-0.0) == -(0.0)
+        brute = sorted(sorted(range(40), key=key)[:k])
+        assert oracle.select_topk(scores, k)[g].tolist() == brute
+
+
 def test_golden_tie_break():
     with open(os.path.join(GOLDEN, "tie_break_lowest_page.json")) as f:
         gj = json.load(f)

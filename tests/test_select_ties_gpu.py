@@ -140,3 +140,51 @@ def test_more_candidates_than_cached_on_chip():
     levels = _groups(50_000, 1, values, seed=9)
     top_k = int(np.sum(levels[:, 0] > 0.375)) + 17
     check_exact(constant_pages(levels, num_q_heads=2), top_k)
+
+
+def given_reps(levels, own_pages=4):
+    """Inputs of constant_pages (all-ones queries, so the group-mean query is
+    exactly 1) with representatives given directly: candidate l of KV head g
+    is levels[l, g] in every column, signed zeros and NaN included, so its
+    score is exactly D times that value on both sides."""
+    levels = np.asarray(levels, np.float64)
+    n_cand, hkv = levels.shape
+    x = constant_pages(np.zeros_like(levels), own_pages=own_pages)
+    reps64 = np.zeros((n_cand + own_pages, hkv, 128))
+    reps64[:n_cand] = levels[:, :, None]
+    reps = torch.as_tensor(reps64, dtype=torch.float32, device=DEV)
+    return x, reps, reps64
+
+
+@pytest.mark.parametrize("n_cand", [300, 700])
+@pytest.mark.parametrize("boundary", ["among_zeros", "among_nan"])
+def test_signed_zeros_tie_and_nan_ranks_last(n_cand, boundary):
+    """Scores of +0 and -0 are equal (the lower page wins between them) and a
+    NaN score never outranks a number: NaN pages are taken last, lowest index
+    first.  300 candidates keep the boundary list short (ranked by counting),
+    700 make it longer (sorted)."""
+    rng = np.random.default_rng(13 + n_cand)
+    levels = rng.choice(np.array([0.5, -0.5, 0.0, -0.0, np.nan]), size=(n_cand, 2),
+                        p=[0.35, 0.2, 0.15, 0.15, 0.15])
+    assert np.any(np.signbit(levels) & (levels == 0)), "the draw holds -0 pages"
+    x, reps, reps64 = given_reps(levels)
+    lv = levels[:, 0]
+    above, zeros, nans = int(np.sum(lv > 0)), int(np.sum(lv == 0)), int(np.sum(np.isnan(lv)))
+    top_k = above + zeros // 2 if boundary == "among_zeros" else n_cand - nans // 2
+    kv = gpu_kv(x, with_grads=False)
+    sel_g, scores_g = gpu_select(x, kv, reps, top_k)
+    sel_o, scores_o = oracle_selection(x, reps64, top_k)
+    nc = x.wl.num_candidates
+    np.testing.assert_array_equal(scores_g[:, :nc].cpu().numpy(), scores_o)   # NaN == NaN, -0 == +0
+    g = sel_g.cpu().numpy()
+    for h in range(2):
+        assert np.array_equal(g[h], sel_o[h]), (h, np.setdiff1d(g[h], sel_o[h])[:8],
+                                                np.setdiff1d(sel_o[h], g[h])[:8])
+    if boundary == "among_zeros":
+        zero_pages = np.flatnonzero(lv == 0)      # +0 and -0 pages in page order
+        assert np.array_equal(np.intersect1d(g[0], zero_pages), zero_pages[:zeros // 2])
+        assert not np.any(np.isnan(lv[g[0]]))
+    else:
+        nan_pages = np.flatnonzero(np.isnan(lv))
+        taken = top_k - (n_cand - nans)            # every number first, then NaN pages
+        assert np.array_equal(np.intersect1d(g[0], nan_pages), nan_pages[:taken])
