@@ -349,7 +349,7 @@ def test_topk_signed_zero_and_nan(k):
     below every number (NaN pages last, lower page first): brute force with a
     key that spells both rules out."""
     rng = np.random.default_rng(100 + k)
-    vals = np.array([1.0, -1.0, 0.0, -0.0, np.nan], np.float32)
+    vals = np.array([np.inf, 1.0, -1.0, -np.inf, 0.0, -0.0, np.nan], np.float32)
     scores = rng.choice(vals, size=(2, 40))
     for g in range(2):
         def key(l):

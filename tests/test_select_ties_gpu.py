@@ -159,13 +159,14 @@ def given_reps(levels, own_pages=4):
 @pytest.mark.parametrize("n_cand", [300, 700])
 @pytest.mark.parametrize("boundary", ["among_zeros", "among_nan"])
 def test_signed_zeros_tie_and_nan_ranks_last(n_cand, boundary):
-    """Scores of +0 and -0 are equal (the lower page wins between them) and a
-    NaN score never outranks a number: NaN pages are taken last, lowest index
-    first.  300 candidates keep the boundary list short (ranked by counting),
-    700 make it longer (sorted)."""
+    """Scores of +0 and -0 are equal (the lower page wins between them), +-inf
+    rank as the largest and smallest numbers, and a NaN score never outranks
+    a number: NaN pages are taken last, lowest index first.  300 candidates
+    keep the boundary list short (ranked by counting), 700 make it longer
+    (sorted)."""
     rng = np.random.default_rng(13 + n_cand)
-    levels = rng.choice(np.array([0.5, -0.5, 0.0, -0.0, np.nan]), size=(n_cand, 2),
-                        p=[0.35, 0.2, 0.15, 0.15, 0.15])
+    levels = rng.choice(np.array([np.inf, 0.5, -0.5, -np.inf, 0.0, -0.0, np.nan]),
+                        size=(n_cand, 2), p=[0.05, 0.3, 0.15, 0.05, 0.15, 0.15, 0.15])
     assert np.any(np.signbit(levels) & (levels == 0)), "the draw holds -0 pages"
     x, reps, reps64 = given_reps(levels)
     lv = levels[:, 0]
