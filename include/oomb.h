@@ -167,7 +167,7 @@ oomb_status oomb_select_topk(const void *q, int32_t num_q_heads, int32_t chunk_l
  * which every GPU that loads the library holds until the process exits.  It
  * must hold oomb_workspace_bytes(OOMB_OP_SELECT_TOPK, ...) for these shapes
  * (about 256 B + 1152 B * Hkv * D + 256 KiB * Hkv + 4 B * Hkv * num_pages,
- * e.g. up to ~157K pages at Hkv = 4, D = 128); larger requests return
+ * e.g. up to ~159K pages at Hkv = 4, D = 128); larger requests return
  * OOMB_ERR_INVALID_ARG before anything is launched.  The
  * first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  The call
